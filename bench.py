@@ -1,0 +1,384 @@
+#!/usr/bin/env python
+"""Benchmark: Maple MoE layer, batch-1 decode (route + expert FFN), on one B300.
+
+Workload (the metric's configuration): hidden 2048, 256 experts, top-8, no shared
+expert, intermediate 512; ternary experts packed 5 trits/byte with fp32 row scales;
+bf16 router [256 x 2048]; one bf16 N(0,1) token per step.  One step = route_topk +
+moe_ffn for one token on one layer.  Steps cycle over 1000 distinct seeded tokens and
+over LAYERS independently seeded layers (10.5 GB packed), so a layer's experts are
+far out of L2 when it comes round again (inputs larger than L2, no flush).
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle instead, on a
+bounded sample of the same workload.  Under torchrun with N > 1 every rank runs an
+independent replica (the path has no exchange step) and `value` sums all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+H, E, I, K_TOP = 2048, 256, 512, 8
+N_TOKENS = 1000
+LAYERS = 64
+METRIC = "ternary MoE layer tokens/s (batch-1 decode)"
+EXPERT_BYTES = 2 * I * ((H + 4) // 5) + H * ((I + 4) // 5) + 4 * (2 * I + H)  # 643,072
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- inputs
+
+def build_layers(maple, synth, n_layers: int, seed0: int = 1000):
+    """n_layers independent Maple layers: bf16 N(0,0.02) experts drawn on the GPU and
+    packed by maple_ternarize_pack (untimed set-up), bf16 router weights."""
+    layers = []
+    Bh, Bi = (H + 4) // 5, (I + 4) // 5
+    for l in range(n_layers):
+        w = synth.expert_weights(E, H, I, seed=seed0 + l, device="cuda")
+        gate = torch.empty((E, I, Bh), dtype=torch.uint8, device="cuda")
+        up = torch.empty((E, I, Bh), dtype=torch.uint8, device="cuda")
+        down = torch.empty((E, H, Bi), dtype=torch.uint8, device="cuda")
+        sg = torch.empty((E, I), device="cuda")
+        su = torch.empty((E, I), device="cuda")
+        sd = torch.empty((E, H), device="cuda")
+        maple.maple_ternarize_pack(w["gate"].view(E * I, H), gate.view(E * I, Bh), sg.view(-1))
+        maple.maple_ternarize_pack(w["up"].view(E * I, H), up.view(E * I, Bh), su.view(-1))
+        maple.maple_ternarize_pack(w["down"].view(E * H, I), down.view(E * H, Bi), sd.view(-1))
+        del w
+        router = synth.router_weights(E, H, seed=seed0 + l, device="cuda")
+        layers.append((maple.Experts(gate, up, down, sg, su, sd, clamp=7.0), router))
+    torch.cuda.synchronize()
+    return layers
+
+
+# ------------------------------------------------------------------------ GPU arm
+
+def run_gpu(args, world, rank, local):
+    from ternary_weight_moe_02_b300 import maple, synth
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    n_layers = args.layers
+    layers = build_layers(maple, synth, n_layers, seed0=1000 + 97 * rank)
+    x_all = synth.tokens(N_TOKENS, H, seed=7 + rank, device="cuda")
+    logits = torch.empty((1, E), device=dev)
+    idx = torch.empty((1, K_TOP), dtype=torch.int32, device=dev)
+    wts = torch.empty((1, K_TOP), device=dev)
+    y = torch.empty((1, H), device=dev)
+    ws = torch.empty(maple.maple_moe_ffn_workspace_size(1, K_TOP, layers[0][0]), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, s, events=None):
+        ex, router = layers[i % n_layers]
+        x = x_all[i % N_TOKENS: i % N_TOKENS + 1]
+        maple.maple_route_topk(x, router, None, K_TOP, logits, idx, wts, stream=s)
+        if events is not None:
+            events[0].record(s)
+        maple.maple_moe_ffn(ex, x, idx, wts, y, ws, stream=s)
+        if events is not None:
+            events[1].record(s)
+
+    chunk = max(1, min(args.chunk, args.steps))
+
+    def capture(n_steps, start):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for i in range(3):  # warm the launch path before capture
+                step(start + i, stream)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n_steps):
+                    step(start + i, stream)
+        return g
+
+    g_chunk = capture(chunk, 0)
+    rem = args.steps % chunk
+    g_rem = capture(rem, 0) if rem else None
+    g_warm = capture(max(1, args.warmup), 0)
+    reps = args.steps // chunk
+
+    # graphs replay on the current stream: make it the one the events are recorded on
+    with torch.cuda.stream(stream):
+        g_warm.replay()
+    torch.cuda.synchronize()
+    _barrier(world)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
+        torch.cuda.synchronize()
+        _barrier(world)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(reps):
+                g_chunk.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            ev1.record(stream)
+        ev1.synchronize()
+        torch.cuda.synchronize()
+        _barrier(world)
+    elapsed_s = ev0.elapsed_time(ev1) / 1e3
+    elapsed_max = _max_over_ranks(elapsed_s, world)
+    value = world * args.steps / elapsed_max
+    launches = args.steps * 4  # route_logits, route_select, ffn_gateup, ffn_down
+
+    # Roofline pass: the same steps with events around each moe_ffn call (graph-captured),
+    # giving the live average duration of the dominant launch pair.
+    n_roof = min(args.steps, 2000)
+    pairs = [(torch.cuda.Event(enable_timing=True, external=True),
+              torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n_roof)]
+    g_roof = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g_roof, stream=stream):
+            for i in range(n_roof):
+                step(i, stream, pairs[i])
+    with torch.cuda.stream(stream):
+        g_roof.replay()
+    torch.cuda.synchronize()
+    ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
+    peak, peak_kind = _peaks()
+    alg_bytes = K_TOP * EXPERT_BYTES  # 8 distinct experts per batch-1 token
+    achieved = alg_bytes / (ffn_ms / 1e3) / 1e9
+
+    # End-to-end through the public API with host buffers: pinned token -> device, route,
+    # FFN, y -> pinned host, every step.
+    n_e2e = min(args.steps, 2000)
+    x_host = x_all[:N_TOKENS].cpu().pin_memory()
+    y_host = torch.empty((1, H), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty((1, H), dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            x_dev.copy_(x_host[i:i + 1], non_blocking=True)
+            ex, router = layers[i % n_layers]
+            maple.maple_route_topk(x_dev, router, None, K_TOP, logits, idx, wts, stream=stream)
+            maple.maple_moe_ffn(ex, x_dev, idx, wts, y, ws, stream=stream)
+            y_host.copy_(y, non_blocking=True)
+        stream.synchronize()
+        e0.record(stream)
+        for i in range(n_e2e):
+            x_dev.copy_(x_host[i % N_TOKENS: i % N_TOKENS + 1], non_blocking=True)
+            ex, router = layers[i % n_layers]
+            maple.maple_route_topk(x_dev, router, None, K_TOP, logits, idx, wts, stream=stream)
+            maple.maple_moe_ffn(ex, x_dev, idx, wts, y, ws, stream=stream)
+            y_host.copy_(y, non_blocking=True)
+        e1.record(stream)
+    e1.synchronize()
+    e2e_s = _max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    e2e_value = world * n_e2e / e2e_s
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_max * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+        "data": "synthetic (seeded bf16 N(0,0.02) weights, ternarized and packed on the GPU)",
+        "config": {"workload": "maple_moe_layer_decode_b1", "hidden": H, "experts": E,
+                   "top_k": K_TOP, "moe_intermediate": I, "tokens_per_step": 1,
+                   "distinct_tokens": N_TOKENS, "layers_cycled": n_layers,
+                   "packed_gb": round(n_layers * E * EXPERT_BYTES / 1e9, 2),
+                   "l2": "inputs larger than L2 (layers cycled; no flush)",
+                   "graph": f"CUDA graph of {chunk} steps replayed", "parallelism": f"replicas{world}"},
+        "gpu_launches": launches,
+        "roofline": {"bound": "hbm", "kernel": "moe_ffn (ffn_gateup + ffn_down launches)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                     "alg_bytes_per_launch": alg_bytes, "avg_launch_us": ffn_ms * 1e3,
+                     "traffic": None},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "steps": n_e2e,
+                "h2d_bytes_per_step": H * 2, "d2h_bytes_per_step": H * 4},
+        "clocks": clocks.summary(),
+    }
+    return result
+
+
+# ------------------------------------------------------------------- CPU (oracle) arm
+
+def oracle_sample(n_tokens: int, seed_layer: int = 1000):
+    """Oracle route + FFN on n_tokens of layer 0 (bf16 weights drawn on the GPU when one
+    is present, else on the CPU; the oracle packs the experts it needs, untimed).
+    Returns (tokens/s, seconds)."""
+    import oracle
+    from ternary_weight_moe_02_b300 import synth
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = synth.expert_weights(E, H, I, seed=seed_layer, device=gen_dev)
+    router = synth.bf16_bits(synth.router_weights(E, H, seed=seed_layer, device=gen_dev))
+    x = synth.bf16_bits(synth.tokens(N_TOKENS, H, seed=7, device=gen_dev))[:n_tokens]
+    _, idx0, _ = oracle.route(x, router, None, K_TOP)
+    packed = {}
+    for name, rows, K in (("gate", I, H), ("up", I, H), ("down", H, I)):
+        packed[name] = np.full((E, rows, (K + 4) // 5), 121, np.uint8)
+        packed["s_" + name] = np.zeros((E, rows), np.float32)
+        for e in sorted(set(idx0.reshape(-1).tolist())):
+            p, s = oracle.ternarize_pack(synth.bf16_bits(w[name][e]))
+            packed[name][e], packed["s_" + name][e] = p, s
+    del w
+    t0 = time.perf_counter()
+    for t in range(n_tokens):
+        _, idx, wt = oracle.route(x[t:t + 1], router, None, K_TOP)
+        oracle.moe_ffn(packed["gate"], packed["up"], packed["down"], packed["s_gate"],
+                       packed["s_up"], packed["s_down"], x[t:t + 1], idx, wt)
+    dt = time.perf_counter() - t0
+    return n_tokens / dt, dt
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    per_step = []
+    for _ in range(args.warmup):
+        oracle_sample(1)
+    for _ in range(args.steps):
+        v, dt = oracle_sample(args.ref_tokens)
+        per_step.append(dt / args.ref_tokens)
+    value = 1.0 / statistics.mean(per_step)
+    sample = f"{args.ref_tokens} tokens of one 256-expert layer per step (route + FFN, oracle)"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": statistics.mean(per_step) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "maple_moe_layer_decode_b1", "hidden": H, "experts": E,
+                   "top_k": K_TOP, "moe_intermediate": I, "tokens_per_step": 1},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample, "host_cpus": os.cpu_count()},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=1000)
+    ap.add_argument("--impl", default="maple", choices=["maple", "reference"])
+    ap.add_argument("--layers", type=int, default=LAYERS)
+    ap.add_argument("--chunk", type=int, default=1000, help="steps per captured graph")
+    ap.add_argument("--ref-tokens", type=int, default=4, help="oracle tokens per reference step")
+    ap.add_argument("--cpu-tokens", type=int, default=40, help="oracle tokens for cpu_baseline")
+    args = ap.parse_args()
+    world, rank, local = _dist()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        out = run_reference(args, world, rank)
+    else:
+        out = run_gpu(args, world, rank, local)
+        if rank == 0 and world == 1 and args.cpu_tokens > 0:
+            v, dt = oracle_sample(args.cpu_tokens)
+            out["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                   "sample": f"{args.cpu_tokens} tokens of one 256-expert layer "
+                                             f"(route + FFN, single-threaded C, {dt:.1f} s)",
+                                   "host_cpus": os.cpu_count()}
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

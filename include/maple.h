@@ -1,0 +1,168 @@
+/*
+ * maple.h -- C-ABI of libmaple.so: the ternary mixture-of-experts FFN step of
+ * DeepGrove's Maple-Preview on one NVIDIA B300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ *  - Every call returns an int status: MAPLE_OK (0) or a negative MAPLE_ERR_* code.
+ *    On error nothing has been launched, except for MAPLE_ERR_CUDA, which reports a
+ *    failed launch.  maple_last_error() gives a one-line reason (per host thread).
+ *  - Array arguments are DEVICE pointers owned by the caller; the library never
+ *    allocates, frees or keeps them.  bf16 arrays are passed as uint16_t bit
+ *    patterns.  Scratch memory comes from a caller-provided workspace whose size is
+ *    given by the matching *_workspace_size call.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  All work is
+ *    asynchronous and ordered on that stream; the host never synchronises.  Errors
+ *    raised while kernels run surface at the caller's next synchronisation.
+ *  - Kernels are launched with programmatic dependent launch: each one waits for
+ *    the preceding work on the stream before it touches memory that work produced.
+ *  - Sizes of zero are valid no-ops where stated.  Inputs must be finite.
+ *
+ * Packed ternary format (shared by every call)
+ *  A weight matrix [rows x K] is stored as rows of ceil(K/5) bytes, row-major, with
+ *  no padding between rows.  Byte b of row r holds the trits q of columns
+ *  5b .. 5b+4 as sum_i (q_{5b+i} + 1) * 3^i (column 5b is the least significant
+ *  base-3 digit); columns at or past K are trit 0.  Codes 243..255 are invalid.
+ *  One fp32 scale per row: the dequantized weight is q * s.
+ *  ("Maple-Preview: a 20B reasoning model where 97% of the weights are -1, 0, or +1",
+ *  sections "The claim, verified from the bytes" and "The 5.31 GB claim reconciles":
+ *  -s/0/+s per output row, five trits per byte since 3^5 = 243 <= 256.)
+ */
+#ifndef MAPLE_H
+#define MAPLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MAPLE_API __attribute__((visibility("default")))
+#else
+#define MAPLE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MAPLE_OK 0
+#define MAPLE_ERR_INVALID_ARG (-1)       /* null pointer, negative size, k out of range */
+#define MAPLE_ERR_UNSUPPORTED_SHAPE (-2) /* a size beyond the limits stated per call */
+#define MAPLE_ERR_MISALIGNED (-3)        /* a pointer that breaks the stated alignment */
+#define MAPLE_ERR_CUDA (-4)              /* a CUDA launch or attribute call failed */
+#define MAPLE_ERR_TIMEOUT (-5)           /* reserved: a bounded device wait gave up */
+#define MAPLE_ERR_BAD_CODE (-6)          /* packed byte >= 243 (reported by maple_unpack) */
+#define MAPLE_ERR_WORKSPACE (-7)         /* workspace missing or smaller than required */
+
+/* Expert weights of one MoE layer, all device pointers, 16-byte aligned.
+ *   gate, up : [E][I][ceil(H/5)] packed bytes   s_gate, s_up : [E][I] fp32
+ *   down     : [E][H][ceil(I/5)] packed bytes   s_down       : [E][H] fp32
+ * clamp: bound of the activation clamps of the shipped forward (7.0f for Maple;
+ * INFINITY gives plain SwiGLU).  Must be > 0. */
+typedef struct maple_experts {
+    const uint8_t* gate;
+    const uint8_t* up;
+    const uint8_t* down;
+    const float* s_gate;
+    const float* s_up;
+    const float* s_down;
+    int32_t E;
+    int32_t H;
+    int32_t I;
+    float clamp;
+} maple_experts;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+MAPLE_API int maple_version(void);
+
+/* Static string naming a status code. */
+MAPLE_API const char* maple_status_string(int status);
+
+/* Reason for the last non-OK status returned on this host thread ("" if none). */
+MAPLE_API const char* maple_last_error(void);
+
+/*
+ * Absmean ternarization + 5-trit packing of a bf16 row-major matrix W [rows x K].
+ * Per row: s = (1/K) * sum_j |w_j| (fp32), q_j = clamp(round(w_j / s), -1, 1) with
+ * round-half-to-even, i.e. q_j = sign(w_j) if |w_j| > s/2 else 0; s = 0 gives all 0.
+ * ("Maple-Preview ...", section "The claim, verified from the bytes": rows are
+ * exactly -s, 0, +s, the BitNet b1.58 absmean shape; "The 5.31 GB claim
+ * reconciles": five trits per byte.)
+ *   W      : [rows][K] bf16, 2-byte aligned (16-byte aligned with K % 8 == 0 takes
+ *            the vector path)
+ *   packed : [rows][ceil(K/5)] bytes, written
+ *   scales : [rows] fp32, written
+ * Limits: rows >= 0 (0 is a no-op), 1 <= K <= 2^24.
+ */
+MAPLE_API int maple_ternarize_pack(const uint16_t* W, int64_t rows, int64_t K, uint8_t* packed,
+                         float* scales, void* stream);
+
+/*
+ * Dequantize packed rows back to fp32: W_out[r][j] = q_rj * s_r (inverse of the
+ * packing above; a test and inspection helper, not on the hot path).
+ *   packed : [rows][ceil(K/5)], scales : [rows], W_out : [rows][K] fp32 (written)
+ *   bad_codes : optional device int32 counter; the kernel adds the number of bytes
+ *               >= 243 it met (those decode as five zero trits).  May be NULL.
+ * Limits: rows >= 0, K >= 1.
+ */
+MAPLE_API int maple_unpack(const uint8_t* packed, const float* scales, int64_t rows, int64_t K,
+                 float* W_out, int32_t* bad_codes, void* stream);
+
+/*
+ * Full-precision router: logits = x Wr^T (+ bias) in fp32, top-k per token,
+ * softmax over the k selected.
+ * ("Maple-Preview ...", section "The claim, verified from the bytes": the router is
+ * kept in full precision and picks 8 of 256 experts from the logit margin;
+ * "IA de 20B Rodando a 120 tok/s no iPhone", section "256 experts, 8 ativos".)
+ *   x      : [T][H] bf16, 16-byte aligned      Wr : [E][H] bf16, 16-byte aligned
+ *   bias   : [E] fp32 or NULL
+ *   logits : [T][E] fp32, written (also the intermediate between the two kernels)
+ *   idx    : [T][k] int32, written: expert ids by descending logit, ties to the
+ *            lower id
+ *   w      : [T][k] fp32, written: exp(l_i - l_0) / sum_j exp(l_j - l_0)
+ * Limits: T >= 0 (0 is a no-op), 1 <= H <= 65536, 1 <= E <= 1024, 1 <= k <= min(E, 32).
+ */
+MAPLE_API int maple_route_topk(const uint16_t* x, const uint16_t* Wr, const float* bias, int32_t T,
+                     int32_t H, int32_t E, int32_t k, float* logits, int32_t* idx, float* w,
+                     void* stream);
+
+/*
+ * Token-to-expert grouping of the T*k routing slots (slot s = t*k + i).
+ *   idx     : [T][k] int32; ids outside [0, E) are left out of every group
+ *   counts  : [E] int32, written: slots routed to each expert
+ *   offsets : [E+1] int32, written: exclusive prefix sum of counts
+ *   perm    : [T*k] int32, written: perm[offsets[e] .. offsets[e+1]) lists the
+ *             slots of expert e in increasing slot order (stable)
+ * Limits: T >= 0, 1 <= k, T*k <= 2^24, 1 <= E <= 1024.
+ */
+MAPLE_API int maple_group_tokens(const int32_t* idx, int32_t T, int32_t k, int32_t E, int32_t* counts,
+                       int32_t* offsets, int32_t* perm, void* stream);
+
+/* Bytes of workspace maple_moe_ffn needs for T tokens with k slots each. */
+MAPLE_API size_t maple_moe_ffn_workspace_size(int32_t T, int32_t k, const maple_experts* ex);
+
+/*
+ * The expert FFN with weighted combine, for T tokens routed to k experts each:
+ *   y_t = sum_{i<k} w[t][i] * down_e( silu(min(gate_e x_t, clamp)) * clamp(up_e x_t) )
+ * with e = idx[t][i]; a weight 0 is skipped, +1 adds, -1 subtracts; each row's scale
+ * is applied once to its sum.  The k terms are added in order i = 0..k-1 (fixed
+ * order: the result is deterministic).
+ * ("Maple-Preview ...", section "The shipped code does no quantization": the
+ * MapleMLP forward with its clamps; "IA de 20B ...", section "Pesos ternarios":
+ * skip / add / subtract.)
+ *   ex  : expert weights (see maple_experts)
+ *   x   : [T][H] bf16, 16-byte aligned
+ *   idx : [T][k] int32 (ids outside [0, E) contribute 0)   w : [T][k] fp32
+ *   y   : [T][H] fp32, written
+ *   ws  : device workspace of at least maple_moe_ffn_workspace_size(T, k, ex) bytes,
+ *         16-byte aligned; contents on entry are ignored
+ * Limits: T >= 0 (0 is a no-op), 1 <= k <= 64, T*k <= 2^24, 1 <= E <= 1024,
+ *         1 <= H <= 2080, 1 <= I <= 2080.
+ */
+MAPLE_API int maple_moe_ffn(const maple_experts* ex, const uint16_t* x, const int32_t* idx,
+                  const float* w, int32_t T, int32_t k, float* y, void* ws, size_t ws_bytes,
+                  void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAPLE_H */

@@ -1,0 +1,200 @@
+// C-ABI entry points of libmaple.so (declared in include/maple.h): argument
+// validation, status codes and per-thread error text, then the kernel launches.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/maple.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int status, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int ok() {
+    g_last_error[0] = '\0';
+    return MAPLE_OK;
+}
+
+int cuda_fail(cudaError_t err, const char* what) {
+    cudaGetLastError();  // clear the sticky-free launch error so later calls start clean
+    return fail(MAPLE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));
+}
+
+bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+int get_device(maple::DeviceInfo* dev, const char* what) {
+    cudaError_t err = maple::device_info(dev);
+    if (err != cudaSuccess) return cuda_fail(err, what);
+    return MAPLE_OK;
+}
+
+}  // namespace
+
+namespace maple {
+
+cudaError_t device_info(DeviceInfo* info) {
+    static int cached_sm[128];
+    static size_t cached_smem[128];
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    if (cached_sm[dev] == 0) {
+        int sm = 0, smem = 0;
+        err = cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev);
+        if (err != cudaSuccess) return err;
+        err = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (err != cudaSuccess) return err;
+        cached_smem[dev] = (size_t)smem;
+        cached_sm[dev] = sm;
+    }
+    info->device = dev;
+    info->sm_count = cached_sm[dev];
+    info->smem_optin = cached_smem[dev];
+    return cudaSuccess;
+}
+
+}  // namespace maple
+
+extern "C" {
+
+int maple_version(void) { return 100; }
+
+const char* maple_status_string(int status) {
+    switch (status) {
+        case MAPLE_OK: return "MAPLE_OK";
+        case MAPLE_ERR_INVALID_ARG: return "MAPLE_ERR_INVALID_ARG";
+        case MAPLE_ERR_UNSUPPORTED_SHAPE: return "MAPLE_ERR_UNSUPPORTED_SHAPE";
+        case MAPLE_ERR_MISALIGNED: return "MAPLE_ERR_MISALIGNED";
+        case MAPLE_ERR_CUDA: return "MAPLE_ERR_CUDA";
+        case MAPLE_ERR_TIMEOUT: return "MAPLE_ERR_TIMEOUT";
+        case MAPLE_ERR_BAD_CODE: return "MAPLE_ERR_BAD_CODE";
+        case MAPLE_ERR_WORKSPACE: return "MAPLE_ERR_WORKSPACE";
+        default: return "MAPLE_ERR_UNKNOWN";
+    }
+}
+
+const char* maple_last_error(void) { return g_last_error; }
+
+int maple_ternarize_pack(const uint16_t* W, int64_t rows, int64_t K, uint8_t* packed,
+                         float* scales, void* stream) {
+    if (rows < 0 || K < 1) return fail(MAPLE_ERR_INVALID_ARG, "ternarize_pack: rows=%lld K=%lld", (long long)rows, (long long)K);
+    if (K > (int64_t(1) << 24)) return fail(MAPLE_ERR_UNSUPPORTED_SHAPE, "ternarize_pack: K=%lld > 2^24", (long long)K);
+    if (rows == 0) return ok();
+    if (!W || !packed || !scales) return fail(MAPLE_ERR_INVALID_ARG, "ternarize_pack: null pointer");
+    if (!aligned(W, 2) || !aligned(scales, 4)) return fail(MAPLE_ERR_MISALIGNED, "ternarize_pack: W needs 2-byte and scales 4-byte alignment");
+    maple::DeviceInfo dev;
+    if (int st = get_device(&dev, "ternarize_pack")) return st;
+    cudaError_t err = maple::launch_ternarize_pack(W, rows, K, packed, scales, (cudaStream_t)stream, dev);
+    if (err != cudaSuccess) return cuda_fail(err, "ternarize_pack launch");
+    return ok();
+}
+
+int maple_unpack(const uint8_t* packed, const float* scales, int64_t rows, int64_t K,
+                 float* W_out, int32_t* bad_codes, void* stream) {
+    if (rows < 0 || K < 1) return fail(MAPLE_ERR_INVALID_ARG, "unpack: rows=%lld K=%lld", (long long)rows, (long long)K);
+    if (rows == 0) return ok();
+    if (!packed || !scales || !W_out) return fail(MAPLE_ERR_INVALID_ARG, "unpack: null pointer");
+    if (!aligned(scales, 4) || !aligned(W_out, 4) || !aligned(bad_codes, 4)) return fail(MAPLE_ERR_MISALIGNED, "unpack: fp32/int32 arrays need 4-byte alignment");
+    maple::DeviceInfo dev;
+    if (int st = get_device(&dev, "unpack")) return st;
+    cudaError_t err = maple::launch_unpack(packed, scales, rows, K, W_out, bad_codes, (cudaStream_t)stream, dev);
+    if (err != cudaSuccess) return cuda_fail(err, "unpack launch");
+    return ok();
+}
+
+int maple_route_topk(const uint16_t* x, const uint16_t* Wr, const float* bias, int32_t T,
+                     int32_t H, int32_t E, int32_t k, float* logits, int32_t* idx, float* w,
+                     void* stream) {
+    if (T < 0 || H < 1 || E < 1 || k < 1 || k > E) return fail(MAPLE_ERR_INVALID_ARG, "route_topk: T=%d H=%d E=%d k=%d", T, H, E, k);
+    if (H > 65536 || E > 1024 || k > 32) return fail(MAPLE_ERR_UNSUPPORTED_SHAPE, "route_topk: H=%d (<=65536) E=%d (<=1024) k=%d (<=32)", H, E, k);
+    if (T == 0) return ok();
+    if (!x || !Wr || !logits || !idx || !w) return fail(MAPLE_ERR_INVALID_ARG, "route_topk: null pointer");
+    if (!aligned(x, 16) || !aligned(Wr, 16)) return fail(MAPLE_ERR_MISALIGNED, "route_topk: x and Wr need 16-byte alignment");
+    if (!aligned(bias, 4) || !aligned(logits, 4) || !aligned(idx, 4) || !aligned(w, 4)) return fail(MAPLE_ERR_MISALIGNED, "route_topk: fp32/int32 arrays need 4-byte alignment");
+    maple::DeviceInfo dev;
+    if (int st = get_device(&dev, "route_topk")) return st;
+    cudaError_t err = maple::launch_route_topk(x, Wr, bias, T, H, E, k, logits, idx, w, (cudaStream_t)stream, dev);
+    if (err != cudaSuccess) return cuda_fail(err, "route_topk launch");
+    return ok();
+}
+
+int maple_group_tokens(const int32_t* idx, int32_t T, int32_t k, int32_t E, int32_t* counts,
+                       int32_t* offsets, int32_t* perm, void* stream) {
+    if (T < 0 || k < 1 || E < 1) return fail(MAPLE_ERR_INVALID_ARG, "group_tokens: T=%d k=%d E=%d", T, k, E);
+    if (E > 1024 || (int64_t)T * k > (int64_t(1) << 24)) return fail(MAPLE_ERR_UNSUPPORTED_SHAPE, "group_tokens: E=%d (<=1024) T*k=%lld (<=2^24)", E, (long long)T * k);
+    if (!counts || !offsets) return fail(MAPLE_ERR_INVALID_ARG, "group_tokens: null pointer");
+    if (T > 0 && (!idx || !perm)) return fail(MAPLE_ERR_INVALID_ARG, "group_tokens: null pointer");
+    if (!aligned(idx, 4) || !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(perm, 4)) return fail(MAPLE_ERR_MISALIGNED, "group_tokens: int32 arrays need 4-byte alignment");
+    maple::DeviceInfo dev;
+    if (int st = get_device(&dev, "group_tokens")) return st;
+    cudaError_t err = maple::launch_group_tokens(idx, T * k, k, E, counts, offsets, perm, nullptr, nullptr, (cudaStream_t)stream, dev);
+    if (err != cudaSuccess) return cuda_fail(err, "group_tokens launch");
+    return ok();
+}
+
+size_t maple_moe_ffn_workspace_size(int32_t T, int32_t k, const maple_experts* ex) {
+    if (!ex || T < 0 || k < 1 || ex->E < 1 || ex->I < 1) return 0;
+    return maple::ffn_workspace_layout(T, k, ex->E, ex->I).total;
+}
+
+int maple_moe_ffn(const maple_experts* ex, const uint16_t* x, const int32_t* idx,
+                  const float* w, int32_t T, int32_t k, float* y, void* ws, size_t ws_bytes,
+                  void* stream) {
+    if (!ex) return fail(MAPLE_ERR_INVALID_ARG, "moe_ffn: null experts");
+    const int E = ex->E, H = ex->H, I = ex->I;
+    if (T < 0 || k < 1 || E < 1 || H < 1 || I < 1) return fail(MAPLE_ERR_INVALID_ARG, "moe_ffn: T=%d k=%d E=%d H=%d I=%d", T, k, E, H, I);
+    if (!(ex->clamp > 0.f)) return fail(MAPLE_ERR_INVALID_ARG, "moe_ffn: clamp must be > 0 (INFINITY for none)");
+    if (k > 64 || E > 1024 || H > 2080 || I > 2080 || (int64_t)T * k > (int64_t(1) << 24))
+        return fail(MAPLE_ERR_UNSUPPORTED_SHAPE, "moe_ffn: k=%d (<=64) E=%d (<=1024) H=%d (<=2080) I=%d (<=2080) T*k=%lld (<=2^24)", k, E, H, I, (long long)T * k);
+    if (T == 0) return ok();
+    if (!ex->gate || !ex->up || !ex->down || !ex->s_gate || !ex->s_up || !ex->s_down || !x || !idx || !w || !y)
+        return fail(MAPLE_ERR_INVALID_ARG, "moe_ffn: null pointer");
+    if (!aligned(ex->gate, 16) || !aligned(ex->up, 16) || !aligned(ex->down, 16) || !aligned(ex->s_gate, 16) ||
+        !aligned(ex->s_up, 16) || !aligned(ex->s_down, 16) || !aligned(x, 16) || !aligned(ws, 16))
+        return fail(MAPLE_ERR_MISALIGNED, "moe_ffn: packed weights, scales, x and ws need 16-byte alignment");
+    if (!aligned(idx, 4) || !aligned(w, 4) || !aligned(y, 4)) return fail(MAPLE_ERR_MISALIGNED, "moe_ffn: idx, w, y need 4-byte alignment");
+    const maple::FfnWorkspaceLayout L = maple::ffn_workspace_layout(T, k, E, I);
+    if (!ws || ws_bytes < L.total) return fail(MAPLE_ERR_WORKSPACE, "moe_ffn: workspace %zu bytes < %zu needed", ws_bytes, L.total);
+    maple::DeviceInfo dev;
+    if (int st = get_device(&dev, "moe_ffn")) return st;
+    char* base = static_cast<char*>(ws);
+    maple::FfnArgs a;
+    a.gate = ex->gate;
+    a.up = ex->up;
+    a.down = ex->down;
+    a.s_gate = ex->s_gate;
+    a.s_up = ex->s_up;
+    a.s_down = ex->s_down;
+    a.E = E;
+    a.H = H;
+    a.I = I;
+    a.clamp = ex->clamp;
+    a.x = x;
+    a.idx = idx;
+    a.w = w;
+    a.T = T;
+    a.k = k;
+    a.y = y;
+    a.counts = reinterpret_cast<int32_t*>(base + L.counts);
+    a.offsets = reinterpret_cast<int32_t*>(base + L.offsets);
+    a.perm = reinterpret_cast<int32_t*>(base + L.perm);
+    a.active = reinterpret_cast<int32_t*>(base + L.active);
+    a.n_active = reinterpret_cast<int32_t*>(base + L.n_active);
+    a.h = reinterpret_cast<float*>(base + L.h);
+    cudaError_t err = maple::launch_moe_ffn(a, (cudaStream_t)stream, dev);
+    if (err != cudaSuccess) return cuda_fail(err, "moe_ffn launch");
+    return ok();
+}
+
+}  // extern "C"

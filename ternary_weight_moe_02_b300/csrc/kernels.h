@@ -1,0 +1,66 @@
+// Internal launchers of libmaple (C++ linkage; the public C-ABI is include/maple.h).
+// Each returns the cudaError_t of its launch(es); arguments are already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace maple {
+
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    size_t smem_optin;
+};
+cudaError_t device_info(DeviceInfo* info);
+
+cudaError_t launch_ternarize_pack(const uint16_t* W, int64_t rows, int64_t K, uint8_t* packed,
+                                  float* scales, cudaStream_t stream, const DeviceInfo& dev);
+
+cudaError_t launch_unpack(const uint8_t* packed, const float* scales, int64_t rows, int64_t K,
+                          float* W_out, int32_t* bad_codes, cudaStream_t stream,
+                          const DeviceInfo& dev);
+
+cudaError_t launch_route_topk(const uint16_t* x, const uint16_t* Wr, const float* bias, int T,
+                              int H, int E, int k, float* logits, int32_t* idx, float* w,
+                              cudaStream_t stream, const DeviceInfo& dev);
+
+// Grouping with optional outputs used by the FFN: `active` lists the experts with a
+// non-zero count in increasing id order and `n_active` receives their number.
+cudaError_t launch_group_tokens(const int32_t* idx, int S, int k, int E, int32_t* counts,
+                                int32_t* offsets, int32_t* perm, int32_t* active,
+                                int32_t* n_active, cudaStream_t stream, const DeviceInfo& dev);
+size_t group_tokens_smem_bytes(int E);
+
+struct FfnArgs {
+    const uint8_t* gate;
+    const uint8_t* up;
+    const uint8_t* down;
+    const float* s_gate;
+    const float* s_up;
+    const float* s_down;
+    int E, H, I;
+    float clamp;
+    const uint16_t* x;
+    const int32_t* idx;
+    const float* w;
+    int T, k;
+    float* y;
+    // workspace views
+    int32_t* counts;   // [E]
+    int32_t* offsets;  // [E+1]
+    int32_t* perm;     // [T*k]
+    int32_t* active;   // [E]
+    int32_t* n_active; // [1]
+    float* h;          // [T*k][I]
+};
+
+struct FfnWorkspaceLayout {
+    size_t counts, offsets, perm, active, n_active, h, total;
+};
+FfnWorkspaceLayout ffn_workspace_layout(int T, int k, int E, int I);
+
+cudaError_t launch_moe_ffn(const FfnArgs& a, cudaStream_t stream, const DeviceInfo& dev);
+
+}  // namespace maple

@@ -1,0 +1,152 @@
+// Full-precision MoE router: bf16 GEMV/GEMM to fp32 logits, top-k, softmax over
+// the k selected.
+//
+// "Maple-Preview: a 20B reasoning model where 97% of the weights are -1, 0, or +1",
+// section "The claim, verified from the bytes": the router stays in full precision
+// and picks 8 of 256 experts from the margin between logits.
+//
+// Kernel 1 (logits): one warp per expert row, a tile of up to 8 tokens per CTA
+// column, so each router row is read once per token tile.  bf16 x bf16 products are
+// exact in fp32; each lane accumulates H/32 products with FMA in column order, then a
+// butterfly combines the lanes (depth H/32 + 5 additions).
+// Kernel 2 (select): one warp per token; k rounds of warp arg-max (ties to the lower
+// expert id), then softmax of the k winners in fp32.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace maple {
+
+namespace {
+
+constexpr int kRouteWarps = 4;   // expert rows per CTA
+constexpr int kRouteTokens = 8;  // tokens per CTA
+
+__global__ void __launch_bounds__(kRouteWarps * 32)
+    route_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ Wr,
+                        const float* __restrict__ bias, int T, int H, int E,
+                        float* __restrict__ logits, int vec) {
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * kRouteWarps + warp;
+    const int t0 = blockIdx.y * kRouteTokens;
+    if (e >= E) return;
+    const int nt = min(kRouteTokens, T - t0);
+    float acc[kRouteTokens];
+#pragma unroll
+    for (int t = 0; t < kRouteTokens; ++t) acc[t] = 0.f;
+    const uint16_t* wr = Wr + (int64_t)e * H;
+    if (vec) {
+        const int n8 = H >> 3;
+        const uint4* w4 = reinterpret_cast<const uint4*>(wr);
+        for (int c = lane; c < n8; c += 32) {
+            const uint4 wv = ldg_nc_v4(w4 + c);
+            const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
+                                 bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
+#pragma unroll
+            for (int t = 0; t < kRouteTokens; ++t) {
+                if (t < nt) {
+                    const uint4 xv =
+                        ldg_nc_v4(reinterpret_cast<const uint4*>(x + (int64_t)(t0 + t) * H) + c);
+                    const float xf[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y),
+                                         bf16_hi(xv.y), bf16_lo(xv.z), bf16_hi(xv.z),
+                                         bf16_lo(xv.w), bf16_hi(xv.w)};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[t] = fmaf(wf[j], xf[j], acc[t]);
+                }
+            }
+        }
+    } else {
+        for (int j = lane; j < H; j += 32) {
+            const float wf = bf16_bits_to_float(wr[j]);
+#pragma unroll
+            for (int t = 0; t < kRouteTokens; ++t)
+                if (t < nt) acc[t] = fmaf(wf, bf16_bits_to_float(x[(int64_t)(t0 + t) * H + j]), acc[t]);
+        }
+    }
+    const float b = bias != nullptr ? bias[e] : 0.f;
+#pragma unroll
+    for (int t = 0; t < kRouteTokens; ++t) {
+        const float v = warp_sum(acc[t]);
+        if (lane == 0 && t < nt) logits[(int64_t)(t0 + t) * E + e] = v + b;
+    }
+}
+
+// JE = logits held per lane (E <= 32 * JE).
+template <int JE>
+__global__ void __launch_bounds__(256)
+    route_select_kernel(const float* __restrict__ logits, int T, int E, int k,
+                        int32_t* __restrict__ idx, float* __restrict__ w) {
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T) return;
+    float v[JE];
+#pragma unroll
+    for (int j = 0; j < JE; ++j) {
+        const int e = lane + 32 * j;
+        float l = e < E ? logits[(int64_t)t * E + e] : -INFINITY;
+        v[j] = (l != l) ? -INFINITY : l;  // NaN ranks last
+    }
+    uint32_t taken = 0;
+    float my_val = -INFINITY;
+    int my_idx = 0;
+    for (int r = 0; r < k; ++r) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < JE; ++j) {
+            const int e = lane + 32 * j;
+            if (e < E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be))) {
+                bv = v[j];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(kFullMask, bv, o);
+            const int oe = __shfl_xor_sync(kFullMask, be, o);
+            if (ov > bv || (ov == bv && oe < be)) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (lane == r) {
+            my_val = bv;
+            my_idx = be;
+        }
+    }
+    const float top = __shfl_sync(kFullMask, my_val, 0);
+    const float ex = lane < k ? expf(my_val - top) : 0.f;
+    const float denom = warp_sum(ex);
+    if (lane < k) {
+        idx[(int64_t)t * k + lane] = my_idx;
+        w[(int64_t)t * k + lane] = ex / denom;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_route_topk(const uint16_t* x, const uint16_t* Wr, const float* bias, int T,
+                              int H, int E, int k, float* logits, int32_t* idx, float* w,
+                              cudaStream_t stream, const DeviceInfo& dev) {
+    (void)dev;
+    const int vec = (H % 8 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
+                    (reinterpret_cast<uintptr_t>(Wr) % 16 == 0);
+    dim3 g1((E + kRouteWarps - 1) / kRouteWarps, (T + kRouteTokens - 1) / kRouteTokens);
+    cudaError_t err = launch_pdl(route_logits_kernel, g1, dim3(kRouteWarps * 32), 0, stream, x, Wr,
+                                 bias, T, H, E, logits, vec);
+    if (err != cudaSuccess) return err;
+    dim3 g2((T + 7) / 8);
+    const float* cl = logits;
+    if (E <= 32) return launch_pdl(route_select_kernel<1>, g2, dim3(256), 0, stream, cl, T, E, k, idx, w);
+    if (E <= 64) return launch_pdl(route_select_kernel<2>, g2, dim3(256), 0, stream, cl, T, E, k, idx, w);
+    if (E <= 128) return launch_pdl(route_select_kernel<4>, g2, dim3(256), 0, stream, cl, T, E, k, idx, w);
+    if (E <= 256) return launch_pdl(route_select_kernel<8>, g2, dim3(256), 0, stream, cl, T, E, k, idx, w);
+    if (E <= 512) return launch_pdl(route_select_kernel<16>, g2, dim3(256), 0, stream, cl, T, E, k, idx, w);
+    return launch_pdl(route_select_kernel<32>, g2, dim3(256), 0, stream, cl, T, E, k, idx, w);
+}
+
+}  // namespace maple

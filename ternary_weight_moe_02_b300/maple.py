@@ -1,0 +1,211 @@
+"""Thin ctypes binding of libmaple.so (C-ABI in include/maple.h).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.  Functions
+carry the C names; tensors are caller-owned torch CUDA tensors, passed by data
+pointer, and work is enqueued on the given stream (default: torch's current stream).
+A non-OK status raises MapleError.  Importing this module fails loudly when the
+library has not been built (python -m ternary_weight_moe_02_b300.build_lib).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmaple.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        f"libmaple.so is missing at {_LIB_PATH}; build it with "
+        "`python -m ternary_weight_moe_02_b300.build_lib` (there is no fallback path)")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+MAPLE_OK = 0
+MAPLE_ERR_INVALID_ARG = -1
+MAPLE_ERR_UNSUPPORTED_SHAPE = -2
+MAPLE_ERR_MISALIGNED = -3
+MAPLE_ERR_CUDA = -4
+MAPLE_ERR_TIMEOUT = -5
+MAPLE_ERR_BAD_CODE = -6
+MAPLE_ERR_WORKSPACE = -7
+
+EXPORTED = ("maple_version", "maple_status_string", "maple_last_error", "maple_ternarize_pack",
+            "maple_unpack", "maple_route_topk", "maple_group_tokens",
+            "maple_moe_ffn_workspace_size", "maple_moe_ffn")
+
+
+class maple_experts(ctypes.Structure):
+    _fields_ = [("gate", ctypes.c_void_p), ("up", ctypes.c_void_p), ("down", ctypes.c_void_p),
+                ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
+                ("E", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
+                ("clamp", ctypes.c_float)]
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_lib.maple_version.restype = ctypes.c_int
+_lib.maple_status_string.restype = ctypes.c_char_p
+_lib.maple_status_string.argtypes = [ctypes.c_int]
+_lib.maple_last_error.restype = ctypes.c_char_p
+_lib.maple_ternarize_pack.argtypes = [_P, _I64, _I64, _P, _P, _P]
+_lib.maple_unpack.argtypes = [_P, _P, _I64, _I64, _P, _P, _P]
+_lib.maple_route_topk.argtypes = [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P]
+_lib.maple_group_tokens.argtypes = [_P, _I32, _I32, _I32, _P, _P, _P, _P]
+_lib.maple_moe_ffn_workspace_size.argtypes = [_I32, _I32, ctypes.POINTER(maple_experts)]
+_lib.maple_moe_ffn_workspace_size.restype = ctypes.c_size_t
+_lib.maple_moe_ffn.argtypes = [ctypes.POINTER(maple_experts), _P, _P, _P, _I32, _I32, _P, _P,
+                               ctypes.c_size_t, _P]
+for _n in ("maple_ternarize_pack", "maple_unpack", "maple_route_topk", "maple_group_tokens",
+           "maple_moe_ffn"):
+    getattr(_lib, _n).restype = ctypes.c_int
+
+
+class MapleError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = _lib.maple_last_error().decode(errors="replace")
+        name = _lib.maple_status_string(status).decode()
+        super().__init__(f"{where}: {name}: {msg}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _check(status: int, where: str):
+    if status != MAPLE_OK:
+        raise MapleError(status, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _expect(t, dtype, shape, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def packed_row_bytes(K: int) -> int:
+    return (K + 4) // 5
+
+
+def maple_version() -> int:
+    return _lib.maple_version()
+
+
+def maple_status_string(status: int) -> str:
+    return _lib.maple_status_string(status).decode()
+
+
+def maple_last_error() -> str:
+    return _lib.maple_last_error().decode(errors="replace")
+
+
+def maple_ternarize_pack(W, packed, scales, stream=None):
+    """W bf16 [rows, K] -> packed uint8 [rows, ceil(K/5)], scales fp32 [rows]."""
+    rows, K = W.shape
+    _expect(W, torch.bfloat16, (rows, K), "W")
+    _expect(packed, torch.uint8, (rows, packed_row_bytes(K)), "packed")
+    _expect(scales, torch.float32, (rows,), "scales")
+    _check(_lib.maple_ternarize_pack(_ptr(W), rows, K, _ptr(packed), _ptr(scales), _stream(stream)),
+           "maple_ternarize_pack")
+
+
+def maple_unpack(packed, scales, K, W_out, bad_codes=None, stream=None):
+    rows = packed.shape[0]
+    _expect(packed, torch.uint8, (rows, packed_row_bytes(K)), "packed")
+    _expect(scales, torch.float32, (rows,), "scales")
+    _expect(W_out, torch.float32, (rows, K), "W_out")
+    if bad_codes is not None:
+        _expect(bad_codes, torch.int32, (1,), "bad_codes")
+    _check(_lib.maple_unpack(_ptr(packed), _ptr(scales), rows, K, _ptr(W_out), _ptr(bad_codes),
+                             _stream(stream)), "maple_unpack")
+
+
+def maple_route_topk(x, Wr, bias, k, logits, idx, w, stream=None):
+    """x bf16 [T,H], Wr bf16 [E,H], bias fp32 [E] or None -> logits [T,E], idx [T,k], w [T,k]."""
+    T, H = x.shape
+    E = Wr.shape[0]
+    _expect(x, torch.bfloat16, (T, H), "x")
+    _expect(Wr, torch.bfloat16, (E, H), "Wr")
+    if bias is not None:
+        _expect(bias, torch.float32, (E,), "bias")
+    _expect(logits, torch.float32, (T, E), "logits")
+    _expect(idx, torch.int32, (T, k), "idx")
+    _expect(w, torch.float32, (T, k), "w")
+    _check(_lib.maple_route_topk(_ptr(x), _ptr(Wr), _ptr(bias), T, H, E, k, _ptr(logits), _ptr(idx),
+                                 _ptr(w), _stream(stream)), "maple_route_topk")
+
+
+def maple_group_tokens(idx, E, counts, offsets, perm, stream=None):
+    T, k = idx.shape
+    _expect(idx, torch.int32, (T, k), "idx")
+    _expect(counts, torch.int32, (E,), "counts")
+    _expect(offsets, torch.int32, (E + 1,), "offsets")
+    _expect(perm, torch.int32, (T * k,), "perm")
+    _check(_lib.maple_group_tokens(_ptr(idx), T, k, E, _ptr(counts), _ptr(offsets), _ptr(perm),
+                                   _stream(stream)), "maple_group_tokens")
+
+
+class Experts:
+    """Packed expert weights of one layer (caller-owned tensors) and their C struct."""
+
+    def __init__(self, gate, up, down, s_gate, s_up, s_down, clamp: float = 7.0):
+        E, I, bh = gate.shape
+        H = down.shape[1]
+        _expect(gate, torch.uint8, (E, I, packed_row_bytes(H)), "gate")
+        _expect(up, torch.uint8, (E, I, packed_row_bytes(H)), "up")
+        _expect(down, torch.uint8, (E, H, packed_row_bytes(I)), "down")
+        _expect(s_gate, torch.float32, (E, I), "s_gate")
+        _expect(s_up, torch.float32, (E, I), "s_up")
+        _expect(s_down, torch.float32, (E, H), "s_down")
+        self.tensors = (gate, up, down, s_gate, s_up, s_down)
+        self.E, self.H, self.I, self.clamp = E, H, I, clamp
+        self.struct = maple_experts(gate.data_ptr(), up.data_ptr(), down.data_ptr(),
+                                    s_gate.data_ptr(), s_up.data_ptr(), s_down.data_ptr(), E, H, I,
+                                    clamp)
+
+    @property
+    def packed_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in self.tensors)
+
+
+def maple_moe_ffn_workspace_size(T: int, k: int, experts: Experts) -> int:
+    return int(_lib.maple_moe_ffn_workspace_size(T, k, ctypes.byref(experts.struct)))
+
+
+def maple_moe_ffn(experts: Experts, x, idx, w, y, ws, stream=None):
+    """y fp32 [T,H] = sum_i w[t,i] * expert_{idx[t,i]}(x_t); ws = uint8 workspace tensor."""
+    T, H = x.shape
+    k = idx.shape[1]
+    _expect(x, torch.bfloat16, (T, experts.H), "x")
+    _expect(idx, torch.int32, (T, k), "idx")
+    _expect(w, torch.float32, (T, k), "w")
+    _expect(y, torch.float32, (T, experts.H), "y")
+    _check(_lib.maple_moe_ffn(ctypes.byref(experts.struct), _ptr(x), _ptr(idx), _ptr(w), T, k,
+                              _ptr(y), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                              _stream(stream)), "maple_moe_ffn")
+
+
+def clamp_none() -> float:
+    """Clamp value that turns the Maple clamps off (plain SwiGLU)."""
+    return math.inf
