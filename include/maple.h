@@ -161,6 +161,26 @@ MAPLE_API int maple_moe_ffn(const maple_experts* ex, const uint16_t* x, const in
                   const float* w, int32_t T, int32_t k, float* y, void* ws, size_t ws_bytes,
                   void* stream);
 
+/*
+ * maple_moe_ffn without a workspace argument, for callers that cannot allocate device
+ * memory: a plugin whose host process owns every device allocation, code running
+ * while a stream is captured into a CUDA graph (cudaMalloc is not allowed there), or
+ * a loop that must never enter an allocator.  The paper has no counterpart: this is
+ * a packaging of maple_moe_ffn, with the same arguments (minus ws / ws_bytes), the
+ * same limits and the same result.
+ * Scratch lives in one static 2 MiB device array per GPU, held from the library's
+ * load until process exit.  A call whose maple_moe_ffn_workspace_size(T, k, ex)
+ * exceeds 2 MiB (at Maple's shapes: T > 127 with k = 8, I = 512) returns
+ * MAPLE_ERR_WORKSPACE and launches nothing.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) and should come before any stream
+ * capture.  The array is shared by every call and keeps the previous call's
+ * contents (none of it needs clearing); calls that overlap on the GPU race on it,
+ * so the caller must serialise them.  Allocates nothing.
+ */
+MAPLE_API int maple_moe_ffn_static_scratch(const maple_experts* ex, const uint16_t* x,
+                                           const int32_t* idx, const float* w, int32_t T,
+                                           int32_t k, float* y, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

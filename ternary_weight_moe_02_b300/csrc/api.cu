@@ -42,6 +42,14 @@ int get_device(maple::DeviceInfo* dev, const char* what) {
 
 namespace maple {
 
+int report_error(int status, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return status;
+}
+
 cudaError_t device_info(DeviceInfo* info) {
     static int cached_sm[128];
     static size_t cached_smem[128];

@@ -8,6 +8,9 @@
 
 namespace maple {
 
+// Sets the per-thread text behind maple_last_error() and returns `status`.
+int report_error(int status, const char* fmt, ...);
+
 struct DeviceInfo {
     int device;
     int sm_count;

@@ -32,7 +32,7 @@ MAPLE_ERR_WORKSPACE = -7
 
 EXPORTED = ("maple_version", "maple_status_string", "maple_last_error", "maple_ternarize_pack",
             "maple_unpack", "maple_route_topk", "maple_group_tokens",
-            "maple_moe_ffn_workspace_size", "maple_moe_ffn")
+            "maple_moe_ffn_workspace_size", "maple_moe_ffn", "maple_moe_ffn_static_scratch")
 
 
 class maple_experts(ctypes.Structure):
@@ -57,8 +57,10 @@ _lib.maple_moe_ffn_workspace_size.argtypes = [_I32, _I32, ctypes.POINTER(maple_e
 _lib.maple_moe_ffn_workspace_size.restype = ctypes.c_size_t
 _lib.maple_moe_ffn.argtypes = [ctypes.POINTER(maple_experts), _P, _P, _P, _I32, _I32, _P, _P,
                                ctypes.c_size_t, _P]
+_lib.maple_moe_ffn_static_scratch.argtypes = [ctypes.POINTER(maple_experts), _P, _P, _P, _I32,
+                                              _I32, _P, _P]
 for _n in ("maple_ternarize_pack", "maple_unpack", "maple_route_topk", "maple_group_tokens",
-           "maple_moe_ffn"):
+           "maple_moe_ffn", "maple_moe_ffn_static_scratch"):
     getattr(_lib, _n).restype = ctypes.c_int
 
 
@@ -204,6 +206,22 @@ def maple_moe_ffn(experts: Experts, x, idx, w, y, ws, stream=None):
     _check(_lib.maple_moe_ffn(ctypes.byref(experts.struct), _ptr(x), _ptr(idx), _ptr(w), T, k,
                               _ptr(y), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                               _stream(stream)), "maple_moe_ffn")
+
+
+def maple_moe_ffn_static_scratch(experts: Experts, x, idx, w, y, stream=None):
+    """maple_moe_ffn for callers that cannot allocate: the library's static per-GPU
+    scratch array stands in for the workspace (T * k * I * 4 bytes plus a few KB must
+    fit in 2 MiB).  Calls that overlap on the GPU share that array and must be
+    serialised by the caller."""
+    T, H = x.shape
+    k = idx.shape[1]
+    _expect(x, torch.bfloat16, (T, experts.H), "x")
+    _expect(idx, torch.int32, (T, k), "idx")
+    _expect(w, torch.float32, (T, k), "w")
+    _expect(y, torch.float32, (T, experts.H), "y")
+    _check(_lib.maple_moe_ffn_static_scratch(ctypes.byref(experts.struct), _ptr(x), _ptr(idx),
+                                             _ptr(w), T, k, _ptr(y), _stream(stream)),
+           "maple_moe_ffn_static_scratch")
 
 
 def clamp_none() -> float:
