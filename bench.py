@@ -167,19 +167,28 @@ def run_gpu(args, world, rank, local):
     idx = torch.empty((1, K_TOP), dtype=torch.int32, device=dev)
     wts = torch.empty((1, K_TOP), device=dev)
     y = torch.empty((1, H), device=dev)
-    ws = torch.empty(maple.maple_moe_ffn_workspace_size(1, K_TOP, layers[0][0]), dtype=torch.uint8,
+    # maple_moe_layer wants the first 256 bytes zero before its first call
+    ws = torch.zeros(maple.maple_moe_layer_workspace_size(1, K_TOP, layers[0][0]), dtype=torch.uint8,
                      device=dev)
+    ws_ffn = torch.empty(maple.maple_moe_ffn_workspace_size(1, K_TOP, layers[0][0]),
+                         dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
     def step(i, s, events=None):
+        # one layer step: route + FFN of one token (a single fused launch)
+        ex, router = layers[i % n_layers]
+        x = x_all[i % N_TOKENS: i % N_TOKENS + 1]
+        if events is not None:
+            events[0].record(s)
+        maple.maple_moe_layer(x, router, None, ex, K_TOP, logits, idx, wts, y, ws, stream=s)
+        if events is not None:
+            events[1].record(s)
+
+    def step_two_calls(i, s):
         ex, router = layers[i % n_layers]
         x = x_all[i % N_TOKENS: i % N_TOKENS + 1]
         maple.maple_route_topk(x, router, None, K_TOP, logits, idx, wts, stream=s)
-        if events is not None:
-            events[0].record(s)
-        maple.maple_moe_ffn(ex, x, idx, wts, y, ws, stream=s)
-        if events is not None:
-            events[1].record(s)
+        maple.maple_moe_ffn(ex, x, idx, wts, y, ws_ffn, stream=s)
 
     chunk = max(1, min(args.chunk, args.steps))
 
@@ -222,7 +231,25 @@ def run_gpu(args, world, rank, local):
     elapsed_s = ev0.elapsed_time(ev1) / 1e3
     elapsed_max = _max_over_ranks(elapsed_s, world)
     value = world * args.steps / elapsed_max
-    launches = args.steps * 4  # route_logits, route_select, ffn_gateup, ffn_down
+    launches = args.steps * 1  # moe_layer_b1_kernel: the whole step in one launch
+
+    # The same steps through the two separate calls (route_topk, moe_ffn: 4 launches).
+    n_two = min(args.steps, chunk)
+    g_two = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step_two_calls(i, stream)
+        stream.synchronize()
+        with torch.cuda.graph(g_two, stream=stream):
+            for i in range(n_two):
+                step_two_calls(i, stream)
+        g_two.replay()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        g_two.replay()
+        t1.record(stream)
+    t1.synchronize()
+    two_call_value = n_two / (t0.elapsed_time(t1) / 1e3)
 
     # Roofline pass: the same steps with events around each moe_ffn call (graph-captured),
     # giving the live average duration of the dominant launch pair.
@@ -239,7 +266,9 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
     peak, peak_kind = _peaks()
-    alg_bytes = K_TOP * EXPERT_BYTES  # 8 distinct experts per batch-1 token
+    packed_bytes = K_TOP * EXPERT_BYTES  # 8 distinct experts per batch-1 token
+    # everything one launch must move: packed experts + scales, router, x, y, logits/idx/w
+    alg_bytes = packed_bytes + E * H * 2 + H * 2 + H * 4 + E * 4 + K_TOP * 8
     achieved = alg_bytes / (ffn_ms / 1e3) / 1e9
 
     # End-to-end through the public API with host buffers: pinned token -> device, route,
@@ -254,16 +283,14 @@ def run_gpu(args, world, rank, local):
         for i in range(3):
             x_dev.copy_(x_host[i:i + 1], non_blocking=True)
             ex, router = layers[i % n_layers]
-            maple.maple_route_topk(x_dev, router, None, K_TOP, logits, idx, wts, stream=stream)
-            maple.maple_moe_ffn(ex, x_dev, idx, wts, y, ws, stream=stream)
+            maple.maple_moe_layer(x_dev, router, None, ex, K_TOP, logits, idx, wts, y, ws, stream=stream)
             y_host.copy_(y, non_blocking=True)
         stream.synchronize()
         e0.record(stream)
         for i in range(n_e2e):
             x_dev.copy_(x_host[i % N_TOKENS: i % N_TOKENS + 1], non_blocking=True)
             ex, router = layers[i % n_layers]
-            maple.maple_route_topk(x_dev, router, None, K_TOP, logits, idx, wts, stream=stream)
-            maple.maple_moe_ffn(ex, x_dev, idx, wts, y, ws, stream=stream)
+            maple.maple_moe_layer(x_dev, router, None, ex, K_TOP, logits, idx, wts, y, ws, stream=stream)
             y_host.copy_(y, non_blocking=True)
         e1.record(stream)
     e1.synchronize()
@@ -282,11 +309,14 @@ def run_gpu(args, world, rank, local):
                    "l2": "inputs larger than L2 (layers cycled; no flush)",
                    "graph": f"CUDA graph of {chunk} steps replayed", "parallelism": f"replicas{world}"},
         "gpu_launches": launches,
-        "roofline": {"bound": "hbm", "kernel": "moe_ffn (ffn_gateup + ffn_down launches)",
+        "roofline": {"bound": "hbm", "kernel": "moe_layer_b1_kernel (whole step, one launch)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                      "alg_bytes_per_launch": alg_bytes, "avg_launch_us": ffn_ms * 1e3,
+                     "packed_weight_gbs": packed_bytes / (ffn_ms / 1e3) / 1e9,
                      "traffic": None},
+        "two_call_path": {"value": two_call_value, "unit": "tokens/s",
+                          "calls": "maple_route_topk + maple_moe_ffn (4 launches per step)"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "steps": n_e2e,
                 "h2d_bytes_per_step": H * 2, "d2h_bytes_per_step": H * 4},
         "clocks": clocks.summary(),

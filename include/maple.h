@@ -48,7 +48,7 @@ extern "C" {
 #define MAPLE_ERR_UNSUPPORTED_SHAPE (-2) /* a size beyond the limits stated per call */
 #define MAPLE_ERR_MISALIGNED (-3)        /* a pointer that breaks the stated alignment */
 #define MAPLE_ERR_CUDA (-4)              /* a CUDA launch or attribute call failed */
-#define MAPLE_ERR_TIMEOUT (-5)           /* reserved: a bounded device wait gave up */
+#define MAPLE_ERR_TIMEOUT (-5)           /* a bounded device wait gave up */
 #define MAPLE_ERR_BAD_CODE (-6)          /* packed byte >= 243 (reported by maple_unpack) */
 #define MAPLE_ERR_WORKSPACE (-7)         /* workspace missing or smaller than required */
 
@@ -78,6 +78,15 @@ MAPLE_API const char* maple_status_string(int status);
 
 /* Reason for the last non-OK status returned on this host thread ("" if none). */
 MAPLE_API const char* maple_last_error(void);
+
+/*
+ * Synchronise `stream`, then read and clear this device's status word.  Kernels
+ * that wait on the completion of their own asynchronous copies do so with a bounded
+ * number of polls; a wait that gives up records MAPLE_ERR_TIMEOUT in the word, skips
+ * its work and returns, so the context stays usable.  Returns MAPLE_OK, the recorded
+ * status, or MAPLE_ERR_CUDA if the synchronisation itself failed.
+ */
+MAPLE_API int maple_check_device_status(void* stream);
 
 /*
  * Absmean ternarization + 5-trit packing of a bf16 row-major matrix W [rows x K].
@@ -160,6 +169,31 @@ MAPLE_API size_t maple_moe_ffn_workspace_size(int32_t T, int32_t k, const maple_
 MAPLE_API int maple_moe_ffn(const maple_experts* ex, const uint16_t* x, const int32_t* idx,
                   const float* w, int32_t T, int32_t k, float* y, void* ws, size_t ws_bytes,
                   void* stream);
+
+/* Bytes of workspace maple_moe_layer needs (256 bytes of counters + the FFN's). */
+MAPLE_API size_t maple_moe_layer_workspace_size(int32_t T, int32_t k, const maple_experts* ex);
+
+/*
+ * One MoE layer step: maple_route_topk followed by maple_moe_ffn, with the same
+ * arguments, outputs and results (logits, idx, w and y are all written).
+ * ("Maple-Preview ...", sections "The claim, verified from the bytes" and "The shipped
+ * code does no quantization".)  For a single token (T = 1) at Maple-like sizes the
+ * whole step runs as one cooperative launch of one CTA per SM: every CTA computes a
+ * share of the logits, all of them select the same top-k, fetch and decode their
+ * share of the gate/up rows and then of the down rows, with two grid-wide barriers in
+ * between (bounded waits: MAPLE_ERR_TIMEOUT via maple_check_device_status).  Other
+ * sizes run the two calls in sequence.
+ *   Wr : [E][H] bf16 router (E = ex->E), bias : [E] fp32 or NULL
+ *   ws : device workspace of at least maple_moe_layer_workspace_size(T, k, ex) bytes,
+ *        16-byte aligned; its first 256 bytes must be zero before the first call (for
+ *        example cudaMemsetAsync once after allocating it).  Every call leaves them
+ *        zero again; after a MAPLE_ERR_TIMEOUT report, zero them again.
+ * Limits: those of maple_route_topk and maple_moe_ffn (k <= 32).
+ */
+MAPLE_API int maple_moe_layer(const uint16_t* x, const uint16_t* Wr, const float* bias,
+                              const maple_experts* ex, int32_t T, int32_t k, float* logits,
+                              int32_t* idx, float* w, float* y, void* ws, size_t ws_bytes,
+                              void* stream);
 
 /*
  * maple_moe_ffn without a workspace argument, for callers that cannot allocate device

@@ -5,12 +5,16 @@
 #include <stdio.h>
 #include <string.h>
 
-#include "../../include/maple.h"
+#include "maple.h"
 #include "kernels.h"
 
 namespace {
 
 thread_local char g_last_error[512] = "";
+
+// Device status word: a kernel whose bounded wait gave up records MAPLE_ERR_TIMEOUT
+// here; maple_check_device_status reads and clears it.
+__device__ int g_device_status;
 
 int fail(int status, const char* fmt, ...) {
     va_list ap;
@@ -53,6 +57,7 @@ int report_error(int status, const char* fmt, ...) {
 cudaError_t device_info(DeviceInfo* info) {
     static int cached_sm[128];
     static size_t cached_smem[128];
+    static int* cached_status[128];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -63,12 +68,17 @@ cudaError_t device_info(DeviceInfo* info) {
         if (err != cudaSuccess) return err;
         err = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (err != cudaSuccess) return err;
+        void* status = nullptr;
+        err = cudaGetSymbolAddress(&status, g_device_status);
+        if (err != cudaSuccess) return err;
+        cached_status[dev] = static_cast<int*>(status);
         cached_smem[dev] = (size_t)smem;
         cached_sm[dev] = sm;
     }
     info->device = dev;
     info->sm_count = cached_sm[dev];
     info->smem_optin = cached_smem[dev];
+    info->status = cached_status[dev];
     return cudaSuccess;
 }
 
@@ -93,6 +103,22 @@ const char* maple_status_string(int status) {
 }
 
 const char* maple_last_error(void) { return g_last_error; }
+
+int maple_check_device_status(void* stream) {
+    maple::DeviceInfo dev;
+    if (int st = get_device(&dev, "check_device_status")) return st;
+    cudaError_t err = cudaStreamSynchronize((cudaStream_t)stream);
+    if (err != cudaSuccess) return cuda_fail(err, "check_device_status: stream synchronize");
+    int value = 0;
+    err = cudaMemcpy(&value, dev.status, sizeof value, cudaMemcpyDeviceToHost);
+    if (err != cudaSuccess) return cuda_fail(err, "check_device_status: read");
+    if (value == MAPLE_OK) return ok();
+    const int zero = 0;
+    err = cudaMemcpy(dev.status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (err != cudaSuccess) return cuda_fail(err, "check_device_status: clear");
+    return fail(value, "check_device_status: a kernel reported %s (a bounded device wait gave up)",
+                maple_status_string(value));
+}
 
 int maple_ternarize_pack(const uint16_t* W, int64_t rows, int64_t K, uint8_t* packed,
                          float* scales, void* stream) {
@@ -152,8 +178,8 @@ int maple_group_tokens(const int32_t* idx, int32_t T, int32_t k, int32_t E, int3
 }
 
 size_t maple_moe_ffn_workspace_size(int32_t T, int32_t k, const maple_experts* ex) {
-    if (!ex || T < 0 || k < 1 || ex->E < 1 || ex->I < 1) return 0;
-    return maple::ffn_workspace_layout(T, k, ex->E, ex->I).total;
+    if (!ex || T < 0 || k < 1 || ex->E < 1 || ex->H < 1 || ex->I < 1) return 0;
+    return maple::ffn_workspace_layout(T, k, ex->E, ex->H, ex->I).total;
 }
 
 int maple_moe_ffn(const maple_experts* ex, const uint16_t* x, const int32_t* idx,
@@ -172,7 +198,7 @@ int maple_moe_ffn(const maple_experts* ex, const uint16_t* x, const int32_t* idx
         !aligned(ex->s_up, 16) || !aligned(ex->s_down, 16) || !aligned(x, 16) || !aligned(ws, 16))
         return fail(MAPLE_ERR_MISALIGNED, "moe_ffn: packed weights, scales, x and ws need 16-byte alignment");
     if (!aligned(idx, 4) || !aligned(w, 4) || !aligned(y, 4)) return fail(MAPLE_ERR_MISALIGNED, "moe_ffn: idx, w, y need 4-byte alignment");
-    const maple::FfnWorkspaceLayout L = maple::ffn_workspace_layout(T, k, E, I);
+    const maple::FfnWorkspaceLayout L = maple::ffn_workspace_layout(T, k, E, H, I);
     if (!ws || ws_bytes < L.total) return fail(MAPLE_ERR_WORKSPACE, "moe_ffn: workspace %zu bytes < %zu needed", ws_bytes, L.total);
     maple::DeviceInfo dev;
     if (int st = get_device(&dev, "moe_ffn")) return st;
@@ -200,9 +226,71 @@ int maple_moe_ffn(const maple_experts* ex, const uint16_t* x, const int32_t* idx
     a.active = reinterpret_cast<int32_t*>(base + L.active);
     a.n_active = reinterpret_cast<int32_t*>(base + L.n_active);
     a.h = reinterpret_cast<float*>(base + L.h);
+    a.status = dev.status;
     cudaError_t err = maple::launch_moe_ffn(a, (cudaStream_t)stream, dev);
     if (err != cudaSuccess) return cuda_fail(err, "moe_ffn launch");
     return ok();
+}
+
+// Workspace of maple_moe_layer: 256 bytes of barrier counters, then the FFN workspace.
+size_t maple_moe_layer_workspace_size(int32_t T, int32_t k, const maple_experts* ex) {
+    const size_t ffn = maple_moe_ffn_workspace_size(T, k, ex);
+    return ffn == 0 ? 0 : 256 + ffn;
+}
+
+int maple_moe_layer(const uint16_t* x, const uint16_t* Wr, const float* bias,
+                    const maple_experts* ex, int32_t T, int32_t k, float* logits, int32_t* idx,
+                    float* w, float* y, void* ws, size_t ws_bytes, void* stream) {
+    if (!ex) return fail(MAPLE_ERR_INVALID_ARG, "moe_layer: null experts");
+    const int E = ex->E, H = ex->H, I = ex->I;
+    if (T < 0 || H < 1 || E < 1 || I < 1 || k < 1 || k > E) return fail(MAPLE_ERR_INVALID_ARG, "moe_layer: T=%d H=%d E=%d I=%d k=%d", T, H, E, I, k);
+    if (!(ex->clamp > 0.f)) return fail(MAPLE_ERR_INVALID_ARG, "moe_layer: clamp must be > 0 (INFINITY for none)");
+    if (E > 1024 || k > 32 || H > 2080 || I > 2080 || (int64_t)T * k > (int64_t(1) << 24))
+        return fail(MAPLE_ERR_UNSUPPORTED_SHAPE, "moe_layer: E=%d (<=1024) k=%d (<=32) H=%d (<=2080) I=%d (<=2080) T*k=%lld", E, k, H, I, (long long)T * k);
+    if (T == 0) return ok();
+    if (!x || !Wr || !logits || !idx || !w || !y || !ex->gate || !ex->up || !ex->down || !ex->s_gate || !ex->s_up || !ex->s_down)
+        return fail(MAPLE_ERR_INVALID_ARG, "moe_layer: null pointer");
+    if (!aligned(x, 16) || !aligned(Wr, 16) || !aligned(ws, 16) || !aligned(ex->gate, 16) || !aligned(ex->up, 16) ||
+        !aligned(ex->down, 16) || !aligned(ex->s_gate, 16) || !aligned(ex->s_up, 16) || !aligned(ex->s_down, 16))
+        return fail(MAPLE_ERR_MISALIGNED, "moe_layer: x, Wr, ws, packed weights and scales need 16-byte alignment");
+    if (!aligned(bias, 4) || !aligned(logits, 4) || !aligned(idx, 4) || !aligned(w, 4) || !aligned(y, 4))
+        return fail(MAPLE_ERR_MISALIGNED, "moe_layer: fp32/int32 arrays need 4-byte alignment");
+    const size_t need = maple_moe_layer_workspace_size(T, k, ex);
+    if (!ws || ws_bytes < need) return fail(MAPLE_ERR_WORKSPACE, "moe_layer: workspace %zu bytes < %zu needed", ws_bytes, need);
+    maple::DeviceInfo dev;
+    if (int st = get_device(&dev, "moe_layer")) return st;
+    char* base = static_cast<char*>(ws);
+    if (T == 1 && maple::layer_b1_supported(H, I, E, k, dev)) {
+        const maple::FfnWorkspaceLayout L = maple::ffn_workspace_layout(T, k, E, H, I);
+        maple::LayerLaunch p;
+        p.x = x;
+        p.Wr = Wr;
+        p.bias = bias;
+        p.gate = ex->gate;
+        p.up = ex->up;
+        p.down = ex->down;
+        p.s_gate = ex->s_gate;
+        p.s_up = ex->s_up;
+        p.s_down = ex->s_down;
+        p.E = E;
+        p.H = H;
+        p.I = I;
+        p.k = k;
+        p.clamp = ex->clamp;
+        p.logits = logits;
+        p.idx = idx;
+        p.w = w;
+        p.y = y;
+        p.h = reinterpret_cast<float*>(base + 256 + L.h);
+        p.sync = reinterpret_cast<unsigned*>(base);
+        cudaError_t err = maple::launch_moe_layer_b1(p, (cudaStream_t)stream, dev);
+        if (err != cudaSuccess) return cuda_fail(err, "moe_layer launch");
+        return ok();
+    }
+    // general sizes: the two calls in sequence
+    int st = maple_route_topk(x, Wr, bias, T, H, E, k, logits, idx, w, stream);
+    if (st != MAPLE_OK) return st;
+    return maple_moe_ffn(ex, x, idx, w, T, k, y, base + 256, ws_bytes - 256, stream);
 }
 
 }  // extern "C"

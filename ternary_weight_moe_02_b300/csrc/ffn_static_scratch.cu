@@ -21,7 +21,7 @@
 
 #include <mutex>
 
-#include "../../include/maple.h"
+#include "maple.h"
 #include "kernels.h"
 
 namespace {

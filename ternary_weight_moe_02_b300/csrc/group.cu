@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(kGroupThreads)
     for (int i = tid; i < kGroupWarps * E; i += kGroupThreads) warp_cnt[i] = 0;
     __syncthreads();
     pdl_wait();
+    pdl_launch_dependents();
 
     for (int s = tid; s < S; s += kGroupThreads) {
         const int e = idx[s];

@@ -15,6 +15,7 @@ struct DeviceInfo {
     int device;
     int sm_count;
     size_t smem_optin;
+    int* status;  // device status word (MAPLE_ERR_TIMEOUT after a bounded wait gave up)
 };
 cudaError_t device_info(DeviceInfo* info);
 
@@ -57,13 +58,38 @@ struct FfnArgs {
     int32_t* active;   // [E]
     int32_t* n_active; // [1]
     float* h;          // [T*k][I]
+    int* status;       // device status word
+    int prefetch_down; // 1 if the down rows may be bulk-prefetched (16-byte multiples)
 };
 
 struct FfnWorkspaceLayout {
     size_t counts, offsets, perm, active, n_active, h, total;
 };
-FfnWorkspaceLayout ffn_workspace_layout(int T, int k, int E, int I);
+FfnWorkspaceLayout ffn_workspace_layout(int T, int k, int E, int H, int I);
 
 cudaError_t launch_moe_ffn(const FfnArgs& a, cudaStream_t stream, const DeviceInfo& dev);
+
+// Fused single-token layer step (route + gate/up + down in one cooperative launch).
+struct LayerLaunch {
+    const uint16_t* x;
+    const uint16_t* Wr;
+    const float* bias;
+    const uint8_t* gate;
+    const uint8_t* up;
+    const uint8_t* down;
+    const float* s_gate;
+    const float* s_up;
+    const float* s_down;
+    int E, H, I, k;
+    float clamp;
+    float* logits;
+    int32_t* idx;
+    float* w;
+    float* y;
+    float* h;        // [k][I] scratch
+    unsigned* sync;  // 2 counters, zero on entry and on exit
+};
+bool layer_b1_supported(int H, int I, int E, int k, const DeviceInfo& dev);
+cudaError_t launch_moe_layer_b1(const LayerLaunch& p, cudaStream_t stream, const DeviceInfo& dev);
 
 }  // namespace maple

@@ -20,7 +20,8 @@ namespace maple {
 
 namespace {
 
-constexpr int kRouteWarps = 4;   // expert rows per CTA
+constexpr int kRouteWarps = 2;   // expert rows per CTA
+constexpr int kRouteBatch = 8;   // 16-byte chunks a lane loads before using them
 constexpr int kRouteTokens = 8;  // tokens per CTA
 
 __global__ void __launch_bounds__(kRouteWarps * 32)
@@ -28,6 +29,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
                         const float* __restrict__ bias, int T, int H, int E,
                         float* __restrict__ logits, int vec) {
     pdl_wait();
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * kRouteWarps + warp;
     const int t0 = blockIdx.y * kRouteTokens;
@@ -38,22 +40,37 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
     for (int t = 0; t < kRouteTokens; ++t) acc[t] = 0.f;
     const uint16_t* wr = Wr + (int64_t)e * H;
     if (vec) {
+        // every lane issues all of a batch's loads before it uses any of them
         const int n8 = H >> 3;
         const uint4* w4 = reinterpret_cast<const uint4*>(wr);
-        for (int c = lane; c < n8; c += 32) {
-            const uint4 wv = ldg_nc_v4(w4 + c);
-            const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
-                                 bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
+        for (int base = 0; base < n8; base += 32 * kRouteBatch) {
+            uint4 wv[kRouteBatch];
+#pragma unroll
+            for (int u = 0; u < kRouteBatch; ++u) {
+                const int c = base + lane + 32 * u;
+                wv[u] = c < n8 ? ldg_nc_v4(w4 + c) : make_uint4(0, 0, 0, 0);
+            }
 #pragma unroll
             for (int t = 0; t < kRouteTokens; ++t) {
                 if (t < nt) {
-                    const uint4 xv =
-                        ldg_nc_v4(reinterpret_cast<const uint4*>(x + (int64_t)(t0 + t) * H) + c);
-                    const float xf[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y),
-                                         bf16_hi(xv.y), bf16_lo(xv.z), bf16_hi(xv.z),
-                                         bf16_lo(xv.w), bf16_hi(xv.w)};
+                    const uint4* x4 = reinterpret_cast<const uint4*>(x + (int64_t)(t0 + t) * H);
+                    uint4 xv[kRouteBatch];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[t] = fmaf(wf[j], xf[j], acc[t]);
+                    for (int u = 0; u < kRouteBatch; ++u) {
+                        const int c = base + lane + 32 * u;
+                        xv[u] = c < n8 ? ldg_nc_v4(x4 + c) : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kRouteBatch; ++u) {
+                        const float wf[8] = {bf16_lo(wv[u].x), bf16_hi(wv[u].x), bf16_lo(wv[u].y),
+                                             bf16_hi(wv[u].y), bf16_lo(wv[u].z), bf16_hi(wv[u].z),
+                                             bf16_lo(wv[u].w), bf16_hi(wv[u].w)};
+                        const float xf[8] = {bf16_lo(xv[u].x), bf16_hi(xv[u].x), bf16_lo(xv[u].y),
+                                             bf16_hi(xv[u].y), bf16_lo(xv[u].z), bf16_hi(xv[u].z),
+                                             bf16_lo(xv[u].w), bf16_hi(xv[u].w)};
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) acc[t] = fmaf(wf[j], xf[j], acc[t]);
+                    }
                 }
             }
         }
@@ -79,51 +96,17 @@ __global__ void __launch_bounds__(256)
     route_select_kernel(const float* __restrict__ logits, int T, int E, int k,
                         int32_t* __restrict__ idx, float* __restrict__ w) {
     pdl_wait();
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= T) return;
-    float v[JE];
-#pragma unroll
-    for (int j = 0; j < JE; ++j) {
-        const int e = lane + 32 * j;
-        float l = e < E ? logits[(int64_t)t * E + e] : -INFINITY;
-        v[j] = (l != l) ? -INFINITY : l;  // NaN ranks last
-    }
-    uint32_t taken = 0;
-    float my_val = -INFINITY;
-    int my_idx = 0;
-    for (int r = 0; r < k; ++r) {
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < JE; ++j) {
-            const int e = lane + 32 * j;
-            if (e < E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be))) {
-                bv = v[j];
-                be = e;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(kFullMask, bv, o);
-            const int oe = __shfl_xor_sync(kFullMask, be, o);
-            if (ov > bv || (ov == bv && oe < be)) {
-                bv = ov;
-                be = oe;
-            }
-        }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        if (lane == r) {
-            my_val = bv;
-            my_idx = be;
-        }
-    }
-    const float top = __shfl_sync(kFullMask, my_val, 0);
-    const float ex = lane < k ? expf(my_val - top) : 0.f;
-    const float denom = warp_sum(ex);
+    int my_idx;
+    float my_w;
+    const float* lt = logits + (int64_t)t * E;
+    warp_topk_softmax<JE>([&](int e) { return lt[e]; }, E, k, lane, my_idx, my_w);
     if (lane < k) {
         idx[(int64_t)t * k + lane] = my_idx;
-        w[(int64_t)t * k + lane] = ex / denom;
+        w[(int64_t)t * k + lane] = my_w;
     }
 }
 

@@ -30,9 +30,11 @@ MAPLE_ERR_TIMEOUT = -5
 MAPLE_ERR_BAD_CODE = -6
 MAPLE_ERR_WORKSPACE = -7
 
-EXPORTED = ("maple_version", "maple_status_string", "maple_last_error", "maple_ternarize_pack",
+EXPORTED = ("maple_version", "maple_status_string", "maple_last_error",
+            "maple_check_device_status", "maple_ternarize_pack",
             "maple_unpack", "maple_route_topk", "maple_group_tokens",
-            "maple_moe_ffn_workspace_size", "maple_moe_ffn", "maple_moe_ffn_static_scratch")
+            "maple_moe_ffn_workspace_size", "maple_moe_ffn", "maple_moe_layer_workspace_size",
+            "maple_moe_layer", "maple_moe_ffn_static_scratch")
 
 
 class maple_experts(ctypes.Structure):
@@ -49,6 +51,8 @@ _lib.maple_version.restype = ctypes.c_int
 _lib.maple_status_string.restype = ctypes.c_char_p
 _lib.maple_status_string.argtypes = [ctypes.c_int]
 _lib.maple_last_error.restype = ctypes.c_char_p
+_lib.maple_check_device_status.argtypes = [_P]
+_lib.maple_check_device_status.restype = ctypes.c_int
 _lib.maple_ternarize_pack.argtypes = [_P, _I64, _I64, _P, _P, _P]
 _lib.maple_unpack.argtypes = [_P, _P, _I64, _I64, _P, _P, _P]
 _lib.maple_route_topk.argtypes = [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P]
@@ -57,6 +61,11 @@ _lib.maple_moe_ffn_workspace_size.argtypes = [_I32, _I32, ctypes.POINTER(maple_e
 _lib.maple_moe_ffn_workspace_size.restype = ctypes.c_size_t
 _lib.maple_moe_ffn.argtypes = [ctypes.POINTER(maple_experts), _P, _P, _P, _I32, _I32, _P, _P,
                                ctypes.c_size_t, _P]
+_lib.maple_moe_layer_workspace_size.argtypes = [_I32, _I32, ctypes.POINTER(maple_experts)]
+_lib.maple_moe_layer_workspace_size.restype = ctypes.c_size_t
+_lib.maple_moe_layer.argtypes = [_P, _P, _P, ctypes.POINTER(maple_experts), _I32, _I32, _P, _P, _P,
+                                 _P, _P, ctypes.c_size_t, _P]
+_lib.maple_moe_layer.restype = ctypes.c_int
 _lib.maple_moe_ffn_static_scratch.argtypes = [ctypes.POINTER(maple_experts), _P, _P, _P, _I32,
                                               _I32, _P, _P]
 for _n in ("maple_ternarize_pack", "maple_unpack", "maple_route_topk", "maple_group_tokens",
@@ -120,6 +129,11 @@ def maple_status_string(status: int) -> str:
 
 def maple_last_error() -> str:
     return _lib.maple_last_error().decode(errors="replace")
+
+
+def maple_check_device_status(stream=None):
+    """Synchronise the stream and raise if a kernel recorded a device-side error."""
+    _check(_lib.maple_check_device_status(_stream(stream)), "maple_check_device_status")
 
 
 def maple_ternarize_pack(W, packed, scales, stream=None):
@@ -208,10 +222,33 @@ def maple_moe_ffn(experts: Experts, x, idx, w, y, ws, stream=None):
                               _stream(stream)), "maple_moe_ffn")
 
 
+def maple_moe_layer_workspace_size(T: int, k: int, experts: Experts) -> int:
+    return int(_lib.maple_moe_layer_workspace_size(T, k, ctypes.byref(experts.struct)))
+
+
+def maple_moe_layer(x, Wr, bias, experts: Experts, k, logits, idx, w, y, ws, stream=None):
+    """Route + FFN for one layer step.  ws: uint8 tensor of maple_moe_layer_workspace_size
+    bytes whose first 256 bytes are zero before the first call (torch.zeros does it)."""
+    T, H = x.shape
+    E = Wr.shape[0]
+    _expect(x, torch.bfloat16, (T, experts.H), "x")
+    _expect(Wr, torch.bfloat16, (experts.E, experts.H), "Wr")
+    if bias is not None:
+        _expect(bias, torch.float32, (E,), "bias")
+    _expect(logits, torch.float32, (T, E), "logits")
+    _expect(idx, torch.int32, (T, k), "idx")
+    _expect(w, torch.float32, (T, k), "w")
+    _expect(y, torch.float32, (T, experts.H), "y")
+    _check(_lib.maple_moe_layer(_ptr(x), _ptr(Wr), _ptr(bias), ctypes.byref(experts.struct), T, k,
+                                _ptr(logits), _ptr(idx), _ptr(w), _ptr(y), _ptr(ws),
+                                0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+           "maple_moe_layer")
+
+
 def maple_moe_ffn_static_scratch(experts: Experts, x, idx, w, y, stream=None):
     """maple_moe_ffn for callers that cannot allocate: the library's static per-GPU
-    scratch array stands in for the workspace (T * k * I * 4 bytes plus a few KB must
-    fit in 2 MiB).  Calls that overlap on the GPU share that array and must be
+    scratch array stands in for the workspace (maple_moe_ffn_workspace_size must not
+    exceed 2 MiB).  Calls that overlap on the GPU share that array and must be
     serialised by the caller."""
     T, H = x.shape
     k = idx.shape[1]

@@ -141,3 +141,27 @@ def test_moe_ffn_validation(lib):
     assert f(ctypes.byref(ex), None, None, None, 0, 8, None, None, 0, None) == 0
     assert f(ctypes.byref(_experts(lib, clamp=math.inf)), None, None, None, 0, 8, None, None, 0,
              None) == 0
+
+
+def test_moe_layer_validation(lib):
+    from ternary_weight_moe_02_b300.maple import maple_experts
+    wsz = lib.maple_moe_layer_workspace_size
+    wsz.argtypes = [I32, I32, ctypes.POINTER(maple_experts)]
+    wsz.restype = ctypes.c_size_t
+    f = lib.maple_moe_layer
+    f.argtypes = [P, P, P, ctypes.POINTER(maple_experts), I32, I32, P, P, P, P, P, ctypes.c_size_t, P]
+    ex = _experts(lib)
+    need = wsz(1, 8, ctypes.byref(ex))
+    ffn = lib.maple_moe_ffn_workspace_size
+    ffn.argtypes = [I32, I32, ctypes.POINTER(maple_experts)]
+    ffn.restype = ctypes.c_size_t
+    assert need == 256 + ffn(1, 8, ctypes.byref(ex))
+    good = (A16, A16, None, ctypes.byref(ex), 1, 8, A16, A16, A16, A16, A16, need, None)
+    assert f(*good[:3], None, *good[4:]) == -1
+    assert f(A16, A16, None, ctypes.byref(ex), 1, 0, A16, A16, A16, A16, A16, need, None) == -1
+    assert f(A16, A16, None, ctypes.byref(ex), 1, 257, A16, A16, A16, A16, A16, need, None) == -1
+    assert f(A16, A16, None, ctypes.byref(ex), 1, 33, A16, A16, A16, A16, A16, need, None) == -2
+    assert f(A16 + 8, A16, None, ctypes.byref(ex), 1, 8, A16, A16, A16, A16, A16, need, None) == -3
+    assert f(A16, A16, None, ctypes.byref(ex), 1, 8, A16, A16, A16, A16, A16, need - 1, None) == -7
+    assert f(A16, A16, None, ctypes.byref(ex), 1, 8, None, A16, A16, A16, A16, need, None) == -1
+    assert f(None, None, None, ctypes.byref(ex), 0, 8, None, None, None, None, None, 0, None) == 0

@@ -136,13 +136,15 @@ def test_ffn_prefill_4096_sampled(layer256, router256):
     _compare(packed, ex, x, idx, w32, rows=sorted(rows), what="prefill sample")
 
 
-def test_ffn_invalid_and_duplicate_ids():
-    E, H, I, T, k = 6, 40, 24, 3, 4
-    w = synth.expert_weights(E, H, I, seed=8, std=0.2)
+@pytest.mark.parametrize("E,H,I", [(6, 40, 24), (8, 2048, 512)])
+def test_ffn_invalid_and_duplicate_ids(E, H, I):
+    """Generic path (H=40, I=24) and bulk-copy path (H=2048, I=512)."""
+    T, k = 3, 4
+    w = synth.expert_weights(E, H, I, seed=8, std=0.2, device="cuda")
     packed = oracle_pack_layer(w)
     ex = upload_experts(packed)
     x = synth.tokens(T, H, seed=8)
-    idx = np.array([[0, 0, 5, 2], [-1, 3, 6, 1], [4, 4, 4, 4]], np.int32)
+    idx = np.array([[0, 0, 5, 2], [-1, 3, E, 1], [4, 4, 4, 4]], np.int32)
     w32 = np.array([[0.4, 0.3, 0.2, 0.1], [0.5, 0.2, 0.2, 0.1], [0.25] * 4], np.float32)
     y_gpu = run_ffn(ex, x.cuda(), torch.from_numpy(idx).cuda(), torch.from_numpy(w32).cuda())
     torch.cuda.synchronize()
@@ -152,6 +154,20 @@ def test_ffn_invalid_and_duplicate_ids():
     y_ref = oracle.moe_ffn(packed["gate"], packed["up"], packed["down"], packed["s_gate"],
                            packed["s_up"], packed["s_down"], synth.bf16_bits(x), idx_ref, w_ref)
     assert_ffn_close(y_gpu.cpu().numpy(), y_ref, "invalid/duplicate ids")
+
+
+@pytest.mark.parametrize("k,T", [(12, 3), (13, 2), (1, 5)])
+def test_ffn_k_range_full_shape(k, T):
+    """k = 12 is the largest k of the bulk-copy down kernel; 13 falls back to the
+    generic down kernel; k = 1 is a single expert per token."""
+    E, H, I = 16, 2048, 512
+    w = synth.expert_weights(E, H, I, seed=30 + k, device="cuda")
+    packed = oracle_pack_layer(w)
+    ex = upload_experts(packed)
+    rng = np.random.default_rng(k)
+    idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    w32 = rng.dirichlet(np.ones(k), size=T).astype(np.float32)
+    _compare(packed, ex, synth.tokens(T, H, seed=k), idx, w32, what=f"k={k}")
 
 
 def test_ffn_all_zero_weights_give_zero():
@@ -165,6 +181,12 @@ def test_ffn_all_zero_weights_give_zero():
                 torch.full((T, k), 0.5).cuda())
     torch.cuda.synchronize()
     assert torch.all(y == 0)
+
+
+def test_device_status_is_clean_after_the_suite():
+    """No bounded device wait gave up in any kernel launched so far in this process."""
+    from ternary_weight_moe_02_b300 import maple
+    maple.maple_check_device_status()
 
 
 def test_ffn_is_deterministic(layer256, router256):

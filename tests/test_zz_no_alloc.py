@@ -73,6 +73,8 @@ def test_static_scratch_rejects_sizes_beyond_the_array():
     E, H, I, k = 16, 2048, 512, 8
     ex = _experts(E, H, I, seed=3)
     T = 128  # 128 tokens x 8 slots x 512 rows x 4 B = 2 MiB of h alone
+    assert maple.maple_moe_ffn_workspace_size(T, k, ex) > 2 << 20
+    assert maple.maple_moe_ffn_workspace_size(127, k, ex) <= 2 << 20
     x, idx, w = _inputs(T, E, H, k, seed=3)
     y = torch.full((T, H), 7.0, device="cuda")
     with pytest.raises(maple.MapleError) as err:
