@@ -297,6 +297,8 @@ def run_gpu(args, world, rank, local):
     e2e_s = _max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
     e2e_value = world * n_e2e / e2e_s
 
+    secondary = run_secondary(maple, synth, layers, dev, stream) if args.secondary else None
+
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_max * 1e3 / args.steps,
@@ -321,7 +323,98 @@ def run_gpu(args, world, rank, local):
                 "h2d_bytes_per_step": H * 2, "d2h_bytes_per_step": H * 4},
         "clocks": clocks.summary(),
     }
+    if secondary is not None:
+        result["secondary"] = secondary
     return result
+
+
+# ------------------------------------------------------------- secondary workloads
+
+def run_secondary(maple, synth, layers, dev, stream):
+    """Other configurations of the same path, measured briefly (not the headline):
+    decode batches over 24 stacked layers with a N(0,0.5) router bias, the 4096-token
+    prefill with a Zipf(1.1) bias, and ternarize + pack throughput on whole layers."""
+    out = {}
+    n_stack = min(24, len(layers))
+
+    def timed_graph(fn, n_steps, reps=3):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for i in range(2):
+                fn(i)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n_steps):
+                    fn(i)
+            g.replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) / 1e3 / (reps * n_steps)
+
+    for T in (8, 64):
+        xs = [synth.tokens(T, H, seed=100 + l, device=dev) for l in range(n_stack)]
+        biases = [synth.bias_normal(E, seed=200 + l).to(dev) for l in range(n_stack)]
+        logits = torch.empty((T, E), device=dev)
+        idx = torch.empty((T, K_TOP), dtype=torch.int32, device=dev)
+        w = torch.empty((T, K_TOP), device=dev)
+        y = torch.empty((T, H), device=dev)
+        ws = torch.zeros(maple.maple_moe_layer_workspace_size(T, K_TOP, layers[0][0]), dtype=torch.uint8,
+                         device=dev)
+
+        def layer(i, T=T, xs=xs, biases=biases, logits=logits, idx=idx, w=w, y=y, ws=ws):
+            ex, router = layers[i % n_stack]
+            maple.maple_moe_layer(xs[i % n_stack], router, biases[i % n_stack], ex, K_TOP, logits, idx,
+                                  w, y, ws, stream=stream)
+        sec = timed_graph(layer, n_stack)
+        out[f"decode_b{T}"] = {"value": T / sec, "unit": "tokens/s", "ms_per_layer": sec * 1e3,
+                               "layers": n_stack, "bias": "N(0, 0.5) per expert"}
+
+    T = 4096
+    x = synth.tokens(T, H, seed=300, device=dev)
+    bias = synth.bias_zipf(E, seed=0, gamma=1.0).to(dev)
+    logits = torch.empty((T, E), device=dev)
+    idx = torch.empty((T, K_TOP), dtype=torch.int32, device=dev)
+    w = torch.empty((T, K_TOP), device=dev)
+    y = torch.empty((T, H), device=dev)
+    ws = torch.zeros(maple.maple_moe_layer_workspace_size(T, K_TOP, layers[0][0]), dtype=torch.uint8,
+                     device=dev)
+
+    def prefill(i):
+        ex, router = layers[i % n_stack]
+        maple.maple_moe_layer(x, router, bias, ex, K_TOP, logits, idx, w, y, ws, stream=stream)
+    sec = timed_graph(prefill, 2, reps=2)
+    flops = 2 * 3 * I * H * T * K_TOP
+    out["prefill_4096"] = {"value": T / sec, "unit": "tokens/s", "ms_per_layer": sec * 1e3,
+                           "dense_equiv_tflops": flops / sec / 1e12, "bias": "Zipf(1.1) ranking"}
+
+    # ternarize + pack of whole layers (all 768 matrices of a layer per chunk)
+    n_pack = 2
+    wts = [synth.expert_weights(E, H, I, seed=5000 + l, device=dev) for l in range(n_pack)]
+    Bh, Bi = (H + 4) // 5, (I + 4) // 5
+    pk = {"gate": torch.empty((E * I, Bh), dtype=torch.uint8, device=dev),
+          "up": torch.empty((E * I, Bh), dtype=torch.uint8, device=dev),
+          "down": torch.empty((E * H, Bi), dtype=torch.uint8, device=dev)}
+    sc = {"gate": torch.empty(E * I, device=dev), "up": torch.empty(E * I, device=dev),
+          "down": torch.empty(E * H, device=dev)}
+
+    def pack(i):
+        wl = wts[i % n_pack]
+        for name, K in (("gate", H), ("up", H), ("down", I)):
+            maple.maple_ternarize_pack(wl[name].view(-1, K), pk[name], sc[name], stream=stream)
+    sec = timed_graph(pack, n_pack, reps=3)
+    weights = 3 * E * H * I
+    bytes_moved = weights * 2 + E * (2 * I * Bh + H * Bi) + 4 * E * (2 * I + H)
+    peak, kind = _peaks()
+    out["ternarize_pack"] = {"value": bytes_moved / sec / 1e9, "unit": "GB/s",
+                             "frac_of_peak": bytes_moved / sec / 1e9 / peak,
+                             "ms_per_layer": sec * 1e3, "bytes_per_layer": bytes_moved,
+                             "weights_per_layer": weights, "peak_source": f"{kind} hbm_gbs"}
+    del wts
+    return out
 
 
 # ------------------------------------------------------------------- CPU (oracle) arm
@@ -389,6 +482,8 @@ def main():
     ap.add_argument("--chunk", type=int, default=1000, help="steps per captured graph")
     ap.add_argument("--ref-tokens", type=int, default=4, help="oracle tokens per reference step")
     ap.add_argument("--cpu-tokens", type=int, default=40, help="oracle tokens for cpu_baseline")
+    ap.add_argument("--secondary", type=int, default=1,
+                    help="also time decode b8/b64, the 4096-token prefill and ternarize+pack")
     args = ap.parse_args()
     world, rank, local = _dist()
     if args.warmup < 3:

@@ -86,6 +86,121 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Bulk-copy path (K % 8 == 0, 16-byte aligned W, K <= kPkMaxK).  Each warp streams
+// its rows (grid-stride) through two shared-memory row buffers: lane 0 bulk-copies the
+// next row while the warp works on the current one, so every row is read from DRAM
+// once.  The row sum reads 16-byte chunks; each output byte b (lane-strided) is built
+// from its five weights as 121 + P - N, where P / N add 3^i for weight i above +s/2 /
+// below -s/2 (the base-3 code with digit q + 1, written out).
+constexpr int kPkWarps = 8;
+constexpr int kPkMaxK = 8192;
+
+__global__ void __launch_bounds__(kPkWarps * 32)
+    ternarize_pack_tma_kernel(const uint16_t* __restrict__ W, int64_t rows, int K,
+                              uint8_t* __restrict__ packed, float* __restrict__ scales, int* status) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ __align__(8) uint64_t bars[kPkWarps][2];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rowbytes = 2 * K;  // a multiple of 16
+    uint16_t* const buf0 = reinterpret_cast<uint16_t*>(smem + (size_t)warp * 2 * rowbytes);
+    const int64_t gw = (int64_t)blockIdx.x * kPkWarps + warp;
+    const int64_t nw = (int64_t)gridDim.x * kPkWarps;
+    const int nb = (K + 4) / 5;
+    if (lane == 0) {
+        mbar_init(&bars[warp][0], 1);
+        mbar_init(&bars[warp][1], 1);
+    }
+    __syncwarp();
+    pdl_wait();
+    if (gw < rows && lane == 0) {
+        mbar_arrive_expect_tx(&bars[warp][0], rowbytes);
+        bulk_copy_g2s(buf0, W + gw * K, rowbytes, &bars[warp][0]);
+    }
+    uint32_t phase0 = 0, phase1 = 0;
+    int slot = 0;
+    bool ok = true;
+    for (int64_t r = gw; r < rows; r += nw) {
+        const int64_t rn = r + nw;
+        if (rn < rows && lane == 0) {
+            // the other buffer was last read (generic proxy) before the previous __syncwarp
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive_expect_tx(&bars[warp][slot ^ 1], rowbytes);
+            bulk_copy_g2s(buf0 + (slot ^ 1) * K, W + rn * K, rowbytes, &bars[warp][slot ^ 1]);
+        }
+        const uint32_t ph = slot ? phase1 : phase0;
+        if (!mbar_wait_bounded(&bars[warp][slot], ph, status)) ok = false;
+        if (slot)
+            phase1 ^= 1u;
+        else
+            phase0 ^= 1u;
+        if (!__all_sync(kFullMask, ok)) break;
+        const uint16_t* row = buf0 + slot * K;
+
+        // row sum of |w|: pairwise inside 16-byte chunks, Kahan across them, butterfly
+        float sum = 0.f, comp = 0.f;
+        const uint4* r4 = reinterpret_cast<const uint4*>(row);
+        for (int c = lane; c < (K >> 3); c += 32) {
+            const uint4 v = r4[c];
+            const float a0 = fabsf(bf16_lo(v.x)) + fabsf(bf16_hi(v.x));
+            const float a1 = fabsf(bf16_lo(v.y)) + fabsf(bf16_hi(v.y));
+            const float a2 = fabsf(bf16_lo(v.z)) + fabsf(bf16_hi(v.z));
+            const float a3 = fabsf(bf16_lo(v.w)) + fabsf(bf16_hi(v.w));
+            const float y = ((a0 + a1) + (a2 + a3)) - comp;
+            const float t = sum + y;
+            comp = (t - sum) - y;
+            sum = t;
+        }
+        const float total = warp_sum(sum - comp);
+        const float s = __fdiv_rn(total, (float)K);
+        const float thr = 0.5f * s;  // exact: |w| > s/2  <=>  round(|w|/s) >= 1
+
+        const uint32_t* row32 = reinterpret_cast<const uint32_t*>(row);
+        uint8_t* out = packed + r * nb;
+        for (int b = lane; b < nb; b += 32) {
+            const int e0 = 5 * b;             // first weight of the byte
+            const int wi = e0 >> 1;           // its 32-bit word
+            const uint32_t sh = (e0 & 1) * 16;
+            const uint32_t w0 = row32[wi], w1 = row32[wi + 1], w2 = row32[wi + 2];
+            const uint32_t v0 = __funnelshift_r(w0, w1, sh);  // weights e0, e0+1
+            const uint32_t v1 = __funnelshift_r(w1, w2, sh);  // e0+2, e0+3
+            const uint32_t v2 = __funnelshift_r(w2, w2, sh);  // e0+4 (low half)
+            const float f0 = __uint_as_float(v0 << 16), f1 = __uint_as_float(v0 & 0xffff0000u);
+            const float f2 = __uint_as_float(v1 << 16), f3 = __uint_as_float(v1 & 0xffff0000u);
+            const float f4 = __uint_as_float(v2 << 16);
+            int P = 0, N = 0;
+            if (e0 + 4 < K) {  // all five weights exist (every byte but a K-tail one)
+                P += (f0 > thr) ? 1 : 0;
+                N += (f0 < -thr) ? 1 : 0;
+                P += (f1 > thr) ? 3 : 0;
+                N += (f1 < -thr) ? 3 : 0;
+                P += (f2 > thr) ? 9 : 0;
+                N += (f2 < -thr) ? 9 : 0;
+                P += (f3 > thr) ? 27 : 0;
+                N += (f3 < -thr) ? 27 : 0;
+                P += (f4 > thr) ? 81 : 0;
+                N += (f4 < -thr) ? 81 : 0;
+            } else {
+                const float f[5] = {f0, f1, f2, f3, f4};
+                int place = 1;
+                for (int i = 0; i < 5 && e0 + i < K; ++i) {
+                    if (f[i] > thr) P += place;
+                    if (f[i] < -thr) N += place;
+                    place *= 3;
+                }
+            }
+            out[b] = (uint8_t)(121 + P - N);
+        }
+        if (lane == 0) scales[r] = s;
+        __syncwarp();  // every lane is done with this buffer before it is refilled
+        slot ^= 1;
+    }
+    // a row prefetched but not consumed (only after a failed wait) must land first
+    if (!ok && lane == 0) {
+        mbar_wait_bounded(&bars[warp][0], phase0, nullptr);
+        mbar_wait_bounded(&bars[warp][1], phase1, nullptr);
+    }
+}
+
 __global__ void __launch_bounds__(256)
     unpack_kernel(const uint8_t* __restrict__ packed, const float* __restrict__ scales,
                   int64_t rows, int64_t K, float* __restrict__ out, int32_t* bad_codes) {
@@ -118,6 +233,19 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_ternarize_pack(const uint16_t* W, int64_t rows, int64_t K, uint8_t* packed,
                                   float* scales, cudaStream_t stream, const DeviceInfo& dev) {
     const int vec = (K % 8 == 0) && (reinterpret_cast<uintptr_t>(W) % 16 == 0);
+    if (vec && K <= kPkMaxK) {
+        // two row buffers per warp, plus 16 bytes: the last byte's third 32-bit load may
+        // run past the end of the row (those weights are masked)
+        const size_t smem = (size_t)kPkWarps * 2 * 2 * K + 16;
+        cudaError_t err = ensure_dynamic_smem(ternarize_pack_tma_kernel, smem);
+        if (err != cudaSuccess) return err;
+        const int per_sm = smem <= 56 * 1024 ? 4 : (smem <= 110 * 1024 ? 2 : 1);
+        const int64_t want = (rows + kPkWarps - 1) / kPkWarps;
+        const int64_t cap = (int64_t)dev.sm_count * per_sm;
+        const int grid = (int)(want < cap ? want : cap);
+        return launch_pdl(ternarize_pack_tma_kernel, dim3(grid), dim3(kPkWarps * 32), smem, stream, W,
+                          rows, (int)K, packed, scales, dev.status);
+    }
     const int64_t want = (rows + 7) / 8;
     const int64_t cap = (int64_t)dev.sm_count * 8;
     const int grid = (int)(want < cap ? want : cap);

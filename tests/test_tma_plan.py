@@ -161,3 +161,17 @@ def test_fused_layer_plan_is_aligned_and_in_bounds():
                 checked += 1
     assert checked > 1000
     assert layer_ok(2048, 512, 256, 8) and layer_ok(2048, 512, 32, 8)
+
+
+def test_pack_plan_is_aligned_and_in_bounds():
+    """ternarize_pack's bulk-copy path: one copy of 2K bytes per row (K % 8 == 0, base
+    16-byte aligned), into one of two row buffers of a warp; the last byte's third
+    32-bit load may read up to 4 bytes past the row, inside the 16-byte pad."""
+    for K in (8, 16, 40, 512, 520, 2048, 4104, 8192):
+        rows = 37
+        for r in range(rows):
+            _check(r * 2 * K, 2 * K, rows * 2 * K, f"pack K={K} row {r}")
+        nb = nbytes(K)
+        last_word = (5 * (nb - 1)) // 2 + 2          # third word of the last byte
+        assert 4 * (last_word + 1) <= 2 * K + 16 + 2 * K  # within the two buffers + pad
+        assert 4 * (last_word + 1) - 2 * K <= 16       # at most 16 bytes past one row
