@@ -1,6 +1,7 @@
 // Device helpers shared by the CUDA kernels of libmaple (internal header).
 #pragma once
 
+#include <mutex>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -406,16 +407,38 @@ __device__ __forceinline__ void down_group_partials(int k, int I, int Bi, const 
 // Raise a kernel's dynamic shared-memory limit when it needs more than the default
 // 48 KB.  The attribute is per device; the last size set per (kernel, device) is
 // remembered so that steady-state launches make no extra driver call.
+// Raises a kernel's dynamic shared-memory limit once per (kernel, device).  The cache
+// is keyed by the kernel's address: template instances share a function type.
 template <typename Kernel>
 cudaError_t ensure_dynamic_smem(Kernel* kernel, size_t bytes) {
     if (bytes <= 48 * 1024) return cudaSuccess;
-    static size_t set_bytes[64] = {};
+    struct Entry {
+        const void* fn;
+        int dev;
+        size_t bytes;
+    };
+    constexpr int kEntries = 128;
+    static Entry cache[kEntries] = {};
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    if (dev >= 0 && dev < 64 && set_bytes[dev] >= bytes) return cudaSuccess;
+    const void* fn = reinterpret_cast<const void*>(kernel);
+    int slot = -1;
+    for (int i = 0; i < kEntries; ++i) {
+        if (cache[i].fn == fn && cache[i].dev == dev) {
+            if (cache[i].bytes >= bytes) return cudaSuccess;
+            slot = i;
+            break;
+        }
+        if (cache[i].fn == nullptr) {
+            slot = i;
+            break;
+        }
+    }
     err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (err == cudaSuccess && dev >= 0 && dev < 64) set_bytes[dev] = bytes;
+    if (err == cudaSuccess && slot >= 0) cache[slot] = Entry{fn, dev, bytes};
     return err;
 }
 

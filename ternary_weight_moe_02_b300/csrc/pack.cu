@@ -86,119 +86,214 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// Bulk-copy path (K % 8 == 0, 16-byte aligned W, K <= kPkMaxK).  Each warp streams
-// its rows (grid-stride) through two shared-memory row buffers: lane 0 bulk-copies the
-// next row while the warp works on the current one, so every row is read from DRAM
-// once.  The row sum reads 16-byte chunks; each output byte b (lane-strided) is built
-// from its five weights as 121 + P - N, where P / N add 3^i for weight i above +s/2 /
-// below -s/2 (the base-3 code with digit q + 1, written out).
-constexpr int kPkWarps = 8;
-constexpr int kPkMaxK = 8192;
+// Bulk-copy path (K % 8 == 0, 16-byte aligned W, two stages of R row slots per warp
+// fit in shared memory).  Each warp streams blocks of R consecutive rows (R a power of
+// two, chosen so that a block is about 4 KB) through two stages: lane 0 issues the next
+// block's row copies while the warp packs the current one, so every row is read from
+// DRAM once.  A row slot is 2K bytes followed by kPkPad zero bytes, which the last,
+// ragged unit of a row reads as +0 weights (digit 1, the zero trit).  Within a stage,
+// G = 32 / R lanes own each row: they sum it, reduce among themselves, and pack it.
+//
+// Per row: the sum of |w| reads 16-byte chunks (Kahan across pairs of chunks).  The
+// packing then works on units of ten weights (five 32-bit words, two output bytes) with
+// integer arithmetic only:
+//   * |w| > thr, for a bf16 w and an fp32 thr >= 0, is the same test as |w| > t where
+//     t is thr truncated to bf16 (the largest bf16 <= thr); on the 15-bit magnitudes of
+//     both halves of a word at once it is bit 15 of (|w| + 0x7fff - t), which never
+//     carries out of its half;
+//   * the base-3 digit q + 1 of a weight is 2p + z, p = (|w| > thr and w > 0), z = not
+//     (|w| > thr); trit_field puts p at bit 15 and z at bit 14 of each half, so each half
+//     holds (q + 1) * 2^14;
+//   * mul.hi by c_lo * 2^18 + c_hi * 4 gives c_lo (q_lo + 1) + c_hi (q_hi + 1) in the
+//     low 16 bits (the higher bits get a harmless c_lo * 2^16 term), so three products
+//     summed give a byte's code, the sum over five weights of 3^i (q_i + 1).
+constexpr int kPkMaxWarps = 8;
+constexpr int kPkStageBytes = 4096;
+constexpr int kPkMaxK = 49152;
+constexpr int kPkPad = 32;
 
-__global__ void __launch_bounds__(kPkWarps * 32)
+template <uint32_t kLut>
+__device__ __forceinline__ uint32_t lop3(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, %4;" : "=r"(d) : "r"(a), "r"(b), "r"(c), "n"(kLut));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t trit_field(uint32_t x, uint32_t c2) {
+    const uint32_t y = (x & 0x7fff7fffu) + c2;             // bit 15 of a half: |w| > threshold
+    const uint32_t p = lop3<0x20>(y, x, 0x80008000u);      // y & ~x & mask: above, positive
+    return lop3<0xF2>(p, y >> 1, 0x40004000u);             // p | (~(y >> 1) & mask): not above
+}
+
+// multipliers c_lo * 2^18 + c_hi * 4 for the words of a ten-weight unit: byte A takes
+// weights 0..4 (3^0..3^4), byte B weights 5..9; word 2 holds weight 4 and weight 5
+__host__ __device__ constexpr uint32_t pk_mul(uint32_t c_lo, uint32_t c_hi) {
+    return (c_lo << 18) | (c_hi << 2);
+}
+
+__device__ __forceinline__ uint32_t pack_unit(const uint32_t* w, uint32_t c2) {
+    const uint32_t f0 = trit_field(w[0], c2), f1 = trit_field(w[1], c2), f2 = trit_field(w[2], c2);
+    const uint32_t f3 = trit_field(w[3], c2), f4 = trit_field(w[4], c2);
+    const uint32_t a = __umulhi(f0, pk_mul(1, 3)) + __umulhi(f1, pk_mul(9, 27)) + __umulhi(f2, pk_mul(81, 0));
+    const uint32_t b = __umulhi(f2, pk_mul(0, 1)) + __umulhi(f3, pk_mul(3, 9)) + __umulhi(f4, pk_mul(27, 81));
+    return __byte_perm(a, b, 0x0040);  // byte 0: code A, byte 1: code B
+}
+
+__device__ __forceinline__ float chunk_abs_sum(uint4 v) {
+    const float a0 = fabsf(bf16_lo(v.x)) + __uint_as_float(v.x & 0x7fff0000u);
+    const float a1 = fabsf(bf16_lo(v.y)) + __uint_as_float(v.y & 0x7fff0000u);
+    const float a2 = fabsf(bf16_lo(v.z)) + __uint_as_float(v.z & 0x7fff0000u);
+    const float a3 = fabsf(bf16_lo(v.w)) + __uint_as_float(v.w & 0x7fff0000u);
+    return (a0 + a1) + (a2 + a3);
+}
+
+// Sum of |w| over a row slot, as every lane of the row's G-lane group sees it (j: the
+// lane's index in the group).
+template <int G>
+__device__ __forceinline__ float group_row_abs_sum(const uint4* r4, int n4, int j) {
+    float sum = 0.f, comp = 0.f;
+    for (int c = j; c < n4; c += 2 * G) {
+        const uint4 v0 = r4[c];
+        const uint4 v1 = c + G < n4 ? r4[c + G] : make_uint4(0u, 0u, 0u, 0u);
+        const float y = (chunk_abs_sum(v0) + chunk_abs_sum(v1)) - comp;
+        const float t = sum + y;
+        comp = (t - sum) - y;
+        sum = t;
+    }
+    float v = sum - comp;
+#pragma unroll
+    for (int o = G / 2; o >= 1; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);
+    return v;
+}
+
+// Packs the units j, j + G, ... of one row slot (two per loop trip).
+template <int G, bool kPairStores>
+__device__ __forceinline__ void group_pack_row(const uint32_t* row32, int units, int nb, int j,
+                                               uint32_t c2, uint8_t* __restrict__ out) {
+    auto store = [&](int u, uint32_t ab) {
+        if (kPairStores) {
+            reinterpret_cast<uint16_t*>(out)[u] = (uint16_t)ab;  // nb even: every unit has A and B
+        } else {
+            out[2 * u] = (uint8_t)ab;
+            if (2 * u + 1 < nb) out[2 * u + 1] = (uint8_t)(ab >> 8);
+        }
+    };
+    int u = j;
+    for (; u + G < units; u += 2 * G) {
+        const uint32_t ab0 = pack_unit(row32 + 5 * u, c2);
+        const uint32_t ab1 = pack_unit(row32 + 5 * (u + G), c2);
+        store(u, ab0);
+        store(u + G, ab1);
+    }
+    if (u < units) store(u, pack_unit(row32 + 5 * u, c2));
+}
+
+template <int G, bool kPairStores>
+__global__ void __launch_bounds__(kPkMaxWarps * 32)
     ternarize_pack_tma_kernel(const uint16_t* __restrict__ W, int64_t rows, int K,
                               uint8_t* __restrict__ packed, float* __restrict__ scales, int* status) {
+    constexpr int R = 32 / G;  // rows per block
     extern __shared__ __align__(16) unsigned char smem[];
-    __shared__ __align__(8) uint64_t bars[kPkWarps][2];
+    __shared__ __align__(8) uint64_t bars[kPkMaxWarps][2];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rowbytes = 2 * K;  // a multiple of 16
-    uint16_t* const buf0 = reinterpret_cast<uint16_t*>(smem + (size_t)warp * 2 * rowbytes);
-    const int64_t gw = (int64_t)blockIdx.x * kPkWarps + warp;
-    const int64_t nw = (int64_t)gridDim.x * kPkWarps;
+    const int nwarps = blockDim.x >> 5;
+    const int rowbytes = 2 * K;              // a multiple of 16
+    const int slot = rowbytes + kPkPad;      // row slot stride
+    const int stagebytes = R * slot;
+    unsigned char* const stage0 = smem + (size_t)warp * 2 * stagebytes;
+    const int64_t nblk = (rows + R - 1) / R;
+    const int64_t gw = (int64_t)blockIdx.x * nwarps + warp;
+    const int64_t nw = (int64_t)gridDim.x * nwarps;
     const int nb = (K + 4) / 5;
+    const int units = (nb + 1) >> 1;         // the last one holds only byte A when nb is odd
+    const int q = lane / G, j = lane % G;    // this lane's row in a block, index in its group
+    // zero the pads after the 2R row slots; copies never write them
+    for (int i = lane; i < 2 * R * (kPkPad / 16); i += 32) {
+        const int sl = i / (kPkPad / 16), part = i % (kPkPad / 16);
+        *reinterpret_cast<uint4*>(stage0 + sl * slot + rowbytes + 16 * part) = make_uint4(0u, 0u, 0u, 0u);
+    }
     if (lane == 0) {
         mbar_init(&bars[warp][0], 1);
         mbar_init(&bars[warp][1], 1);
     }
     __syncwarp();
     pdl_wait();
-    if (gw < rows && lane == 0) {
-        mbar_arrive_expect_tx(&bars[warp][0], rowbytes);
-        bulk_copy_g2s(buf0, W + gw * K, rowbytes, &bars[warp][0]);
-    }
+    auto issue = [&](int64_t blk, int st) {
+        const int64_t r0 = blk * R;
+        const int64_t left = rows - r0;
+        const int n = (int)(left < R ? left : R);
+        mbar_arrive_expect_tx(&bars[warp][st], (uint32_t)(n * rowbytes));
+        for (int i = 0; i < n; ++i)
+            bulk_copy_g2s(stage0 + st * stagebytes + i * slot, W + (r0 + i) * K, (uint32_t)rowbytes,
+                          &bars[warp][st]);
+    };
+    if (gw < nblk && lane == 0) issue(gw, 0);
     uint32_t phase0 = 0, phase1 = 0;
-    int slot = 0;
+    int st = 0;
     bool ok = true;
-    for (int64_t r = gw; r < rows; r += nw) {
-        const int64_t rn = r + nw;
-        if (rn < rows && lane == 0) {
-            // the other buffer was last read (generic proxy) before the previous __syncwarp
+    for (int64_t blk = gw; blk < nblk; blk += nw) {
+        if (blk + nw < nblk && lane == 0) {
+            // the other stage was last read (generic proxy) before the previous __syncwarp
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive_expect_tx(&bars[warp][slot ^ 1], rowbytes);
-            bulk_copy_g2s(buf0 + (slot ^ 1) * K, W + rn * K, rowbytes, &bars[warp][slot ^ 1]);
+            issue(blk + nw, st ^ 1);
         }
-        const uint32_t ph = slot ? phase1 : phase0;
-        if (!mbar_wait_bounded(&bars[warp][slot], ph, status)) ok = false;
-        if (slot)
+        const uint32_t ph = st ? phase1 : phase0;
+        if (!mbar_wait_bounded(&bars[warp][st], ph, status)) ok = false;
+        if (st)
             phase1 ^= 1u;
         else
             phase0 ^= 1u;
         if (!__all_sync(kFullMask, ok)) break;
-        const uint16_t* row = buf0 + slot * K;
-
-        // row sum of |w|: pairwise inside 16-byte chunks, Kahan across them, butterfly
-        float sum = 0.f, comp = 0.f;
-        const uint4* r4 = reinterpret_cast<const uint4*>(row);
-        for (int c = lane; c < (K >> 3); c += 32) {
-            const uint4 v = r4[c];
-            const float a0 = fabsf(bf16_lo(v.x)) + fabsf(bf16_hi(v.x));
-            const float a1 = fabsf(bf16_lo(v.y)) + fabsf(bf16_hi(v.y));
-            const float a2 = fabsf(bf16_lo(v.z)) + fabsf(bf16_hi(v.z));
-            const float a3 = fabsf(bf16_lo(v.w)) + fabsf(bf16_hi(v.w));
-            const float y = ((a0 + a1) + (a2 + a3)) - comp;
-            const float t = sum + y;
-            comp = (t - sum) - y;
-            sum = t;
+        const int64_t r = blk * R + q;
+        // a group whose row is past the end (last block) sums its stale slot harmlessly
+        // and stores nothing
+        const unsigned char* rowp = stage0 + st * stagebytes + q * slot;
+        const float total = group_row_abs_sum<G>(reinterpret_cast<const uint4*>(rowp), K >> 3, j);
+        if (r < rows) {
+            const float s = __fdiv_rn(total, (float)K);
+            const uint32_t t16 = (__float_as_uint(0.5f * s) >> 16) & 0x7fffu;
+            const uint32_t c2 = (0x7fffu - t16) * 0x10001u;
+            group_pack_row<G, kPairStores>(reinterpret_cast<const uint32_t*>(rowp), units, nb, j, c2,
+                                           packed + r * nb);
+            if (j == 0) scales[r] = s;
         }
-        const float total = warp_sum(sum - comp);
-        const float s = __fdiv_rn(total, (float)K);
-        const float thr = 0.5f * s;  // exact: |w| > s/2  <=>  round(|w|/s) >= 1
-
-        const uint32_t* row32 = reinterpret_cast<const uint32_t*>(row);
-        uint8_t* out = packed + r * nb;
-        for (int b = lane; b < nb; b += 32) {
-            const int e0 = 5 * b;             // first weight of the byte
-            const int wi = e0 >> 1;           // its 32-bit word
-            const uint32_t sh = (e0 & 1) * 16;
-            const uint32_t w0 = row32[wi], w1 = row32[wi + 1], w2 = row32[wi + 2];
-            const uint32_t v0 = __funnelshift_r(w0, w1, sh);  // weights e0, e0+1
-            const uint32_t v1 = __funnelshift_r(w1, w2, sh);  // e0+2, e0+3
-            const uint32_t v2 = __funnelshift_r(w2, w2, sh);  // e0+4 (low half)
-            const float f0 = __uint_as_float(v0 << 16), f1 = __uint_as_float(v0 & 0xffff0000u);
-            const float f2 = __uint_as_float(v1 << 16), f3 = __uint_as_float(v1 & 0xffff0000u);
-            const float f4 = __uint_as_float(v2 << 16);
-            int P = 0, N = 0;
-            if (e0 + 4 < K) {  // all five weights exist (every byte but a K-tail one)
-                P += (f0 > thr) ? 1 : 0;
-                N += (f0 < -thr) ? 1 : 0;
-                P += (f1 > thr) ? 3 : 0;
-                N += (f1 < -thr) ? 3 : 0;
-                P += (f2 > thr) ? 9 : 0;
-                N += (f2 < -thr) ? 9 : 0;
-                P += (f3 > thr) ? 27 : 0;
-                N += (f3 < -thr) ? 27 : 0;
-                P += (f4 > thr) ? 81 : 0;
-                N += (f4 < -thr) ? 81 : 0;
-            } else {
-                const float f[5] = {f0, f1, f2, f3, f4};
-                int place = 1;
-                for (int i = 0; i < 5 && e0 + i < K; ++i) {
-                    if (f[i] > thr) P += place;
-                    if (f[i] < -thr) N += place;
-                    place *= 3;
-                }
-            }
-            out[b] = (uint8_t)(121 + P - N);
-        }
-        if (lane == 0) scales[r] = s;
-        __syncwarp();  // every lane is done with this buffer before it is refilled
-        slot ^= 1;
+        __syncwarp();  // every lane is done with this stage before it is refilled
+        st ^= 1;
     }
-    // a row prefetched but not consumed (only after a failed wait) must land first
+    // a block prefetched but not consumed (only after a failed wait) must land first
     if (!ok && lane == 0) {
         mbar_wait_bounded(&bars[warp][0], phase0, nullptr);
         mbar_wait_bounded(&bars[warp][1], phase1, nullptr);
     }
+}
+
+template <int G, bool kPairStores>
+cudaError_t launch_pack_tma(const uint16_t* W, int64_t rows, int K, uint8_t* packed, float* scales,
+                            int warps, cudaStream_t stream, const DeviceInfo& dev) {
+    constexpr int R = 32 / G;
+    auto kernel = ternarize_pack_tma_kernel<G, kPairStores>;
+    const size_t smem = (size_t)warps * 2 * R * (2 * (size_t)K + kPkPad);
+    cudaError_t err = ensure_dynamic_smem(kernel, smem);
+    if (err != cudaSuccess) return err;
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, warps * 32, smem);
+    if (err != cudaSuccess) return err;
+    per_sm = per_sm < 1 ? 1 : per_sm;
+    const int64_t nblk = (rows + R - 1) / R;
+    const int64_t want = (nblk + warps - 1) / warps;
+    const int64_t cap = (int64_t)dev.sm_count * per_sm;
+    const int grid = (int)(want < cap ? want : cap);
+    return launch_pdl(kernel, dim3(grid), dim3(warps * 32), smem, stream, W, rows, K, packed, scales,
+                      dev.status);
+}
+
+template <int G>
+cudaError_t launch_pack_tma_g(const uint16_t* W, int64_t rows, int K, uint8_t* packed, float* scales,
+                              int warps, cudaStream_t stream, const DeviceInfo& dev) {
+    const int nb = (K + 4) / 5;
+    if (nb % 2 == 0 && reinterpret_cast<uintptr_t>(packed) % 2 == 0)
+        return launch_pack_tma<G, true>(W, rows, K, packed, scales, warps, stream, dev);
+    return launch_pack_tma<G, false>(W, rows, K, packed, scales, warps, stream, dev);
 }
 
 __global__ void __launch_bounds__(256)
@@ -234,17 +329,23 @@ cudaError_t launch_ternarize_pack(const uint16_t* W, int64_t rows, int64_t K, ui
                                   float* scales, cudaStream_t stream, const DeviceInfo& dev) {
     const int vec = (K % 8 == 0) && (reinterpret_cast<uintptr_t>(W) % 16 == 0);
     if (vec && K <= kPkMaxK) {
-        // two row buffers per warp, plus 16 bytes: the last byte's third 32-bit load may
-        // run past the end of the row (those weights are masked)
-        const size_t smem = (size_t)kPkWarps * 2 * 2 * K + 16;
-        cudaError_t err = ensure_dynamic_smem(ternarize_pack_tma_kernel, smem);
-        if (err != cudaSuccess) return err;
-        const int per_sm = smem <= 56 * 1024 ? 4 : (smem <= 110 * 1024 ? 2 : 1);
-        const int64_t want = (rows + kPkWarps - 1) / kPkWarps;
-        const int64_t cap = (int64_t)dev.sm_count * per_sm;
-        const int grid = (int)(want < cap ? want : cap);
-        return launch_pdl(ternarize_pack_tma_kernel, dim3(grid), dim3(kPkWarps * 32), smem, stream, W,
-                          rows, (int)K, packed, scales, dev.status);
+        // rows per block: the largest power of two <= 32 whose block is at most ~4 KB
+        const int rowbytes = 2 * (int)K;
+        int R = 1;
+        while (R < 32 && 2 * R * rowbytes <= kPkStageBytes) R *= 2;
+        const size_t per_warp = (size_t)2 * R * (rowbytes + kPkPad);  // two stages
+        int warps = (int)((dev.smem_optin - 1024) / per_warp);
+        warps = warps > kPkMaxWarps ? kPkMaxWarps : warps;
+        if (warps >= 1) {
+            switch (R) {
+                case 1: return launch_pack_tma_g<32>(W, rows, (int)K, packed, scales, warps, stream, dev);
+                case 2: return launch_pack_tma_g<16>(W, rows, (int)K, packed, scales, warps, stream, dev);
+                case 4: return launch_pack_tma_g<8>(W, rows, (int)K, packed, scales, warps, stream, dev);
+                case 8: return launch_pack_tma_g<4>(W, rows, (int)K, packed, scales, warps, stream, dev);
+                case 16: return launch_pack_tma_g<2>(W, rows, (int)K, packed, scales, warps, stream, dev);
+                default: return launch_pack_tma_g<1>(W, rows, (int)K, packed, scales, warps, stream, dev);
+            }
+        }
     }
     const int64_t want = (rows + 7) / 8;
     const int64_t cap = (int64_t)dev.sm_count * 8;

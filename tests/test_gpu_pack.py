@@ -25,7 +25,8 @@ def _gpu_pack(w):
 
 
 @pytest.mark.parametrize("rows,K", [(1, 1), (3, 4), (5, 5), (4, 13), (7, 16), (33, 2047),
-                                    (64, 2048), (130, 512), (17, 1000), (9, 4101)])
+                                    (64, 2048), (130, 512), (17, 1000), (9, 4101), (11, 8),
+                                    (600, 16), (77, 4104), (50, 520), (3, 16384), (2, 49152)])
 def test_pack_parity_shapes(rows, K):
     w = synth.bf16_normal((rows, K), 0.02, seed=rows * 1000 + K).cuda()
     gp, gs = _gpu_pack(w)

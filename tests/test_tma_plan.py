@@ -7,6 +7,8 @@ check that all of them start on a 16-byte boundary, have a size that is a multip
 a misaligned bulk copy faults the GPU, so this runs on the CPU first."""
 import itertools
 
+import numpy as np
+
 GU_ROWS = 8      # row pairs per gate/up CTA
 DN_ROWS = 16     # output rows per down CTA
 DN_MAX_K = 12
@@ -163,15 +165,119 @@ def test_fused_layer_plan_is_aligned_and_in_bounds():
     assert layer_ok(2048, 512, 256, 8) and layer_ok(2048, 512, 32, 8)
 
 
+PK_MAX_WARPS = 8
+PK_STAGE_BYTES = 4096
+PK_MAX_K = 49152
+PK_PAD = 32
+
+
+def pack_plan(K, smem_optin=232448):
+    """(rows per stage R, warps per CTA, dynamic shared memory) of the bulk-copy pack
+    path, or None where the generic path runs; restates the launcher in csrc/pack.cu."""
+    if K % 8 or K > PK_MAX_K:
+        return None
+    rowbytes = 2 * K
+    R = 1
+    while R < 32 and 2 * R * rowbytes <= PK_STAGE_BYTES:
+        R *= 2
+    per_warp = 2 * R * (rowbytes + PK_PAD)
+    warps = min(PK_MAX_WARPS, (smem_optin - 1024) // per_warp)
+    if warps < 1:
+        return None
+    return R, warps, per_warp * warps
+
+
 def test_pack_plan_is_aligned_and_in_bounds():
-    """ternarize_pack's bulk-copy path: one copy of 2K bytes per row (K % 8 == 0, base
-    16-byte aligned), into one of two row buffers of a warp; the last byte's third
-    32-bit load may read up to 4 bytes past the row, inside the 16-byte pad."""
-    for K in (8, 16, 40, 512, 520, 2048, 4104, 8192):
-        rows = 37
-        for r in range(rows):
-            _check(r * 2 * K, 2 * K, rows * 2 * K, f"pack K={K} row {r}")
+    """ternarize_pack's bulk-copy path: warps stream blocks of R rows (one 2K-byte copy
+    per row, into row slots of 2K + PK_PAD bytes) into one of two stages; every shared-
+    memory read of a row (16-byte chunks for the sum, five words per ten-weight unit)
+    stays inside its slot, and the ragged unit reads only the slot's zeroed pad."""
+    for K in (8, 16, 40, 512, 520, 2048, 4104, 8192, 16384, 49152):
+        R, warps, smem = pack_plan(K)
+        assert R in (1, 2, 4, 8, 16, 32) and (R == 1 or R * 2 * K <= PK_STAGE_BYTES)
+        assert smem + 128 + 1024 <= 232448
+        stage = R * 2 * K  # bytes copied per full block
+        for rows in (1, R - 1, R, 3 * R + 1, 37):
+            if rows < 1:
+                continue
+            nblk = -(-rows // R)
+            for b in range(nblk):
+                n = min(R, rows - b * R)
+                _check(b * R * 2 * K, n * 2 * K, rows * 2 * K, f"pack K={K} block {b}")
+                assert n * 2 * K <= stage
+        slot = 2 * K + PK_PAD
+        assert slot % 16 == 0
+        for w in range(warps):
+            for st in (0, 1):
+                for q in range(R):
+                    off = (w * 2 + st) * R * slot + q * slot
+                    assert off % 16 == 0 and off + slot <= smem
+        assert 16 * (K // 8) <= 2 * K                  # row-sum chunks
         nb = nbytes(K)
-        last_word = (5 * (nb - 1)) // 2 + 2          # third word of the last byte
-        assert 4 * (last_word + 1) <= 2 * K + 16 + 2 * K  # within the two buffers + pad
-        assert 4 * (last_word + 1) - 2 * K <= 16       # at most 16 bytes past one row
+        units = (nb + 1) // 2
+        assert units == -(-K // 10)
+        assert 4 * (5 * (units - 1) + 4) + 4 <= slot   # last unit's fifth word
+    assert pack_plan(49160) is None and pack_plan(2052) is None
+    assert pack_plan(512)[0] == 4 and pack_plan(2048)[0] == 1 and pack_plan(8)[0] == 32
+
+
+def _trit_field(x, c2):
+    y = ((x & 0x7FFF7FFF) + c2) & 0xFFFFFFFF
+    return (y & ~x & 0x80008000) | ((~y >> 1) & 0x40004000)
+
+
+def _mad_hi(a, b, c):
+    return (((a * b) >> 32) + c) & 0xFFFFFFFF
+
+
+def _pk_mul(lo, hi):
+    return (lo << 18) | (hi << 2)
+
+
+def _model_pack_unit(words, thr):
+    """The integer packing of ten bf16 weights (five 32-bit words) at threshold thr,
+    as csrc/pack.cu computes it; returns the two code bytes."""
+    t16 = (int(np.float32(thr).view(np.uint32)) >> 16) & 0x7FFF
+    c2 = (0x7FFF - t16) * 0x10001
+    f = [_trit_field(int(w), c2) for w in words]
+    a = _mad_hi(f[0], _pk_mul(1, 3), 0)
+    a = _mad_hi(f[1], _pk_mul(9, 27), a)
+    a = _mad_hi(f[2], _pk_mul(81, 0), a)
+    b = _mad_hi(f[2], _pk_mul(0, 1), 0)
+    b = _mad_hi(f[3], _pk_mul(3, 9), b)
+    b = _mad_hi(f[4], _pk_mul(27, 81), b)
+    return a & 0xFF, b & 0xFF
+
+
+def test_integer_pack_unit_matches_the_oracle_packing():
+    """The bit trick (bf16 threshold, digit fields, mad.hi sums) against the oracle's
+    five-trits-per-byte packing of the trits q = sign(w) [|w| > thr], compared in fp32;
+    thresholds are set on, just above and just below weight magnitudes."""
+    import oracle
+    rng = np.random.default_rng(5)
+    checked = 0
+    for trial in range(3000):
+        kind = trial % 4
+        if kind == 0:
+            w = rng.normal(0, 0.02, 10).astype(np.float32)
+        elif kind == 1:
+            w = rng.choice([0.0, -0.0, 1e-38, -3e-39, 5.0, -5.0, np.inf, -np.inf], 10).astype(np.float32)
+        else:
+            w = (rng.normal(0, 1, 10) * 10.0 ** rng.integers(-30, 30)).astype(np.float32)
+        bits = (w.view(np.uint32) >> 16).astype(np.uint32)  # truncate to bf16
+        wb = (bits << 16).view(np.float32)
+        mags = np.abs(wb[np.isfinite(wb)])
+        base = float(mags[rng.integers(len(mags))]) if len(mags) else 0.0
+        thr = np.float32(base)
+        if kind == 3:
+            thr = np.nextafter(thr, np.float32(np.inf)) if trial % 8 == 3 else np.nextafter(
+                thr, np.float32(0))
+        if not np.isfinite(thr):
+            continue
+        q = np.where(np.abs(wb) > thr, np.sign(wb), 0).astype(np.int8)
+        words = [int(bits[2 * i]) | (int(bits[2 * i + 1]) << 16) for i in range(5)]
+        got = _model_pack_unit(words, thr)
+        want = oracle.pack(q[None, :])[0]
+        assert got == (int(want[0]), int(want[1])), (w, thr, q)
+        checked += 1
+    assert checked > 2500
