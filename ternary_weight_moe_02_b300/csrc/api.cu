@@ -226,6 +226,10 @@ int maple_moe_ffn(const maple_experts* ex, const uint16_t* x, const int32_t* idx
     a.active = reinterpret_cast<int32_t*>(base + L.active);
     a.n_active = reinterpret_cast<int32_t*>(base + L.n_active);
     a.h = reinterpret_cast<float*>(base + L.h);
+    a.tile_off = reinterpret_cast<int32_t*>(base + L.tile_off);
+    a.xs = reinterpret_cast<uint16_t*>(base + L.xs);
+    a.hs = reinterpret_cast<uint16_t*>(base + L.hs);
+    a.ys = reinterpret_cast<float*>(base + L.ys);
     a.status = dev.status;
     cudaError_t err = maple::launch_moe_ffn(a, (cudaStream_t)stream, dev);
     if (err != cudaSuccess) return cuda_fail(err, "moe_ffn launch");

@@ -506,6 +506,18 @@ FfnWorkspaceLayout ffn_workspace_layout(int T, int k, int E, int H, int I) {
     o = align_up(o + 4, 256);
     L.h = o;
     o = align_up(o + 4 * S * (size_t)I, 256);
+    L.tensor = ffn_use_tensor(T, k, E, H, I);
+    L.tile_off = L.xs = L.hs = L.ys = o;
+    if (L.tensor) {
+        const size_t R = (size_t)ffn_tensor_b_rows((int)S);
+        o = align_up(o + 4 * ((size_t)E + 1), 256);
+        L.xs = o;
+        o = align_up(o + 2 * R * (size_t)H, 256);
+        L.hs = o;
+        o = align_up(o + 2 * R * (size_t)I, 256);
+        L.ys = o;
+        o = align_up(o + 4 * S * (size_t)H, 256);
+    }
     L.total = o;
     return L;
 }
@@ -514,6 +526,7 @@ cudaError_t launch_moe_ffn(const FfnArgs& args, cudaStream_t stream, const Devic
     FfnArgs a = args;
     const int64_t down_bytes = (int64_t)a.H * ((a.I + 4) / 5);
     a.prefetch_down = (down_bytes % 16 == 0 && a.H % 4 == 0) ? 1 : 0;
+    if (ffn_use_tensor(a.T, a.k, a.E, a.H, a.I)) return launch_moe_ffn_tensor(a, stream, dev);
     const int S = a.T * a.k;
     const int slot_mode = a.T == 1 ? 1 : 0;
     if (!slot_mode) {

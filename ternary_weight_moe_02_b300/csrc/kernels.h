@@ -57,17 +57,30 @@ struct FfnArgs {
     int32_t* perm;     // [T*k]
     int32_t* active;   // [E]
     int32_t* n_active; // [1]
-    float* h;          // [T*k][I]
+    float* h;          // [T*k][I] (bf16 [T*k][I] on the tensor path)
+    int32_t* tile_off; // [E+1] tensor path only
+    uint16_t* xs;      // [max(T*k, 128)][H] bf16, tensor path only
+    uint16_t* hs;      // [max(T*k, 128)][I] bf16, tensor path only
+    float* ys;         // [T*k][H] tensor path only
     int* status;       // device status word
     int prefetch_down; // 1 if the down rows may be bulk-prefetched (16-byte multiples)
 };
 
 struct FfnWorkspaceLayout {
-    size_t counts, offsets, perm, active, n_active, h, total;
+    size_t counts, offsets, perm, active, n_active, h, tile_off, xs, hs, ys, total;
+    bool tensor;
 };
 FfnWorkspaceLayout ffn_workspace_layout(int T, int k, int E, int H, int I);
 
 cudaError_t launch_moe_ffn(const FfnArgs& a, cudaStream_t stream, const DeviceInfo& dev);
+
+// Grouped tensor-core FFN (tcgen05): shapes it takes, the path choice for a call, and
+// the launch (group, tile prefix, gate/up, down, combine).
+bool ffn_tensor_shape_ok(int H, int I);
+bool ffn_use_tensor(int T, int k, int E, int H, int I);
+int ffn_tensor_max_tiles(int S, int E);
+int ffn_tensor_b_rows(int S);
+cudaError_t launch_moe_ffn_tensor(const FfnArgs& a, cudaStream_t stream, const DeviceInfo& dev);
 
 // Fused single-token layer step (route + gate/up + down in one cooperative launch).
 struct LayerLaunch {

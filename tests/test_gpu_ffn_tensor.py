@@ -1,0 +1,149 @@
+"""GPU parity of the grouped tensor-core FFN path (tcgen05 MMAs on trits decoded to
+bf16) against the CPU oracle, element by element: |y_gpu - y| <= 2e-3 * max|y| + 1e-5
+("Maple-Preview ...", section "The shipped code does no quantization").  This path
+rounds h to bf16 before the down projection; the bound above covers it.
+
+MAPLE_FFN_PATH=tensor forces the path on shapes where the call would otherwise take
+the CUDA-core kernels, so both paths run on the same inputs."""
+import contextlib
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from support import assert_ffn_close, oracle_pack_layer, run_ffn, upload_experts
+from ternary_weight_moe_02_b300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@contextlib.contextmanager
+def ffn_path(name):
+    old = os.environ.get("MAPLE_FFN_PATH")
+    os.environ["MAPLE_FFN_PATH"] = name
+    try:
+        yield
+    finally:
+        if old is None:
+            del os.environ["MAPLE_FFN_PATH"]
+        else:
+            os.environ["MAPLE_FFN_PATH"] = old
+
+
+def _layer(E, H, I, seed, std=0.02):
+    w = synth.expert_weights(E, H, I, seed=seed, std=std, device="cuda")
+    packed = oracle_pack_layer(w)
+    return packed, upload_experts(packed)
+
+
+def _oracle(packed, x, idx, w32, clamp=7.0):
+    return oracle.moe_ffn(packed["gate"], packed["up"], packed["down"], packed["s_gate"],
+                          packed["s_up"], packed["s_down"], synth.bf16_bits(x), idx,
+                          w32.astype(np.float64), clamp=clamp)
+
+
+def _run(ex, x, idx, w32):
+    y = run_ffn(ex, x.cuda(), torch.from_numpy(idx).cuda(), torch.from_numpy(w32).cuda())
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def _random_routing(T, E, k, seed):
+    rng = np.random.default_rng(seed)
+    idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    w32 = rng.dirichlet(np.ones(k), size=T).astype(np.float32)
+    return idx, w32
+
+
+@pytest.mark.parametrize("E,H,I,T,k", [(8, 256, 128, 40, 4), (4, 384, 192, 33, 3),
+                                       (6, 128, 128, 17, 6), (16, 2048, 512, 24, 8)])
+def test_tensor_path_shapes(E, H, I, T, k):
+    """Ragged token tiles (n_e not a multiple of 16), K tails (H = 384: 77 packed bytes
+    per row, the fifth K tile half padding; I = 192: 39 bytes), the smallest shape the
+    path takes (H = I = 128) and the Maple expert shape."""
+    packed, ex = _layer(E, H, I, seed=E + H + T)
+    x = synth.tokens(T, H, seed=T)
+    idx, w32 = _random_routing(T, E, k, seed=T)
+    with ffn_path("tensor"):
+        y = _run(ex, x, idx, w32)
+    assert_ffn_close(y, _oracle(packed, x, idx, w32), f"tensor E={E} H={H} I={I}")
+
+
+def test_tensor_path_several_token_tiles_per_expert():
+    """Four experts, 300 tokens, top-2: about 150 tokens per expert, so each expert
+    spans two 128-token tiles; expert 0 gets exactly 128 + 1 tokens."""
+    E, H, I, T, k = 4, 256, 128, 300, 2
+    packed, ex = _layer(E, H, I, seed=11)
+    x = synth.tokens(T, H, seed=11)
+    idx, w32 = _random_routing(T, E, k, seed=11)
+    idx[:129, 0] = 0
+    idx[:129, 1] = 1 + (np.arange(129) % 3)
+    idx[129:, 0] = 1 + (np.arange(T - 129) % 3)
+    idx[129:, 1] = 1 + ((np.arange(T - 129) + 1) % 3)
+    assert np.bincount(idx.reshape(-1), minlength=E)[0] == 129
+    with ffn_path("tensor"):
+        y = _run(ex, x, idx, w32)
+    assert_ffn_close(y, _oracle(packed, x, idx, w32), "two token tiles")
+
+
+def test_tensor_path_is_the_automatic_choice_for_dense_loads():
+    """Without the override, 96 tokens on 16 experts (48 slots per expert) take the
+    tensor path; the result matches the oracle and repeats bit for bit."""
+    E, H, I, T, k = 16, 2048, 512, 96, 8
+    packed, ex = _layer(E, H, I, seed=3)
+    x = synth.tokens(T, H, seed=3)
+    idx, w32 = _random_routing(T, E, k, seed=3)
+    assert "MAPLE_FFN_PATH" not in os.environ
+    y1 = _run(ex, x, idx, w32)
+    y2 = _run(ex, x, idx, w32)
+    assert np.array_equal(y1, y2)
+    assert_ffn_close(y1, _oracle(packed, x, idx, w32), "automatic tensor path")
+
+
+def test_tensor_and_core_paths_agree():
+    E, H, I, T, k = 8, 2048, 512, 20, 8
+    packed, ex = _layer(E, H, I, seed=21)
+    x = synth.tokens(T, H, seed=21)
+    idx, w32 = _random_routing(T, E, k, seed=21)
+    with ffn_path("tensor"):
+        y_t = _run(ex, x, idx, w32)
+    with ffn_path("cores"):
+        y_c = _run(ex, x, idx, w32)
+    y_ref = _oracle(packed, x, idx, w32)
+    assert_ffn_close(y_t, y_ref, "tensor")
+    assert_ffn_close(y_c, y_ref, "cores")
+    assert np.abs(y_t - y_c).max() <= 4e-3 * np.abs(y_ref).max()
+
+
+def test_tensor_path_invalid_ids_and_clamp():
+    """Out-of-range ids add nothing; x scaled by 50 makes both clamps bind."""
+    E, H, I, T, k = 6, 256, 128, 5, 4
+    packed, ex = _layer(E, H, I, seed=8, std=0.2)
+    x = (synth.tokens(T, H, seed=8).float() * 50).to(torch.bfloat16)
+    idx = np.array([[0, 0, 5, 2], [-1, 3, E, 1], [4, 4, 4, 4], [1, 2, 3, 5], [5, -7, 0, 2]], np.int32)
+    w32 = np.full((T, k), 0.25, np.float32)
+    with ffn_path("tensor"):
+        y = _run(ex, x, idx, w32)
+    valid = (idx >= 0) & (idx < E)
+    y_ref = _oracle(packed, x, np.where(valid, idx, 0).astype(np.int32), np.where(valid, w32, 0))
+    assert_ffn_close(y, y_ref, "tensor invalid ids, clamped")
+
+
+def test_tensor_path_all_zero_weights_give_zero():
+    E, H, I, T, k = 2, 256, 128, 3, 2
+    Bh, Bi = (H + 4) // 5, (I + 4) // 5
+    packed = {"gate": np.full((E, I, Bh), 121, np.uint8), "up": np.full((E, I, Bh), 121, np.uint8),
+              "down": np.full((E, H, Bi), 121, np.uint8), "s_gate": np.ones((E, I), np.float32),
+              "s_up": np.ones((E, I), np.float32), "s_down": np.ones((E, H), np.float32)}
+    ex = upload_experts(packed)
+    with ffn_path("tensor"):
+        y = _run(ex, synth.tokens(T, H, seed=1), np.array([[0, 1]] * T, np.int32),
+                 np.full((T, k), 0.5, np.float32))
+    assert np.all(y == 0)
+
+
+def test_device_status_is_clean_after_the_tensor_cases():
+    from ternary_weight_moe_02_b300 import maple
+    maple.maple_check_device_status()

@@ -281,3 +281,50 @@ def test_integer_pack_unit_matches_the_oracle_packing():
         assert got == (int(want[0]), int(want[1])), (w, thr, q)
         checked += 1
     assert checked > 2500
+
+
+TC_ROWS, TC_TOK, TC_KTILE, TC_STAGES, TC_LUTS = 128, 128, 80, 4, 2 * 256 * 16
+TC_STAGE_A = TC_KTILE // 8 * TC_ROWS * 16
+TC_STAGE_B = TC_KTILE // 8 * TC_TOK * 16
+
+
+def tc_shape_ok(H, I):
+    return (H % TC_ROWS == 0 and I % (TC_ROWS // 2) == 0 and H >= 128 and I >= 128
+            and H <= 2080 and I <= 2080)
+
+
+def tc_smem(row_bytes):
+    stage_off = -(-(TC_LUTS + TC_ROWS * row_bytes) // 128) * 128
+    return stage_off, stage_off + TC_STAGES * (TC_STAGE_A + TC_STAGE_B)
+
+
+def test_tensor_path_plan_fits_and_is_aligned():
+    """The grouped tcgen05 kernels (csrc/ffn_tensor.cu): shared memory within the
+    opt-in limit for every accepted shape, the packed-row bulk copies 16-byte aligned,
+    and every MMA operand read (5 MMAs of K = 16 per stage, 16 row groups at 128 B,
+    2 core-matrix columns at rows * 16 B) and cp.async write inside its stage."""
+    shapes = [(H, I) for H in range(128, 2081, 128) for I in range(128, 2081, 64)]
+    for H, I in shapes:
+        assert tc_shape_ok(H, I)
+        # B operand maps: (8, max(S, 128), cols / 8) with a (8, 128, 10) box; strides
+        # cols * 2 and 16 bytes are multiples of 16, the box's first coordinate is 0
+        for cols in (H, I):
+            assert cols // 8 >= TC_KTILE // 8 and (cols * 2) % 16 == 0
+        for rb, rows_per_cta, mstep, mtot in ((nbytes(H), TC_ROWS // 2, TC_ROWS // 2, I),
+                                              (nbytes(I), TC_ROWS, TC_ROWS, H)):
+            _, total = tc_smem(rb)
+            assert total + 1280 <= 232448, (H, I, total)
+            size = rows_per_cta * rb
+            for e in (0, 1, 7):
+                for m0 in range(0, mtot, mstep):
+                    _check((e * mtot + m0) * rb, size, (e + 1) * mtot * rb, f"tc H={H} I={I}")
+    for q in range(TC_KTILE // 16):
+        start = q * 2 * TC_ROWS * 16
+        last = start + TC_ROWS * 16 + (TC_ROWS // 8 - 1) * 128 + 127
+        assert last < TC_STAGE_A and q * 2 * TC_TOK * 16 + TC_TOK * 16 + (TC_TOK // 8 - 1) * 128 + 127 < TC_STAGE_B
+    assert (TC_KTILE // 8 - 1) * TC_TOK * 16 + (TC_TOK - 1) * 16 + 16 <= TC_STAGE_B
+    # epilogue buffers reuse the stages
+    assert TC_TOK * 64 * 4 + TC_TOK * 64 * 2 <= TC_STAGES * (TC_STAGE_A + TC_STAGE_B)
+    assert TC_TOK * TC_ROWS * 4 <= TC_STAGES * (TC_STAGE_A + TC_STAGE_B)
+    assert not tc_shape_ok(2080, 512) and not tc_shape_ok(2048, 520) and not tc_shape_ok(40, 24)
+    assert not tc_shape_ok(128, 64)
