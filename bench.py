@@ -32,7 +32,11 @@ sys.path.insert(0, ROOT)
 H, E, I, K_TOP = 2048, 256, 512, 8
 N_TOKENS = 1000
 LAYERS = 64
-METRIC = "ternary MoE layer tokens/s (batch-1 decode)"
+METRIC = "ternary MoE layer tokens/s (batch 1 & 64 decode); packed-weight HBM GB/s vs peak"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+LAYER_KERNEL_SOURCES = ("ternary_weight_moe_02_b300/csrc/layer_decode.cu",
+                        "ternary_weight_moe_02_b300/csrc/common.cuh",
+                        "ternary_weight_moe_02_b300/csrc/kernels.h")
 EXPERT_BYTES = 2 * I * ((H + 4) // 5) + H * ((I + 4) // 5) + 4 * (2 * I + H)  # 643,072
 
 
@@ -130,6 +134,28 @@ def _max_over_ranks(v: float, world: int) -> float:
 
 
 # ----------------------------------------------------------------------------- inputs
+
+def sources_sha256(paths) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str, sources) -> float | None:
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu summary,
+    or None when there is none or the kernel's sources changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)[kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    if rec.get("source_sha256") != sources_sha256(sources):
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
 
 def build_layers(maple, synth, n_layers: int, seed0: int = 1000):
     """n_layers independent Maple layers: bf16 N(0,0.02) experts drawn on the GPU and
@@ -316,7 +342,7 @@ def run_gpu(args, world, rank, local):
                      "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                      "alg_bytes_per_launch": alg_bytes, "avg_launch_us": ffn_ms * 1e3,
                      "packed_weight_gbs": packed_bytes / (ffn_ms / 1e3) / 1e9,
-                     "traffic": None},
+                     "traffic": measured_traffic("moe_layer_b1_kernel", LAYER_KERNEL_SOURCES)},
         "two_call_path": {"value": two_call_value, "unit": "tokens/s",
                           "calls": "maple_route_topk + maple_moe_ffn (4 launches per step)"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "steps": n_e2e,
