@@ -1,29 +1,32 @@
-// Expert FFN on the tcgen05 tensor cores (grouped path for many tokens per expert).
+// Expert FFN on the tcgen05 tensor cores (grouped path: tokens batched per expert).
 //
 // "Maple-Preview: a 20B reasoning model where 97% of the weights are -1, 0, or +1",
 // sections "The claim, verified from the bytes" (one scale per output row, trits
 // -1/0/+1) and "The shipped code does no quantization" (the expert body
 // down(act(clamp(gate x, max=7)) * clamp(up x, -7, 7))).  The pages give no kernel for
-// many tokens per expert; with hundreds of tokens on an expert the contraction is dense
-// enough for the tensor cores, and a trit is exact in bf16.
+// many tokens per expert; a trit is exact in bf16, so the sums can run on the tensor
+// cores with fp32 accumulation.
 //
-// Per expert e with n_e routed tokens (slots grouped by expert, tiles of kTok tokens):
-//   gate/up CTA: D[128 x kTok] = A . X^T, A = 64 gate rows and the same 64 up rows of
-//     e decoded from the packed bytes to bf16 (+-0.5, 0: half the trit, exact, undone
-//     by the factor 2 in the epilogue) in shared memory, X = the
-//     tokens' bf16 activations (gathered once per call into expert order, then loaded
-//     by TMA); fp32 accumulation in tensor memory.  Epilogue: h = silu(min(s_g g, clamp)) * clamp(s_u u, -clamp, clamp),
-//     rounded to bf16, stored per slot in expert order.
-//   down CTA: D[128 x kTok] = A_down . H^T over I, epilogue w_slot * s_d * D stored
-//     per slot (fp32); a combine kernel adds each token's k slots in order 0..k-1.
+// Per expert e with n_e routed tokens (slots grouped by expert, tiles of NT tokens;
+// NT = 128 for prefill-sized calls, 16 for decode batches):
+//   gate/up CTA: D[128 x NT] = A . X^T, A = 64 gate rows and the same 64 up rows of e,
+//     X = the tokens' bf16 activations (gathered once per call into expert order,
+//     loaded by TMA); fp32 accumulation in tensor memory.  Epilogue:
+//     h = silu(min(s_g g, clamp)) * clamp(s_u u, -clamp, clamp), rounded to bf16, stored
+//     per slot in expert order.
+//   down CTA: D[128 x NT] = A_down . H^T over I; epilogue w_slot * s_d * D stored per
+//     slot (fp32); a combine kernel adds each token's k slots in order 0..k-1.
 //
-// Operands are K-major without swizzle: a K tile of 80 values (16 packed bytes per row)
-// is 10 core-matrix columns of 8 bf16; element (row, k) of a stage sits at
-// (k / 8) * (rows * 16) + row * 16 + (k % 8) * 2, which is what a 3-D TMA box
-// (8 values, rows, K chunks) of a row-major [rows][K] matrix writes.  Eight producer
-// warps fill a ring of four stages (A rows decoded, the B tile by one TMA) and one
-// thread issues five tcgen05.mma (K = 16 each) per stage, committing them to the
-// stage's "empty" mbarrier.  All waits are bounded.
+// A is decoded from the packed bytes straight into tensor memory: thread r of lane
+// quarter r / 32 owns weight row r (TMEM lane r) and writes its K values as bf16 +-0.5
+// or 0 (half the trit, exact; the epilogues scale by 2 s), two per 32-bit column, with
+// tcgen05.st; the MMA reads A from tensor memory.  B (tokens) sits in shared memory
+// K-major without swizzle: element (n, k) of a stage at (k / 8) * (NT * 16) + n * 16 +
+// (k % 8) * 2, which is what a 3-D TMA box (8 values, NT rows, 10 chunks) of a
+// row-major [rows][K] matrix writes.  K tiles hold 80 values (16 packed bytes per row).
+// Eight producer warps fill a ring of four stages; one thread issues five tcgen05.mma
+// (K = 16 each) per stage and commits them to the stage's "empty" mbarrier, which the
+// producers wait for before refilling the stage.  All waits are bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -39,19 +42,26 @@ namespace maple {
 namespace {
 
 constexpr int kRows = 128;                 // MMA M: weight rows per CTA
-constexpr int kTok = 128;                  // MMA N: tokens per CTA
 constexpr int kKTile = 80;                 // K values per stage (16 packed bytes)
-constexpr int kChunks = kKTile / 8;        // 16-byte core-matrix columns per stage
-constexpr int kStages = 4;
-constexpr int kStageA = kChunks * kRows * 16;  // 20,480 B
-constexpr int kStageB = kChunks * kTok * 16;   // 20,480 B
-constexpr int kLutReps = 4;                    // copies of the decode table, by lane & 3
+constexpr int kChunks = kKTile / 8;        // 16-byte core-matrix columns per B stage
+constexpr int kMaxStages = 8;
+constexpr int kAStride = 48;               // TMEM column stride between A stages (40 used)
+constexpr int kLutReps = 4;                // copies of the decode table, by lane & 3
 constexpr int kLutBytes = 256 * kLutReps * 8;  // 8 KB
-constexpr int kProducerWarps = 8;          // decode A and copy B; warp 8 issues the MMAs
+constexpr int kProducerWarps = 8;          // decode A, load B; warp 8 issues the MMAs
 constexpr int kThreads = (kProducerWarps + 1) * 32;
-// instruction descriptor: D fp32, A and B bf16, both K-major, N = kTok, M = kRows
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTok >> 3) << 17) |
-                            ((uint32_t)(kRows >> 4) << 24);
+
+template <int NT>
+struct TileCfg {
+    static constexpr int kStages = 4;                                    // ring depth
+    static constexpr int kStageB = kChunks * NT * 16;                    // bytes of a B stage
+    static constexpr int kABase = NT < 32 ? 32 : NT;                     // first A column
+    static constexpr int kUsedCols = kABase + kStages * kAStride;
+    static constexpr int kTmemCols = kUsedCols <= 256 ? 256 : 512;       // power of two
+    // instruction descriptor: D fp32, A and B bf16, both K-major, N = NT, M = 128
+    static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NT >> 3) << 17) |
+                                       ((uint32_t)(kRows >> 4) << 24);
+};
 
 // ----------------------------------------------------------------- tcgen05 helpers
 
@@ -76,11 +86,13 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] . B[smem descriptor]
+__device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
     asm volatile(
         "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -90,29 +102,38 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
+// 16 and 4 consecutive 32-bit columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* w) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "r"(w[8]),
+        "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
         : "memory");
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t* w) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3])
+                 : "memory");
+}
+
+// 8 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// B tile: a (8, kTok, kChunks) box at rows row0.., K chunks chunk0.. of a 3-D tensor
+// B tile: an (8, NT, kChunks) box at rows row0.., K chunks chunk0.. of a 3-D tensor
 // map; the copy's bytes complete on `bar`
 __device__ __forceinline__ void tma_load_b(void* dst, const CUtensorMap* map, int row0, int chunk0,
                                            uint64_t* bar) {
@@ -123,14 +144,12 @@ __device__ __forceinline__ void tma_load_b(void* dst, const CUtensorMap* map, in
         : "memory");
 }
 
-// ----------------------------------------------------------------- decode tables
+// ----------------------------------------------------------------- decode table
 
-// Decode table: for each code, the high bytes of the five bf16 values +-0.5 / 0 of its
-// trits (0xBF for -1, 0x00 for 0, 0x3F for +1; the low byte of those bf16 values is
-// zero), bytes 5-7 zero; the invalid codes 243..255 give five zeros.  kLutReps copies
-// interleaved by entry ([code][copy]) so that the 8-byte loads of a half-warp spread
-// over more banks.  The MMAs then accumulate half the true sums; the epilogues scale
-// by 2 s.
+// For each code, the high bytes of the five bf16 values +-0.5 / 0 of its trits (0xBF
+// for -1, 0x00 for 0, 0x3F for +1; the low byte of those bf16 values is zero), bytes
+// 5-7 zero; the invalid codes 243..255 give five zeros.  kLutReps copies interleaved by
+// entry ([code][copy]) so that the 8-byte loads of a half-warp spread over more banks.
 __device__ __forceinline__ void build_half_lut(uint2* lut, int tid, int nthreads) {
     for (int i = tid; i < 256 * kLutReps; i += nthreads) {
         const int c = i / kLutReps;
@@ -149,12 +168,10 @@ __device__ __forceinline__ void build_half_lut(uint2* lut, int tid, int nthreads
 }
 
 // Decodes packed bytes [16 kt + 8 h, +8) of one row (bytes at or past rb read as the
-// all-zero code 121) into core-matrix columns 5h..5h+4 of the row in a stage.  Two
-// bytes (ten values) become five words of two bf16 each by byte permutes of their two
-// table entries.
+// all-zero code 121) into 20 words of two bf16 each (K order).  Two bytes (ten values)
+// become five words by byte permutes of their two table entries.
 __device__ __forceinline__ void decode_half_tile(const uint8_t* row, int rb, int kt, int h, const uint2* lut,
-                                                 int rep, unsigned char* stage_a, int r) {
-    uint32_t words[20];
+                                                 int rep, uint32_t* words) {
     const int b0 = 16 * kt + 8 * h;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
@@ -169,10 +186,6 @@ __device__ __forceinline__ void decode_half_tile(const uint8_t* row, int rb, int
         words[5 * p + 3] = __byte_perm(eb.x, eb.y, 0x2515);  // 0, b1, 0, b2
         words[5 * p + 4] = __byte_perm(eb.x, eb.y, 0x4535);  // 0, b3, 0, b4
     }
-#pragma unroll
-    for (int c = 0; c < 5; ++c)
-        *reinterpret_cast<uint4*>(stage_a + (5 * h + c) * (kRows * 16) + r * 16) =
-            make_uint4(words[4 * c], words[4 * c + 1], words[4 * c + 2], words[4 * c + 3]);
 }
 
 struct TcArgs {
@@ -190,7 +203,7 @@ struct TcArgs {
     const int32_t* counts;
     const int32_t* offsets;
     const int32_t* perm;
-    const int32_t* tile_off;  // [E + 1] prefix of ceil(counts / kTok)
+    const int32_t* tile_off;  // [E + 1] prefix of ceil(counts / NT)
     uint16_t* xs;             // [T k][H] bf16, the slots' tokens in expert order
     uint16_t* hs;             // [T k][I] bf16, slots in expert order
     float* ys;                // [T k][H] fp32, per original slot
@@ -199,17 +212,19 @@ struct TcArgs {
     int* status;
 };
 
-// Shared-memory plan of a grouped CTA: two decode tables, the CTA's packed rows, the
-// stages.  The epilogue reuses the stage area.
+// Shared-memory plan of a grouped CTA: the decode table, the CTA's packed rows, the B
+// stages.  The epilogue reuses the packed rows and the stages.
 __host__ __device__ constexpr size_t tc_packed_offset() { return (size_t)kLutBytes; }
 __host__ __device__ constexpr size_t tc_stage_offset(int row_bytes) {
     return (tc_packed_offset() + (size_t)kRows * row_bytes + 127) / 128 * 128;
 }
+template <int NT>
 __host__ __device__ constexpr size_t tc_smem_bytes(int row_bytes) {
-    return tc_stage_offset(row_bytes) + (size_t)kStages * (kStageA + kStageB);
+    return tc_stage_offset(row_bytes) + (size_t)TileCfg<NT>::kStages * TileCfg<NT>::kStageB;
 }
 
 // Finds the expert and token range of grid row `tile`; false when past the last tile.
+template <int NT>
 __device__ __forceinline__ bool tc_tile(const TcArgs& a, int tile, int& e, int& n0, int& nv, int& pos0) {
     if (tile >= a.tile_off[a.E]) return false;
     int lo = 0, hi = a.E - 1;  // largest e with tile_off[e] <= tile
@@ -221,99 +236,105 @@ __device__ __forceinline__ bool tc_tile(const TcArgs& a, int tile, int& e, int& 
             hi = mid - 1;
     }
     e = lo;
-    n0 = (tile - a.tile_off[e]) * kTok;
+    n0 = (tile - a.tile_off[e]) * NT;
     const int left = a.counts[e] - n0;
-    nv = left < kTok ? left : kTok;
+    nv = left < NT ? left : NT;
     pos0 = a.offsets[e] + n0;
     return nv > 0;
 }
 
-// Barriers of a grouped CTA: full[s] (one arrival per producer thread for its decoded
-// A rows), bfull[s] (the B tile's TMA bytes), empty[s] (MMA commit), done (commit
-// after the last MMA), packed (bulk copy of the CTA's packed rows).
+// Barriers of a grouped CTA: full[s] (one arrival per producer thread once its A words
+// are in tensor memory), bfull[s] (the B tile's TMA bytes), empty[s] (MMA commit),
+// done (commit after the last MMA), packed (bulk copy of the CTA's packed rows).
 struct TcBars {
-    uint64_t full[kStages];
-    uint64_t bfull[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[kMaxStages];
+    uint64_t bfull[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t done;
     uint64_t packed;
 };
 
-// Warp-specialised main loop.  Warps 0-7 produce: each thread decodes half of one row
-// of each A tile and arrives on full[s]; thread 0 also loads the stage's B
-// tile (rows row0.., chunks of this K tile) by TMA onto bfull[s].  Warp 8 lane 0 waits
-// for both, issues the stage's five MMAs and commits empty[s]; its last commit goes to
-// done.  Returns false if a bounded wait gave up.
+// Warp-specialised main loop.  Warp w < 8 produces: its thread owns row 32 (w & 3) +
+// lane (the warp's TMEM lane quarter) and decodes half w >> 2 of that row's 16 bytes of
+// each K tile into A stage s (tensor memory), then arrives on full[s]; thread 0 also
+// loads the stage's B tile (rows row0.., this K tile's chunks) by TMA onto bfull[s].
+// Warp 8 lane 0 waits for both, issues the stage's five MMAs and commits empty[s]; its
+// last commit goes to done.  Returns false if a bounded wait gave up.
+template <int NT>
 __device__ bool tc_mainloop(unsigned char* smem, const uint8_t* packed, int rb, int Kdim, const CUtensorMap* bmap,
                             int row0, uint32_t tmem, TcBars& bars, int* status) {
-    const int tid = threadIdx.x, warp = tid >> 5;
+    using Cfg = TileCfg<NT>;
+    constexpr int S = Cfg::kStages;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint2* lut = reinterpret_cast<const uint2*>(smem);
     unsigned char* stages = smem + tc_stage_offset(rb);
     const int KT = (Kdim + kKTile - 1) / kKTile;
     bool ok = true;
     int issued = 0;  // B tiles thread 0 has loaded
     if (warp < kProducerWarps) {
-        // warp w decodes half w & 1 of rows 32 (w >> 1) .. +31: its 16-byte stores of one
-        // core-matrix column are 512 contiguous bytes
-        const int h = warp & 1, r = ((warp >> 1) << 5) | (tid & 31);
+        const int q = warp & 3, h = warp >> 2, r = 32 * q + lane;
         const uint8_t* my_row = packed + r * rb;
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         for (int j = 0; j < KT && ok; ++j) {
-            const int s = j % kStages;
-            if (j >= kStages && !mbar_wait_bounded(&bars.empty[s], (uint32_t)(((j - kStages) / kStages) & 1), status)) {
+            const int s = j % S;
+            if (j >= S && !mbar_wait_bounded(&bars.empty[s], (uint32_t)(((j - S) / S) & 1), status)) {
                 ok = false;
                 break;
             }
-            unsigned char* sa = stages + s * (kStageA + kStageB);
             if (tid == 0) {
-                mbar_arrive_expect_tx(&bars.bfull[s], (uint32_t)kStageB);
-                tma_load_b(sa + kStageA, bmap, row0, j * kChunks, &bars.bfull[s]);
+                mbar_arrive_expect_tx(&bars.bfull[s], (uint32_t)Cfg::kStageB);
+                tma_load_b(stages + s * Cfg::kStageB, bmap, row0, j * kChunks, &bars.bfull[s]);
                 issued = j + 1;
             }
-            decode_half_tile(my_row, rb, j, h, lut, tid & (kLutReps - 1), sa, r);
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            uint32_t words[20];
+            decode_half_tile(my_row, rb, j, h, lut, lane & (kLutReps - 1), words);
+            const uint32_t col = (uint32_t)(Cfg::kABase + s * kAStride + 20 * h);
+            tmem_st16(lane_base + col, words);
+            tmem_st4(lane_base + col + 16, words + 16);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
             mbar_arrive(&bars.full[s]);
         }
     } else if (tid == kProducerWarps * 32) {
         for (int j = 0; j < KT; ++j) {
-            const int s = j % kStages;
-            const uint32_t par = (uint32_t)((j / kStages) & 1);
+            const int s = j % S;
+            const uint32_t par = (uint32_t)((j / S) & 1);
             if (!mbar_wait_bounded(&bars.full[s], par, status) || !mbar_wait_bounded(&bars.bfull[s], par, status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            unsigned char* sa = stages + s * (kStageA + kStageB);
-            const uint32_t a0 = smem_addr(sa), b0 = smem_addr(sa + kStageA);
+            const uint32_t a0 = tmem + (uint32_t)(Cfg::kABase + s * kAStride);
+            const uint32_t b0 = smem_addr(stages + s * Cfg::kStageB);
 #pragma unroll
-            for (int q = 0; q < kKTile / 16; ++q) {
-                const uint64_t ad = smem_desc(a0 + q * 2 * (kRows * 16), kRows * 16, 128);
-                const uint64_t bd = smem_desc(b0 + q * 2 * (kTok * 16), kTok * 16, 128);
-                mma_bf16(tmem, ad, bd, (j | q) != 0 ? 1u : 0u);
+            for (int qk = 0; qk < kKTile / 16; ++qk) {
+                const uint64_t bd = smem_desc(b0 + qk * 2 * (NT * 16), NT * 16, 128);
+                mma_tmem_a(tmem, a0 + 8 * qk, bd, Cfg::kIdesc, (j | qk) != 0 ? 1u : 0u);
             }
             mma_commit(j == KT - 1 ? &bars.done : &bars.empty[s]);
         }
     }
     __syncwarp();
-    // every thread waits for the last MMA (the epilogue reads TMEM and reuses the stages)
+    // every thread waits for the last MMA (the epilogue reads TMEM and reuses shared memory)
     if (ok && !mbar_wait_bounded(&bars.done, 0, status)) ok = false;
     if (!ok && tid == 0) {
         // the last B load of each stage may still be in flight: let it land first
-        for (int t = issued - kStages > 0 ? issued - kStages : 0; t < issued; ++t)
-            mbar_wait_bounded(&bars.bfull[t % kStages], (uint32_t)((t / kStages) & 1), nullptr);
+        for (int t = issued - S > 0 ? issued - S : 0; t < issued; ++t)
+            mbar_wait_bounded(&bars.bfull[t % S], (uint32_t)((t / S) & 1), nullptr);
     }
     tc_fence_after();
     return !__syncthreads_or(!ok);
 }
 
-// CTA prologue shared by both stages: decode tables, barriers, TMEM (warp 8), and the
+// CTA prologue shared by both stages: decode table, barriers, TMEM (warp 8), and the
 // bulk copy of the CTA's packed rows (nrows_copy rows of rb bytes from src0 and, when
 // src1 is set, as many from src1).
-__device__ bool tc_prologue(unsigned char* smem, TcBars& bars, uint32_t* tmem_slot, const uint8_t* src0,
-                            const uint8_t* src1, int nrows_copy, int rb, int* status) {
+__device__ bool tc_prologue(unsigned char* smem, TcBars& bars, uint32_t* tmem_slot, uint32_t tmem_cols,
+                            const uint8_t* src0, const uint8_t* src1, int nrows_copy, int rb, int* status) {
     const int tid = threadIdx.x;
     build_half_lut(reinterpret_cast<uint2*>(smem), tid, blockDim.x);
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kMaxStages; ++i) {
             mbar_init(&bars.full[i], kProducerWarps * 32);
             mbar_init(&bars.bfull[i], 1);
             mbar_init(&bars.empty[i], 1);
@@ -325,7 +346,7 @@ __device__ bool tc_prologue(unsigned char* smem, TcBars& bars, uint32_t* tmem_sl
         bulk_copy_g2s(smem + tc_packed_offset(), src0, bytes, &bars.packed);
         if (src1) bulk_copy_g2s(smem + tc_packed_offset() + bytes, src1, bytes, &bars.packed);
     }
-    if ((tid >> 5) == kProducerWarps) tmem_alloc(tmem_slot, kTok);
+    if ((tid >> 5) == kProducerWarps) tmem_alloc(tmem_slot, tmem_cols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -333,61 +354,60 @@ __device__ bool tc_prologue(unsigned char* smem, TcBars& bars, uint32_t* tmem_sl
     return !__syncthreads_or(!ok);
 }
 
-__device__ __forceinline__ void tc_release(uint32_t tmem) {
+__device__ __forceinline__ void tc_release(uint32_t tmem, uint32_t tmem_cols) {
     tc_fence_before();
     __syncthreads();
-    if ((threadIdx.x >> 5) == kProducerWarps) tmem_dealloc(tmem, kTok);
+    if ((threadIdx.x >> 5) == kProducerWarps) tmem_dealloc(tmem, tmem_cols);
 }
 
 // gate/up: grid (I / 64, max tiles); rows 0..63 of the CTA are gate rows m0..m0+63 of
 // the expert, rows 64..127 the same up rows.
+template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) tc_gateup_kernel(TcArgs a, const __grid_constant__ CUtensorMap xmap) {
+    using Cfg = TileCfg<NT>;
+    constexpr int CW = NT / 2;  // columns per epilogue warp (two warps per lane quarter)
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ TcBars bars;
     __shared__ uint32_t tmem_slot;
     pdl_wait();
     pdl_launch_dependents();
     int e, n0, nv, pos0;
-    if (!tc_tile(a, blockIdx.y, e, n0, nv, pos0)) return;
-    const int tid = threadIdx.x;
+    if (!tc_tile<NT>(a, blockIdx.y, e, n0, nv, pos0)) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, I = a.I, Bh = (H + 4) / 5;
     const int m0 = blockIdx.x * (kRows / 2);
     const uint8_t* gsrc = a.gate + ((int64_t)e * I + m0) * Bh;
     const uint8_t* usrc = a.up + ((int64_t)e * I + m0) * Bh;
-    bool ok = tc_prologue(smem, bars, &tmem_slot, gsrc, usrc, kRows / 2, Bh, a.status);
+    bool ok = tc_prologue(smem, bars, &tmem_slot, Cfg::kTmemCols, gsrc, usrc, kRows / 2, Bh, a.status);
     const uint32_t tmem = tmem_slot;
-    if (ok) ok = tc_mainloop(smem, smem + tc_packed_offset(), Bh, H, &xmap, pos0, tmem, bars, a.status);
+    if (ok) ok = tc_mainloop<NT>(smem, smem + tc_packed_offset(), Bh, H, &xmap, pos0, tmem, bars, a.status);
     if (ok) {
-        // epilogue: warps 2-3 hold the up rows, warps 0-1 the gate rows (TMEM lane = row)
-        unsigned char* epi = smem + tc_stage_offset(Bh);
-        float* U = reinterpret_cast<float*>(epi);                        // [kTok][64]
-        uint16_t* Hs = reinterpret_cast<uint16_t*>(epi + kTok * 64 * 4);  // [kTok][64]
-        const int warp = tid >> 5;
-        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-        if (tid >= 64 && tid < 128) {
-            const float su = 2.f * a.s_up[(int64_t)e * I + m0 + tid - 64];
-            for (int c0 = 0; c0 < kTok; c0 += 32) {
-                float v[32];
-                tmem_ld32(lane_addr + c0, v);
+        // epilogue over eight warps: warp w reads rows 32 (w & 3) + lane (gate rows for
+        // w & 3 < 2, up rows otherwise) and columns CW (w >> 2) .. +CW
+        unsigned char* epi = smem + tc_packed_offset();
+        float* U = reinterpret_cast<float*>(epi);                       // [NT][64]
+        uint16_t* Hs = reinterpret_cast<uint16_t*>(epi + NT * 64 * 4);  // [NT][64]
+        float v[CW];
+        if (warp < kProducerWarps) {
+            const int q = warp & 3, c0 = CW * (warp >> 2);
+            const uint32_t addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float u = su * v[i];
-                    U[(c0 + i) * 64 + tid - 64] = fminf(fmaxf(u, -a.clamp), a.clamp);
-                }
+            for (int i = 0; i < CW; i += 8) tmem_ld8(addr + i, v + i);
+            if (q >= 2) {
+                const int r = 32 * (q - 2) + lane;
+                const float su = 2.f * a.s_up[(int64_t)e * I + m0 + r];
+#pragma unroll
+                for (int i = 0; i < CW; ++i) U[(c0 + i) * 64 + r] = fminf(fmaxf(su * v[i], -a.clamp), a.clamp);
             }
         }
         __syncthreads();
-        if (tid < 64) {
-            const float sg = 2.f * a.s_gate[(int64_t)e * I + m0 + tid];
-            for (int c0 = 0; c0 < kTok; c0 += 32) {
-                float v[32];
-                tmem_ld32(lane_addr + c0, v);
+        if (warp < kProducerWarps && (warp & 3) < 2) {
+            const int r = 32 * (warp & 3) + lane, c0 = CW * (warp >> 2);
+            const float sg = 2.f * a.s_gate[(int64_t)e * I + m0 + r];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float g = fminf(sg * v[i], a.clamp);
-                    const float hv = silu_f(g) * U[(c0 + i) * 64 + tid];
-                    Hs[(c0 + i) * 64 + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
-                }
+            for (int i = 0; i < CW; ++i) {
+                const float g = fminf(sg * v[i], a.clamp);
+                Hs[(c0 + i) * 64 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(silu_f(g) * U[(c0 + i) * 64 + r]));
             }
         }
         __syncthreads();
@@ -398,47 +418,46 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gateup_kernel(TcArgs a, const 
                 *reinterpret_cast<const uint4*>(Hs + nn * 64 + 8 * part);
         }
     }
-    tc_release(tmem);
+    tc_release(tmem, Cfg::kTmemCols);
 }
 
 // down: grid (H / 128, max tiles); the CTA's 128 rows are down rows m0..m0+127.
+template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) tc_down_kernel(TcArgs a, const __grid_constant__ CUtensorMap hmap) {
+    using Cfg = TileCfg<NT>;
+    constexpr int CW = NT / 2;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ TcBars bars;
     __shared__ uint32_t tmem_slot;
-    __shared__ int s_slot[kTok];
-    __shared__ float s_w[kTok];
+    __shared__ int s_slot[NT];
+    __shared__ float s_w[NT];
     pdl_wait();
     pdl_launch_dependents();
     int e, n0, nv, pos0;
-    if (!tc_tile(a, blockIdx.y, e, n0, nv, pos0)) return;
-    const int tid = threadIdx.x;
+    if (!tc_tile<NT>(a, blockIdx.y, e, n0, nv, pos0)) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, I = a.I, Bi = (I + 4) / 5;
     const int m0 = blockIdx.x * kRows;
-    if (tid < nv) {
-        const int slot = a.perm[pos0 + tid];
+    if (tid < NT) {
+        const int slot = tid < nv ? a.perm[pos0 + tid] : 0;
         s_slot[tid] = slot;
-        s_w[tid] = a.w[slot];
+        s_w[tid] = tid < nv ? a.w[slot] : 0.f;
     }
     const uint8_t* dsrc = a.down + ((int64_t)e * H + m0) * Bi;
-    bool ok = tc_prologue(smem, bars, &tmem_slot, dsrc, nullptr, kRows, Bi, a.status);
+    bool ok = tc_prologue(smem, bars, &tmem_slot, Cfg::kTmemCols, dsrc, nullptr, kRows, Bi, a.status);
     const uint32_t tmem = tmem_slot;
-    if (ok) ok = tc_mainloop(smem, smem + tc_packed_offset(), Bi, I, &hmap, pos0, tmem, bars, a.status);
+    if (ok) ok = tc_mainloop<NT>(smem, smem + tc_packed_offset(), Bi, I, &hmap, pos0, tmem, bars, a.status);
     if (ok) {
-        float* Ys = reinterpret_cast<float*>(smem + tc_stage_offset(Bi));  // [kTok][kRows]
-        const int warp = tid >> 5;
-        if (warp < 4) {
-            const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-            const float sd = 2.f * a.s_down[(int64_t)e * H + m0 + tid];
-            for (int c0 = 0; c0 < kTok; c0 += 32) {
-                float v[32];
-                tmem_ld32(lane_addr + c0, v);
+        float* Ys = reinterpret_cast<float*>(smem + tc_packed_offset());  // [NT][kRows]
+        if (warp < kProducerWarps) {
+            const int q = warp & 3, c0 = CW * (warp >> 2), r = 32 * q + lane;
+            const uint32_t addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
+            const float sd = 2.f * a.s_down[(int64_t)e * H + m0 + r];
+            float v[CW];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int nn = c0 + i;
-                    Ys[nn * kRows + tid] = nn < nv ? s_w[nn] * (sd * v[i]) : 0.f;
-                }
-            }
+            for (int i = 0; i < CW; i += 8) tmem_ld8(addr + i, v + i);
+#pragma unroll
+            for (int i = 0; i < CW; ++i) Ys[(c0 + i) * kRows + r] = s_w[c0 + i] * (sd * v[i]);
         }
         __syncthreads();
         for (int i = tid; i < nv * (kRows / 4); i += kThreads) {
@@ -447,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_down_kernel(TcArgs a, const __
                 *reinterpret_cast<const float4*>(Ys + nn * kRows + 4 * part);
         }
     }
-    tc_release(tmem);
+    tc_release(tmem, Cfg::kTmemCols);
 }
 
 // xs[pos] = x[token of slot perm[pos]] for the offsets[E] grouped slots, 16 bytes per
@@ -492,14 +511,14 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(TcArgs a) {
     }
 }
 
-// tile_off[e] = sum over e' < e of ceil(counts[e'] / kTok); one CTA, E <= 1024.
-__global__ void __launch_bounds__(1024) tc_tile_prefix_kernel(const int32_t* __restrict__ counts, int E,
+// tile_off[e] = sum over e' < e of ceil(counts[e'] / nt); one CTA, E <= 1024.
+__global__ void __launch_bounds__(1024) tc_tile_prefix_kernel(const int32_t* __restrict__ counts, int E, int nt,
                                                               int32_t* __restrict__ tile_off) {
     __shared__ int32_t part[32];
     pdl_wait();
     pdl_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int v = tid < E ? (counts[tid] + kTok - 1) / kTok : 0;
+    const int v = tid < E ? (counts[tid] + nt - 1) / nt : 0;
     int incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -523,19 +542,23 @@ __global__ void __launch_bounds__(1024) tc_tile_prefix_kernel(const int32_t* __r
     if (tid == E - 1) tile_off[E] = excl + v;
 }
 
+// Token-tile width of a call: 128 when the slots average at least 64 per expert
+// (prefill), 16 otherwise (decode batches: fewer padded MMA columns and a smaller
+// TMEM allocation, so that two CTAs share an SM).
+int tile_tokens(int S, int E) { return (int64_t)S >= 64 * (int64_t)E ? 128 : 16; }
+
 }  // namespace
 
 // MAPLE_FFN_PATH=tensor or =cores forces a path (for parity tests of both on the same
-// inputs); otherwise the tensor path runs when the slots average at least
-// kTensorMinPerExpert per expert.
-constexpr int kTensorMinPerExpert = 16;
-
+// inputs); otherwise the tensor path runs once there are at least half as many slots
+// as experts (on the Maple layer, 16 tokens and up: measured faster than the CUDA-core
+// kernels from there on, slower below).
 bool ffn_use_tensor(int T, int k, int E, int H, int I) {
     if (!ffn_tensor_shape_ok(H, I) || T < 1) return false;
     const char* env = getenv("MAPLE_FFN_PATH");
     if (env != nullptr && strcmp(env, "tensor") == 0) return true;
     if (env != nullptr && strcmp(env, "cores") == 0) return false;
-    return (int64_t)T * k >= (int64_t)kTensorMinPerExpert * E;
+    return 2 * (int64_t)T * k >= (int64_t)E;
 }
 
 // H a multiple of the 128 down rows of a CTA, I of the 64 gate (and up) rows; both at
@@ -544,7 +567,7 @@ bool ffn_tensor_shape_ok(int H, int I) {
     return H % kRows == 0 && I % (kRows / 2) == 0 && H >= 128 && I >= 128 && H <= 2080 && I <= 2080;
 }
 
-int ffn_tensor_b_rows(int S) { return S > kTok ? S : kTok; }
+int ffn_tensor_b_rows(int S) { return S > 128 ? S : 128; }
 
 namespace {
 
@@ -564,13 +587,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // A row-major bf16 [rows][cols] matrix as a 3-D map (8 values, rows, cols / 8) whose box
-// (8, kTok, kChunks) lands in shared memory as the K-major no-swizzle operand layout.
-cudaError_t make_rows_map(CUtensorMap* map, const uint16_t* base, int rows, int cols) {
+// (8, nt, kChunks) lands in shared memory as the K-major no-swizzle operand layout.
+cudaError_t make_rows_map(CUtensorMap* map, const uint16_t* base, int rows, int cols, int nt) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (encode == nullptr) return cudaErrorNotSupported;
     const cuuint64_t dims[3] = {8, (cuuint64_t)rows, (cuuint64_t)(cols / 8)};
     const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, 16};
-    const cuuint32_t box[3] = {8, kTok, kChunks};
+    const cuuint32_t box[3] = {8, (cuuint32_t)nt, kChunks};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides,
                               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -578,16 +601,37 @@ cudaError_t make_rows_map(CUtensorMap* map, const uint16_t* base, int rows, int 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-}  // namespace
+template <int NT>
+cudaError_t launch_tc_ffn(const TcArgs& a, int S, cudaStream_t stream) {
+    const int tiles = (S + NT - 1) / NT + (a.E < S ? a.E : S);  // >= sum of ceil(n_e / NT)
+    const int Bh = (a.H + 4) / 5, Bi = (a.I + 4) / 5;
+    const size_t smem_gu = tc_smem_bytes<NT>(Bh), smem_dn = tc_smem_bytes<NT>(Bi);
+    auto gu = tc_gateup_kernel<NT>;
+    auto dn = tc_down_kernel<NT>;
+    cudaError_t err = ensure_dynamic_smem(gu, smem_gu);
+    if (err != cudaSuccess) return err;
+    err = ensure_dynamic_smem(dn, smem_dn);
+    if (err != cudaSuccess) return err;
+    const int R = ffn_tensor_b_rows(S);
+    CUtensorMap xmap, hmap;
+    err = make_rows_map(&xmap, a.xs, R, a.H, NT);
+    if (err != cudaSuccess) return err;
+    err = make_rows_map(&hmap, a.hs, R, a.I, NT);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(gu, dim3(a.I / (kRows / 2), tiles), dim3(kThreads), smem_gu, stream, a, xmap);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(dn, dim3(a.H / kRows, tiles), dim3(kThreads), smem_dn, stream, a, hmap);
+}
 
-int ffn_tensor_max_tiles(int S, int E) { return (S + kTok - 1) / kTok + (E < S ? E : S); }
+}  // namespace
 
 cudaError_t launch_moe_ffn_tensor(const FfnArgs& f, cudaStream_t stream, const DeviceInfo& dev) {
     const int S = f.T * f.k;
+    const int nt = tile_tokens(S, f.E);
     cudaError_t err = launch_group_tokens(f.idx, S, f.k, f.E, f.counts, f.offsets, f.perm, f.active,
                                           f.n_active, stream, dev);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(tc_tile_prefix_kernel, dim3(1), dim3(1024), 0, stream, (const int32_t*)f.counts, f.E,
+    err = launch_pdl(tc_tile_prefix_kernel, dim3(1), dim3(1024), 0, stream, (const int32_t*)f.counts, f.E, nt,
                      f.tile_off);
     if (err != cudaSuccess) return err;
     TcArgs a;
@@ -615,19 +659,6 @@ cudaError_t launch_moe_ffn_tensor(const FfnArgs& f, cudaStream_t stream, const D
     a.y = f.y;
     a.T = f.T;
     a.status = f.status;
-    const int tiles = ffn_tensor_max_tiles(S, f.E);
-    const int Bh = (f.H + 4) / 5, Bi = (f.I + 4) / 5;
-    const size_t smem_gu = tc_smem_bytes(Bh), smem_dn = tc_smem_bytes(Bi);
-    err = ensure_dynamic_smem(tc_gateup_kernel, smem_gu);
-    if (err != cudaSuccess) return err;
-    err = ensure_dynamic_smem(tc_down_kernel, smem_dn);
-    if (err != cudaSuccess) return err;
-    const int R = ffn_tensor_b_rows(S);
-    CUtensorMap xmap, hmap;
-    err = make_rows_map(&xmap, f.xs, R, f.H);
-    if (err != cudaSuccess) return err;
-    err = make_rows_map(&hmap, f.hs, R, f.I);
-    if (err != cudaSuccess) return err;
     {
         const int64_t work = (int64_t)S * (f.H / 8);
         const int64_t want = (work + 255) / 256;
@@ -635,9 +666,7 @@ cudaError_t launch_moe_ffn_tensor(const FfnArgs& f, cudaStream_t stream, const D
         err = launch_pdl(tc_gather_kernel, dim3((unsigned)(want < cap ? want : cap)), dim3(256), 0, stream, a);
         if (err != cudaSuccess) return err;
     }
-    err = launch_pdl(tc_gateup_kernel, dim3(f.I / (kRows / 2), tiles), dim3(kThreads), smem_gu, stream, a, xmap);
-    if (err != cudaSuccess) return err;
-    err = launch_pdl(tc_down_kernel, dim3(f.H / kRows, tiles), dim3(kThreads), smem_dn, stream, a, hmap);
+    err = nt == 128 ? launch_tc_ffn<128>(a, S, stream) : launch_tc_ffn<16>(a, S, stream);
     if (err != cudaSuccess) return err;
     const int64_t work = (int64_t)f.T * (f.H / 4);
     const int64_t want = (work + 255) / 256;

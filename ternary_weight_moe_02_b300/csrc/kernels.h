@@ -78,7 +78,6 @@ cudaError_t launch_moe_ffn(const FfnArgs& a, cudaStream_t stream, const DeviceIn
 // the launch (group, tile prefix, gate/up, down, combine).
 bool ffn_tensor_shape_ok(int H, int I);
 bool ffn_use_tensor(int T, int k, int E, int H, int I);
-int ffn_tensor_max_tiles(int S, int E);
 int ffn_tensor_b_rows(int S);
 cudaError_t launch_moe_ffn_tensor(const FfnArgs& a, cudaStream_t stream, const DeviceInfo& dev);
 

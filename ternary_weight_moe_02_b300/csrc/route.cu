@@ -9,6 +9,10 @@
 // column, so each router row is read once per token tile.  bf16 x bf16 products are
 // exact in fp32; each lane accumulates H/32 products with FMA in column order, then a
 // butterfly combines the lanes (depth H/32 + 5 additions).
+// Kernel 1' (logits, T >= 32): the same sums, register-tiled: a warp computes 4 tokens
+// x 8 experts, so each 16-byte chunk of x or Wr it loads serves 8 or 4 outputs.  Every
+// logit is the same FMA chain in the same column order and the same butterfly as in
+// kernel 1, so the two kernels give identical logits.
 // Kernel 2 (select): one warp per token; k rounds of warp arg-max (ties to the lower
 // expert id), then softmax of the k winners in fp32.
 #include <math.h>
@@ -90,6 +94,66 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
     }
 }
 
+constexpr int kTileTok = 4;    // tokens per warp
+constexpr int kTileExp = 8;    // experts per warp
+constexpr int kTileWarpsT = 2; // warps along tokens in a CTA
+constexpr int kTileWarpsE = 4; // warps along experts in a CTA
+
+__global__ void __launch_bounds__(kTileWarpsT * kTileWarpsE * 32)
+    route_logits_tiled_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ Wr,
+                              const float* __restrict__ bias, int T, int H, int E,
+                              float* __restrict__ logits) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = (blockIdx.y * kTileWarpsT + (warp % kTileWarpsT)) * kTileTok;
+    const int e0 = (blockIdx.x * kTileWarpsE + (warp / kTileWarpsT)) * kTileExp;
+    if (t0 >= T || e0 >= E) return;
+    float acc[kTileTok][kTileExp];
+#pragma unroll
+    for (int t = 0; t < kTileTok; ++t)
+#pragma unroll
+        for (int e = 0; e < kTileExp; ++e) acc[t][e] = 0.f;
+    const int n8 = H >> 3;
+    for (int c = lane; c < n8; c += 32) {
+        uint4 wv[kTileExp], xv[kTileTok];
+#pragma unroll
+        for (int e = 0; e < kTileExp; ++e)
+            wv[e] = e0 + e < E ? ldg_nc_v4(reinterpret_cast<const uint4*>(Wr + (int64_t)(e0 + e) * H) + c)
+                               : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int t = 0; t < kTileTok; ++t)
+            xv[t] = t0 + t < T ? ldg_nc_v4(reinterpret_cast<const uint4*>(x + (int64_t)(t0 + t) * H) + c)
+                               : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float wf[kTileExp], xf[kTileTok];
+#pragma unroll
+            for (int e = 0; e < kTileExp; ++e) {
+                const uint32_t word = j < 2 ? wv[e].x : (j < 4 ? wv[e].y : (j < 6 ? wv[e].z : wv[e].w));
+                wf[e] = (j & 1) ? bf16_hi(word) : bf16_lo(word);
+            }
+#pragma unroll
+            for (int t = 0; t < kTileTok; ++t) {
+                const uint32_t word = j < 2 ? xv[t].x : (j < 4 ? xv[t].y : (j < 6 ? xv[t].z : xv[t].w));
+                xf[t] = (j & 1) ? bf16_hi(word) : bf16_lo(word);
+            }
+#pragma unroll
+            for (int t = 0; t < kTileTok; ++t)
+#pragma unroll
+                for (int e = 0; e < kTileExp; ++e) acc[t][e] = fmaf(wf[e], xf[t], acc[t][e]);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kTileTok; ++t)
+#pragma unroll
+        for (int e = 0; e < kTileExp; ++e) {
+            const float v = warp_sum(acc[t][e]);
+            if (lane == 0 && t0 + t < T && e0 + e < E)
+                logits[(int64_t)(t0 + t) * E + e0 + e] = v + (bias != nullptr ? bias[e0 + e] : 0.f);
+        }
+}
+
 // JE = logits held per lane (E <= 32 * JE).
 template <int JE>
 __global__ void __launch_bounds__(256)
@@ -118,9 +182,17 @@ cudaError_t launch_route_topk(const uint16_t* x, const uint16_t* Wr, const float
     (void)dev;
     const int vec = (H % 8 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
                     (reinterpret_cast<uintptr_t>(Wr) % 16 == 0);
-    dim3 g1((E + kRouteWarps - 1) / kRouteWarps, (T + kRouteTokens - 1) / kRouteTokens);
-    cudaError_t err = launch_pdl(route_logits_kernel, g1, dim3(kRouteWarps * 32), 0, stream, x, Wr,
-                                 bias, T, H, E, logits, vec);
+    cudaError_t err;
+    if (vec && T >= 32) {
+        dim3 gt((E + kTileWarpsE * kTileExp - 1) / (kTileWarpsE * kTileExp),
+                (T + kTileWarpsT * kTileTok - 1) / (kTileWarpsT * kTileTok));
+        err = launch_pdl(route_logits_tiled_kernel, gt, dim3(kTileWarpsT * kTileWarpsE * 32), 0, stream, x, Wr,
+                         bias, T, H, E, logits);
+    } else {
+        dim3 g1((E + kRouteWarps - 1) / kRouteWarps, (T + kRouteTokens - 1) / kRouteTokens);
+        err = launch_pdl(route_logits_kernel, g1, dim3(kRouteWarps * 32), 0, stream, x, Wr, bias, T, H, E,
+                         logits, vec);
+    }
     if (err != cudaSuccess) return err;
     dim3 g2((T + 7) / 8);
     const float* cl = logits;

@@ -39,6 +39,8 @@ CASES = {
     "single_expert": (2, 16, 1, 1, None),
     "E1024_k32": (5, 256, 1024, 32, "normal"),
     "ragged_T_and_E": (19, 2048, 250, 8, None),
+    "tiled_ragged_T_and_E": (37, 2048, 250, 8, "normal"),
+    "tiled_E1024": (33, 512, 1024, 32, None),
 }
 
 
@@ -61,6 +63,20 @@ def test_route_parity(name):
     near = check_route(ref_logits, ref_idx, bounds, g_logits, g_idx, g_w, k)
     assert near <= max(1, T // 50), f"{near} near-tie tokens of {T}"
     assert np.all(np.abs(g_w.sum(axis=1) - 1) < 1e-5)
+
+
+@pytest.mark.parametrize("T,H,E", [(96, 2048, 256), (37, 2048, 250), (64, 520, 33)])
+def test_route_tiled_logits_equal_the_per_row_kernel(T, H, E):
+    """From 32 tokens on, the logits come from the register-tiled kernel; it performs
+    every logit's FMA chain and butterfly in the same order as the per-row kernel used
+    below 32 tokens, so the logits of one call equal, bit for bit, those of the same
+    tokens routed 8 at a time."""
+    x = synth.tokens(T, H, seed=T + E, device="cuda")
+    wr = synth.router_weights(E, H, seed=T + E, device="cuda")
+    bias = synth.bias_normal(E, seed=T).cuda()
+    whole, _, _ = _route_gpu(x, wr, bias, 8)
+    parts = [_route_gpu(x[t:t + 8].contiguous(), wr, bias, 8)[0] for t in range(0, T, 8)]
+    np.testing.assert_array_equal(whole, np.concatenate(parts))
 
 
 def test_route_exact_ties_go_to_lower_index():

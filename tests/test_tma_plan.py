@@ -283,9 +283,12 @@ def test_integer_pack_unit_matches_the_oracle_packing():
     assert checked > 2500
 
 
-TC_ROWS, TC_TOK, TC_KTILE, TC_STAGES, TC_LUTS = 128, 128, 80, 4, 2 * 256 * 16
-TC_STAGE_A = TC_KTILE // 8 * TC_ROWS * 16
-TC_STAGE_B = TC_KTILE // 8 * TC_TOK * 16
+TC_ROWS, TC_KTILE, TC_LUT = 128, 80, 256 * 4 * 8
+TC_A_STRIDE = 48
+
+
+def tc_stage_b(nt):
+    return TC_KTILE // 8 * nt * 16
 
 
 def tc_shape_ok(H, I):
@@ -293,38 +296,51 @@ def tc_shape_ok(H, I):
             and H <= 2080 and I <= 2080)
 
 
-def tc_smem(row_bytes):
-    stage_off = -(-(TC_LUTS + TC_ROWS * row_bytes) // 128) * 128
-    return stage_off, stage_off + TC_STAGES * (TC_STAGE_A + TC_STAGE_B)
+def tc_stages(nt):
+    return 4
+
+
+def tc_smem(row_bytes, nt):
+    stage_off = -(-(TC_LUT + TC_ROWS * row_bytes) // 128) * 128
+    return stage_off, stage_off + tc_stages(nt) * tc_stage_b(nt)
+
+
+def tc_tmem(nt):
+    a_base = 32 if nt < 32 else nt
+    used = a_base + tc_stages(nt) * TC_A_STRIDE
+    return a_base, used, 256 if used <= 256 else 512
 
 
 def test_tensor_path_plan_fits_and_is_aligned():
-    """The grouped tcgen05 kernels (csrc/ffn_tensor.cu): shared memory within the
-    opt-in limit for every accepted shape, the packed-row bulk copies 16-byte aligned,
-    and every MMA operand read (5 MMAs of K = 16 per stage, 16 row groups at 128 B,
-    2 core-matrix columns at rows * 16 B) and cp.async write inside its stage."""
+    """The grouped tcgen05 kernels (csrc/ffn_tensor.cu), for both token-tile widths:
+    shared memory within the opt-in limit for every accepted shape and the epilogue
+    buffers inside it, the packed-row bulk copies 16-byte aligned, every MMA read of a
+    B stage (5 MMAs of K = 16, NT/8 row groups at 128 B, 2 core-matrix columns at
+    NT * 16 B) inside the stage, and the tensor-memory columns (accumulator, A stages
+    of 40 columns at a 48-column stride, four stages) inside the power-of-two
+    allocation."""
     shapes = [(H, I) for H in range(128, 2081, 128) for I in range(128, 2081, 64)]
-    for H, I in shapes:
-        assert tc_shape_ok(H, I)
-        # B operand maps: (8, max(S, 128), cols / 8) with a (8, 128, 10) box; strides
-        # cols * 2 and 16 bytes are multiples of 16, the box's first coordinate is 0
-        for cols in (H, I):
-            assert cols // 8 >= TC_KTILE // 8 and (cols * 2) % 16 == 0
-        for rb, rows_per_cta, mstep, mtot in ((nbytes(H), TC_ROWS // 2, TC_ROWS // 2, I),
-                                              (nbytes(I), TC_ROWS, TC_ROWS, H)):
-            _, total = tc_smem(rb)
-            assert total + 1280 <= 232448, (H, I, total)
-            size = rows_per_cta * rb
-            for e in (0, 1, 7):
-                for m0 in range(0, mtot, mstep):
-                    _check((e * mtot + m0) * rb, size, (e + 1) * mtot * rb, f"tc H={H} I={I}")
-    for q in range(TC_KTILE // 16):
-        start = q * 2 * TC_ROWS * 16
-        last = start + TC_ROWS * 16 + (TC_ROWS // 8 - 1) * 128 + 127
-        assert last < TC_STAGE_A and q * 2 * TC_TOK * 16 + TC_TOK * 16 + (TC_TOK // 8 - 1) * 128 + 127 < TC_STAGE_B
-    assert (TC_KTILE // 8 - 1) * TC_TOK * 16 + (TC_TOK - 1) * 16 + 16 <= TC_STAGE_B
-    # epilogue buffers reuse the stages
-    assert TC_TOK * 64 * 4 + TC_TOK * 64 * 2 <= TC_STAGES * (TC_STAGE_A + TC_STAGE_B)
-    assert TC_TOK * TC_ROWS * 4 <= TC_STAGES * (TC_STAGE_A + TC_STAGE_B)
+    for nt in (16, 128):
+        a_base, used, alloc = tc_tmem(nt)
+        assert nt <= a_base and a_base % 16 == 0
+        assert a_base + (tc_stages(nt) - 1) * TC_A_STRIDE + TC_KTILE // 2 <= used <= alloc
+        assert alloc in (256, 512) and (nt == 16) == (alloc == 256)
+        sb = tc_stage_b(nt)
+        for q in range(TC_KTILE // 16):
+            assert q * 2 * nt * 16 + nt * 16 + (nt // 8 - 1) * 128 + 127 < sb
+        for H, I in shapes:
+            assert tc_shape_ok(H, I)
+            for cols in (H, I):
+                assert cols // 8 >= TC_KTILE // 8 and (cols * 2) % 16 == 0
+            for rb, rows_per_cta, mstep, mtot, epi in (
+                    (nbytes(H), TC_ROWS // 2, TC_ROWS // 2, I, nt * 64 * 4 + nt * 64 * 2),
+                    (nbytes(I), TC_ROWS, TC_ROWS, H, nt * TC_ROWS * 4)):
+                stage_off, total = tc_smem(rb, nt)
+                assert total + 1280 <= 232448, (H, I, nt, total)
+                assert TC_LUT + epi <= total
+                size = rows_per_cta * rb
+                for e in (0, 1, 7):
+                    for m0 in range(0, mtot, mstep):
+                        _check((e * mtot + m0) * rb, size, (e + 1) * mtot * rb, f"tc H={H} I={I}")
     assert not tc_shape_ok(2080, 512) and not tc_shape_ok(2048, 520) and not tc_shape_ok(40, 24)
     assert not tc_shape_ok(128, 64)
