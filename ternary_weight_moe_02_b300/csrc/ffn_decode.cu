@@ -509,12 +509,11 @@ FfnWorkspaceLayout ffn_workspace_layout(int T, int k, int E, int H, int I) {
     L.tensor = ffn_use_tensor(T, k, E, H, I);
     L.tile_off = L.xs = L.hs = L.ys = o;
     if (L.tensor) {
-        const size_t R = (size_t)ffn_tensor_b_rows((int)S);
         o = align_up(o + 4 * ((size_t)E + 1), 256);
         L.xs = o;
-        o = align_up(o + 2 * R * (size_t)H, 256);
+        o = align_up(o + ffn_tensor_x_bytes((int)S, E, H), 256);
         L.hs = o;
-        o = align_up(o + 2 * R * (size_t)I, 256);
+        o = align_up(o + ffn_tensor_h_bytes((int)S, E, I), 256);
         L.ys = o;
         o = align_up(o + 4 * S * (size_t)H, 256);
     }

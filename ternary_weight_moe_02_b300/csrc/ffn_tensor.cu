@@ -22,13 +22,13 @@
 // or 0 (half the trit, exact; the epilogues scale by 2 s), two per 32-bit column, with
 // tcgen05.st; the MMA reads A from tensor memory.  B (tokens) sits in shared memory
 // K-major without swizzle: element (n, k) of a stage at (k / 8) * (NT * 16) + n * 16 +
-// (k % 8) * 2, which is what a 3-D TMA box (8 values, NT rows, 10 chunks) of a
-// row-major [rows][K] matrix writes.  K tiles hold 80 values (16 packed bytes per row).
+// (k % 8) * 2.  The gather kernel (for x) and the gate/up epilogue (for h) store each
+// tile's rows in global memory in that same order (chunk-major, [tile][K/8][NT][8]),
+// so a stage is one contiguous block loaded by one 1-D bulk copy.  K tiles hold 80
+// values (16 packed bytes per row).
 // Eight producer warps fill a ring of four stages; one thread issues five tcgen05.mma
 // (K = 16 each) per stage and commits them to the stage's "empty" mbarrier, which the
 // producers wait for before refilling the stage.  All waits are bounded.
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdlib.h>
@@ -44,7 +44,7 @@ namespace {
 constexpr int kRows = 128;                 // MMA M: weight rows per CTA
 constexpr int kKTile = 80;                 // K values per stage (16 packed bytes)
 constexpr int kChunks = kKTile / 8;        // 16-byte core-matrix columns per B stage
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 4;
 constexpr int kAStride = 48;               // TMEM column stride between A stages (40 used)
 constexpr int kLutReps = 4;                // copies of the decode table, by lane & 3
 constexpr int kLutBytes = 256 * kLutReps * 8;  // 8 KB
@@ -133,17 +133,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// B tile: an (8, NT, kChunks) box at rows row0.., K chunks chunk0.. of a 3-D tensor
-// map; the copy's bytes complete on `bar`
-__device__ __forceinline__ void tma_load_b(void* dst, const CUtensorMap* map, int row0, int chunk0,
-                                           uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
-            smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row0), "r"(chunk0), "r"(smem_addr(bar))
-        : "memory");
-}
-
 // ----------------------------------------------------------------- decode table
 
 // For each code, the high bytes of the five bf16 values +-0.5 / 0 of its trits (0xBF
@@ -204,8 +193,8 @@ struct TcArgs {
     const int32_t* offsets;
     const int32_t* perm;
     const int32_t* tile_off;  // [E + 1] prefix of ceil(counts / NT)
-    uint16_t* xs;             // [T k][H] bf16, the slots' tokens in expert order
-    uint16_t* hs;             // [T k][I] bf16, slots in expert order
+    uint16_t* xs;             // [tile][H / 8][NT][8] bf16: each tile's token rows
+    uint16_t* hs;             // [tile][I / 8][NT][8] bf16: each tile's h rows
     float* ys;                // [T k][H] fp32, per original slot
     float* y;                 // [T][H]
     int T;
@@ -224,22 +213,24 @@ __host__ __device__ constexpr size_t tc_smem_bytes(int row_bytes) {
 }
 
 // Finds the expert and token range of grid row `tile`; false when past the last tile.
+// The tile table, counts and offsets come from kernels that completed before the
+// previous one started, so they are read (through L2) before this grid's PDL wait.
 template <int NT>
 __device__ __forceinline__ bool tc_tile(const TcArgs& a, int tile, int& e, int& n0, int& nv, int& pos0) {
-    if (tile >= a.tile_off[a.E]) return false;
+    if (tile >= __ldcg(a.tile_off + a.E)) return false;
     int lo = 0, hi = a.E - 1;  // largest e with tile_off[e] <= tile
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (a.tile_off[mid] <= tile)
+        if (__ldcg(a.tile_off + mid) <= tile)
             lo = mid;
         else
             hi = mid - 1;
     }
     e = lo;
-    n0 = (tile - a.tile_off[e]) * NT;
-    const int left = a.counts[e] - n0;
+    n0 = (tile - __ldcg(a.tile_off + e)) * NT;
+    const int left = __ldcg(a.counts + e) - n0;
     nv = left < NT ? left : NT;
-    pos0 = a.offsets[e] + n0;
+    pos0 = __ldcg(a.offsets + e) + n0;
     return nv > 0;
 }
 
@@ -257,12 +248,13 @@ struct TcBars {
 // Warp-specialised main loop.  Warp w < 8 produces: its thread owns row 32 (w & 3) +
 // lane (the warp's TMEM lane quarter) and decodes half w >> 2 of that row's 16 bytes of
 // each K tile into A stage s (tensor memory), then arrives on full[s]; thread 0 also
-// loads the stage's B tile (rows row0.., this K tile's chunks) by TMA onto bfull[s].
+// copies the stage's B block (this K tile's chunks of the tile's operand block bsrc,
+// fewer at the K tail) with one bulk copy onto bfull[s].
 // Warp 8 lane 0 waits for both, issues the stage's five MMAs and commits empty[s]; its
 // last commit goes to done.  Returns false if a bounded wait gave up.
 template <int NT>
-__device__ bool tc_mainloop(unsigned char* smem, const uint8_t* packed, int rb, int Kdim, const CUtensorMap* bmap,
-                            int row0, uint32_t tmem, TcBars& bars, int* status) {
+__device__ bool tc_mainloop(unsigned char* smem, const uint8_t* packed, int rb, int Kdim, const uint16_t* bsrc,
+                            uint32_t tmem, TcBars& bars, int* status) {
     using Cfg = TileCfg<NT>;
     constexpr int S = Cfg::kStages;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -275,6 +267,9 @@ __device__ bool tc_mainloop(unsigned char* smem, const uint8_t* packed, int rb, 
         const int q = warp & 3, h = warp >> 2, r = 32 * q + lane;
         const uint8_t* my_row = packed + r * rb;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+        // tile j + 1 is decoded while tile j's tensor-memory stores complete
+        uint32_t cur[20], nxt[20];
+        decode_half_tile(my_row, rb, 0, h, lut, lane & (kLutReps - 1), cur);
         for (int j = 0; j < KT && ok; ++j) {
             const int s = j % S;
             if (j >= S && !mbar_wait_bounded(&bars.empty[s], (uint32_t)(((j - S) / S) & 1), status)) {
@@ -282,18 +277,21 @@ __device__ bool tc_mainloop(unsigned char* smem, const uint8_t* packed, int rb, 
                 break;
             }
             if (tid == 0) {
-                mbar_arrive_expect_tx(&bars.bfull[s], (uint32_t)Cfg::kStageB);
-                tma_load_b(stages + s * Cfg::kStageB, bmap, row0, j * kChunks, &bars.bfull[s]);
+                const int left = Kdim / 8 - j * kChunks;
+                const uint32_t bytes = (uint32_t)((left < kChunks ? left : kChunks) * NT * 16);
+                mbar_arrive_expect_tx(&bars.bfull[s], bytes);
+                bulk_copy_g2s(stages + s * Cfg::kStageB, bsrc + (size_t)j * kChunks * NT * 8, bytes, &bars.bfull[s]);
                 issued = j + 1;
             }
-            uint32_t words[20];
-            decode_half_tile(my_row, rb, j, h, lut, lane & (kLutReps - 1), words);
             const uint32_t col = (uint32_t)(Cfg::kABase + s * kAStride + 20 * h);
-            tmem_st16(lane_base + col, words);
-            tmem_st4(lane_base + col + 16, words + 16);
+            tmem_st16(lane_base + col, cur);
+            tmem_st4(lane_base + col + 16, cur + 16);
+            if (j + 1 < KT) decode_half_tile(my_row, rb, j + 1, h, lut, lane & (kLutReps - 1), nxt);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             mbar_arrive(&bars.full[s]);
+#pragma unroll
+            for (int i = 0; i < 20; ++i) cur[i] = nxt[i];
         }
     } else if (tid == kProducerWarps * 32) {
         for (int j = 0; j < KT; ++j) {
@@ -326,13 +324,19 @@ __device__ bool tc_mainloop(unsigned char* smem, const uint8_t* packed, int rb, 
     return !__syncthreads_or(!ok);
 }
 
-// CTA prologue shared by both stages: decode table, barriers, TMEM (warp 8), and the
-// bulk copy of the CTA's packed rows (nrows_copy rows of rb bytes from src0 and, when
-// src1 is set, as many from src1).
+// CTA prologue shared by both stages: decode table, zeroed B stages, barriers, TMEM
+// (warp 8), and the bulk copy of the CTA's packed rows (nrows_copy rows of rb bytes
+// from src0 and, when src1 is set, as many from src1).
 __device__ bool tc_prologue(unsigned char* smem, TcBars& bars, uint32_t* tmem_slot, uint32_t tmem_cols,
-                            const uint8_t* src0, const uint8_t* src1, int nrows_copy, int rb, int* status) {
+                            const uint8_t* src0, const uint8_t* src1, int nrows_copy, int rb, size_t stage_bytes,
+                            int* status) {
     const int tid = threadIdx.x;
     build_half_lut(reinterpret_cast<uint2*>(smem), tid, blockDim.x);
+    // zero the B stages: the K tail's chunks are never copied, and the MMA multiplies
+    // them by zero A values, which must not meet NaN bit patterns
+    uint4* st4 = reinterpret_cast<uint4*>(smem + tc_stage_offset(rb));
+    for (size_t i = tid; i < stage_bytes / 16; i += blockDim.x) st4[i] = make_uint4(0u, 0u, 0u, 0u);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (tid == 0) {
         for (int i = 0; i < kMaxStages; ++i) {
             mbar_init(&bars.full[i], kProducerWarps * 32);
@@ -363,58 +367,63 @@ __device__ __forceinline__ void tc_release(uint32_t tmem, uint32_t tmem_cols) {
 // gate/up: grid (I / 64, max tiles); rows 0..63 of the CTA are gate rows m0..m0+63 of
 // the expert, rows 64..127 the same up rows.
 template <int NT>
-__global__ void __launch_bounds__(kThreads, 1) tc_gateup_kernel(TcArgs a, const __grid_constant__ CUtensorMap xmap) {
+__global__ void __launch_bounds__(kThreads, 1) tc_gateup_kernel(TcArgs a) {
     using Cfg = TileCfg<NT>;
     constexpr int CW = NT / 2;  // columns per epilogue warp (two warps per lane quarter)
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ TcBars bars;
     __shared__ uint32_t tmem_slot;
-    pdl_wait();
-    pdl_launch_dependents();
+    __shared__ float s_scale[kRows];  // 2 s of rows 0..127 (gate rows, then up rows)
     int e, n0, nv, pos0;
     if (!tc_tile<NT>(a, blockIdx.y, e, n0, nv, pos0)) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, I = a.I, Bh = (H + 4) / 5;
     const int m0 = blockIdx.x * (kRows / 2);
+    const int tile = blockIdx.y;
+    if (tid < kRows)
+        s_scale[tid] = 2.f * (tid < kRows / 2 ? a.s_gate[(int64_t)e * I + m0 + tid]
+                                             : a.s_up[(int64_t)e * I + m0 + tid - kRows / 2]);
     const uint8_t* gsrc = a.gate + ((int64_t)e * I + m0) * Bh;
     const uint8_t* usrc = a.up + ((int64_t)e * I + m0) * Bh;
-    bool ok = tc_prologue(smem, bars, &tmem_slot, Cfg::kTmemCols, gsrc, usrc, kRows / 2, Bh, a.status);
+    // everything up to here reads data no kernel of this call writes
+    bool ok = tc_prologue(smem, bars, &tmem_slot, Cfg::kTmemCols, gsrc, usrc, kRows / 2, Bh,
+                          (size_t)Cfg::kStages * Cfg::kStageB, a.status);
     const uint32_t tmem = tmem_slot;
-    if (ok) ok = tc_mainloop<NT>(smem, smem + tc_packed_offset(), Bh, H, &xmap, pos0, tmem, bars, a.status);
+    pdl_wait();  // the gathered x of the previous kernel
+    pdl_launch_dependents();
+    if (ok) ok = tc_mainloop<NT>(smem, smem + tc_packed_offset(), Bh, H, a.xs + (size_t)tile * H * NT, tmem, bars, a.status);
     if (ok) {
-        // epilogue over eight warps: warp w reads rows 32 (w & 3) + lane (gate rows for
-        // w & 3 < 2, up rows otherwise) and columns CW (w >> 2) .. +CW
+        // epilogue: warps 0-7 read rows 32 (w & 3) + lane and columns CW (w >> 2) .. +CW,
+        // store min(2 s_g g, clamp) (gate rows) or clamp(2 s_u u) (up rows); then every
+        // thread forms h = silu(g) u for its share of the tile and rounds it to bf16
         unsigned char* epi = smem + tc_packed_offset();
-        float* U = reinterpret_cast<float*>(epi);                       // [NT][64]
-        uint16_t* Hs = reinterpret_cast<uint16_t*>(epi + NT * 64 * 4);  // [NT][64]
-        float v[CW];
+        float* G = reinterpret_cast<float*>(epi);                             // [NT][64]
+        float* U = G + NT * 64;                                               // [NT][64]
+        uint16_t* Hs = reinterpret_cast<uint16_t*>(U + NT * 64);              // [NT][64]
         if (warp < kProducerWarps) {
-            const int q = warp & 3, c0 = CW * (warp >> 2);
+            const int q = warp & 3, c0 = CW * (warp >> 2), r = 32 * q + lane;
             const uint32_t addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
+            const float sc = s_scale[r];
+            float v[CW];
 #pragma unroll
             for (int i = 0; i < CW; i += 8) tmem_ld8(addr + i, v + i);
-            if (q >= 2) {
-                const int r = 32 * (q - 2) + lane;
-                const float su = 2.f * a.s_up[(int64_t)e * I + m0 + r];
+            if (q < 2) {
 #pragma unroll
-                for (int i = 0; i < CW; ++i) U[(c0 + i) * 64 + r] = fminf(fmaxf(su * v[i], -a.clamp), a.clamp);
+                for (int i = 0; i < CW; ++i) G[(c0 + i) * 64 + r] = fminf(sc * v[i], a.clamp);
+            } else {
+#pragma unroll
+                for (int i = 0; i < CW; ++i) U[(c0 + i) * 64 + r - 64] = fminf(fmaxf(sc * v[i], -a.clamp), a.clamp);
             }
         }
         __syncthreads();
-        if (warp < kProducerWarps && (warp & 3) < 2) {
-            const int r = 32 * (warp & 3) + lane, c0 = CW * (warp >> 2);
-            const float sg = 2.f * a.s_gate[(int64_t)e * I + m0 + r];
-#pragma unroll
-            for (int i = 0; i < CW; ++i) {
-                const float g = fminf(sg * v[i], a.clamp);
-                Hs[(c0 + i) * 64 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(silu_f(g) * U[(c0 + i) * 64 + r]));
-            }
-        }
+        for (int i = tid; i < nv * 64; i += kThreads)
+            Hs[i] = __bfloat16_as_ushort(__float2bfloat16_rn(silu_f(G[i]) * U[i]));
         __syncthreads();
-        // rows of 64 bf16 (128 bytes) per token into the expert-ordered h
+        // the tile's h rows, chunk-major: chunk m0 / 8 + part, row nn
+        uint16_t* hblk = a.hs + (size_t)tile * I * NT;
         for (int i = tid; i < nv * 8; i += kThreads) {
-            const int nn = i >> 3, part = i & 7;
-            *reinterpret_cast<uint4*>(a.hs + (int64_t)(pos0 + nn) * I + m0 + 8 * part) =
+            const int part = i / nv, nn = i - part * nv;
+            *reinterpret_cast<uint4*>(hblk + ((size_t)(m0 / 8 + part) * NT + nn) * 8) =
                 *reinterpret_cast<const uint4*>(Hs + nn * 64 + 8 * part);
         }
     }
@@ -423,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gateup_kernel(TcArgs a, const 
 
 // down: grid (H / 128, max tiles); the CTA's 128 rows are down rows m0..m0+127.
 template <int NT>
-__global__ void __launch_bounds__(kThreads, 1) tc_down_kernel(TcArgs a, const __grid_constant__ CUtensorMap hmap) {
+__global__ void __launch_bounds__(kThreads, 1) tc_down_kernel(TcArgs a) {
     using Cfg = TileCfg<NT>;
     constexpr int CW = NT / 2;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -431,28 +440,34 @@ __global__ void __launch_bounds__(kThreads, 1) tc_down_kernel(TcArgs a, const __
     __shared__ uint32_t tmem_slot;
     __shared__ int s_slot[NT];
     __shared__ float s_w[NT];
-    pdl_wait();
-    pdl_launch_dependents();
+    __shared__ float s_scale[kRows];
     int e, n0, nv, pos0;
     if (!tc_tile<NT>(a, blockIdx.y, e, n0, nv, pos0)) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, I = a.I, Bi = (I + 4) / 5;
     const int m0 = blockIdx.x * kRows;
     if (tid < NT) {
-        const int slot = tid < nv ? a.perm[pos0 + tid] : 0;
+        const int slot = tid < nv ? __ldcg(a.perm + pos0 + tid) : 0;
         s_slot[tid] = slot;
-        s_w[tid] = tid < nv ? a.w[slot] : 0.f;
+        s_w[tid] = tid < nv ? __ldcg(a.w + slot) : 0.f;
     }
+    if (tid < kRows) s_scale[tid] = 2.f * a.s_down[(int64_t)e * H + m0 + tid];
     const uint8_t* dsrc = a.down + ((int64_t)e * H + m0) * Bi;
-    bool ok = tc_prologue(smem, bars, &tmem_slot, Cfg::kTmemCols, dsrc, nullptr, kRows, Bi, a.status);
+    // everything up to here reads data no kernel of this call writes after the grouping
+    bool ok = tc_prologue(smem, bars, &tmem_slot, Cfg::kTmemCols, dsrc, nullptr, kRows, Bi,
+                          (size_t)Cfg::kStages * Cfg::kStageB, a.status);
     const uint32_t tmem = tmem_slot;
-    if (ok) ok = tc_mainloop<NT>(smem, smem + tc_packed_offset(), Bi, I, &hmap, pos0, tmem, bars, a.status);
+    pdl_wait();  // h of the gate/up kernel
+    pdl_launch_dependents();
+    if (ok)
+        ok = tc_mainloop<NT>(smem, smem + tc_packed_offset(), Bi, I, a.hs + (size_t)blockIdx.y * I * NT, tmem, bars,
+                             a.status);
     if (ok) {
         float* Ys = reinterpret_cast<float*>(smem + tc_packed_offset());  // [NT][kRows]
         if (warp < kProducerWarps) {
             const int q = warp & 3, c0 = CW * (warp >> 2), r = 32 * q + lane;
             const uint32_t addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
-            const float sd = 2.f * a.s_down[(int64_t)e * H + m0 + r];
+            const float sd = s_scale[r];
             float v[CW];
 #pragma unroll
             for (int i = 0; i < CW; i += 8) tmem_ld8(addr + i, v + i);
@@ -469,20 +484,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_down_kernel(TcArgs a, const __
     tc_release(tmem, Cfg::kTmemCols);
 }
 
-// xs[pos] = x[token of slot perm[pos]] for the offsets[E] grouped slots, 16 bytes per
-// thread and step.
+// One CTA per tile: the tile's token rows of x, chunk-major ([H / 8][NT][8]), rows
+// past the tile's tokens zero.
+template <int NT>
 __global__ void __launch_bounds__(256) tc_gather_kernel(TcArgs a) {
     pdl_wait();
     pdl_launch_dependents();
-    const int n_slots = a.offsets[a.E];
+    int e, n0, nv, pos0;
+    if (!tc_tile<NT>(a, blockIdx.x, e, n0, nv, pos0)) return;
     const int H8 = a.H / 8;
-    const int64_t total = (int64_t)n_slots * H8;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int pos = (int)(i / H8), c = (int)(i - (int64_t)pos * H8);
-        const int t = a.perm[pos] / a.k;
-        reinterpret_cast<uint4*>(a.xs + (int64_t)pos * a.H)[c] =
-            reinterpret_cast<const uint4*>(a.x + (int64_t)t * a.H)[c];
+    uint4* blk = reinterpret_cast<uint4*>(a.xs + (size_t)blockIdx.x * a.H * NT);
+    for (int i = threadIdx.x; i < H8 * NT; i += blockDim.x) {
+        const int c = i / NT, r = i - c * NT;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r < nv) v = reinterpret_cast<const uint4*>(a.x + (int64_t)(a.perm[pos0 + r] / a.k) * a.H)[c];
+        blk[i] = v;
     }
 }
 
@@ -542,12 +558,18 @@ __global__ void __launch_bounds__(1024) tc_tile_prefix_kernel(const int32_t* __r
     if (tid == E - 1) tile_off[E] = excl + v;
 }
 
+}  // namespace
+
 // Token-tile width of a call: 128 when the slots average at least 64 per expert
 // (prefill), 16 otherwise (decode batches: fewer padded MMA columns and a smaller
 // TMEM allocation, so that two CTAs share an SM).
-int tile_tokens(int S, int E) { return (int64_t)S >= 64 * (int64_t)E ? 128 : 16; }
+int ffn_tensor_tile_tokens(int S, int E) { return (int64_t)S >= 64 * (int64_t)E ? 128 : 16; }
 
-}  // namespace
+// An upper bound of the number of tiles, sum over experts of ceil(n_e / NT).
+int ffn_tensor_max_tiles(int S, int E) {
+    const int nt = ffn_tensor_tile_tokens(S, E);
+    return (S + nt - 1) / nt + (E < S ? E : S);
+}
 
 // MAPLE_FFN_PATH=tensor or =cores forces a path (for parity tests of both on the same
 // inputs); otherwise the tensor path runs once there are at least half as many slots
@@ -567,43 +589,21 @@ bool ffn_tensor_shape_ok(int H, int I) {
     return H % kRows == 0 && I % (kRows / 2) == 0 && H >= 128 && I >= 128 && H <= 2080 && I <= 2080;
 }
 
-int ffn_tensor_b_rows(int S) { return S > 128 ? S : 128; }
+size_t ffn_tensor_x_bytes(int S, int E, int H) {
+    const int nt = ffn_tensor_tile_tokens(S, E);
+    return (size_t)ffn_tensor_max_tiles(S, E) * H * nt * 2;
+}
+
+size_t ffn_tensor_h_bytes(int S, int E, int I) {
+    const int nt = ffn_tensor_tile_tokens(S, E);
+    return (size_t)ffn_tensor_max_tiles(S, E) * I * nt * 2;
+}
 
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::mutex mu;
-    std::lock_guard<std::mutex> lock(mu);
-    if (fn == nullptr) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// A row-major bf16 [rows][cols] matrix as a 3-D map (8 values, rows, cols / 8) whose box
-// (8, nt, kChunks) lands in shared memory as the K-major no-swizzle operand layout.
-cudaError_t make_rows_map(CUtensorMap* map, const uint16_t* base, int rows, int cols, int nt) {
-    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-    if (encode == nullptr) return cudaErrorNotSupported;
-    const cuuint64_t dims[3] = {8, (cuuint64_t)rows, (cuuint64_t)(cols / 8)};
-    const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, 16};
-    const cuuint32_t box[3] = {8, (cuuint32_t)nt, kChunks};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides,
-                              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <int NT>
 cudaError_t launch_tc_ffn(const TcArgs& a, int S, cudaStream_t stream) {
-    const int tiles = (S + NT - 1) / NT + (a.E < S ? a.E : S);  // >= sum of ceil(n_e / NT)
+    const int tiles = ffn_tensor_max_tiles(S, a.E);
     const int Bh = (a.H + 4) / 5, Bi = (a.I + 4) / 5;
     const size_t smem_gu = tc_smem_bytes<NT>(Bh), smem_dn = tc_smem_bytes<NT>(Bi);
     auto gu = tc_gateup_kernel<NT>;
@@ -612,22 +612,18 @@ cudaError_t launch_tc_ffn(const TcArgs& a, int S, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     err = ensure_dynamic_smem(dn, smem_dn);
     if (err != cudaSuccess) return err;
-    const int R = ffn_tensor_b_rows(S);
-    CUtensorMap xmap, hmap;
-    err = make_rows_map(&xmap, a.xs, R, a.H, NT);
+    err = launch_pdl(tc_gather_kernel<NT>, dim3(tiles), dim3(256), 0, stream, a);
     if (err != cudaSuccess) return err;
-    err = make_rows_map(&hmap, a.hs, R, a.I, NT);
+    err = launch_pdl(gu, dim3(a.I / (kRows / 2), tiles), dim3(kThreads), smem_gu, stream, a);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(gu, dim3(a.I / (kRows / 2), tiles), dim3(kThreads), smem_gu, stream, a, xmap);
-    if (err != cudaSuccess) return err;
-    return launch_pdl(dn, dim3(a.H / kRows, tiles), dim3(kThreads), smem_dn, stream, a, hmap);
+    return launch_pdl(dn, dim3(a.H / kRows, tiles), dim3(kThreads), smem_dn, stream, a);
 }
 
 }  // namespace
 
 cudaError_t launch_moe_ffn_tensor(const FfnArgs& f, cudaStream_t stream, const DeviceInfo& dev) {
     const int S = f.T * f.k;
-    const int nt = tile_tokens(S, f.E);
+    const int nt = ffn_tensor_tile_tokens(S, f.E);
     cudaError_t err = launch_group_tokens(f.idx, S, f.k, f.E, f.counts, f.offsets, f.perm, f.active,
                                           f.n_active, stream, dev);
     if (err != cudaSuccess) return err;
@@ -659,13 +655,6 @@ cudaError_t launch_moe_ffn_tensor(const FfnArgs& f, cudaStream_t stream, const D
     a.y = f.y;
     a.T = f.T;
     a.status = f.status;
-    {
-        const int64_t work = (int64_t)S * (f.H / 8);
-        const int64_t want = (work + 255) / 256;
-        const int64_t cap = (int64_t)dev.sm_count * 8;
-        err = launch_pdl(tc_gather_kernel, dim3((unsigned)(want < cap ? want : cap)), dim3(256), 0, stream, a);
-        if (err != cudaSuccess) return err;
-    }
     err = nt == 128 ? launch_tc_ffn<128>(a, S, stream) : launch_tc_ffn<16>(a, S, stream);
     if (err != cudaSuccess) return err;
     const int64_t work = (int64_t)f.T * (f.H / 4);

@@ -59,8 +59,8 @@ struct FfnArgs {
     int32_t* n_active; // [1]
     float* h;          // [T*k][I] (bf16 [T*k][I] on the tensor path)
     int32_t* tile_off; // [E+1] tensor path only
-    uint16_t* xs;      // [max(T*k, 128)][H] bf16, tensor path only
-    uint16_t* hs;      // [max(T*k, 128)][I] bf16, tensor path only
+    uint16_t* xs;      // tensor path only: per tile, the tokens' x rows, chunk-major
+    uint16_t* hs;      // tensor path only: per tile, the tokens' h rows, chunk-major
     float* ys;         // [T*k][H] tensor path only
     int* status;       // device status word
     int prefetch_down; // 1 if the down rows may be bulk-prefetched (16-byte multiples)
@@ -78,7 +78,10 @@ cudaError_t launch_moe_ffn(const FfnArgs& a, cudaStream_t stream, const DeviceIn
 // the launch (group, tile prefix, gate/up, down, combine).
 bool ffn_tensor_shape_ok(int H, int I);
 bool ffn_use_tensor(int T, int k, int E, int H, int I);
-int ffn_tensor_b_rows(int S);
+int ffn_tensor_tile_tokens(int S, int E);
+int ffn_tensor_max_tiles(int S, int E);
+size_t ffn_tensor_x_bytes(int S, int E, int H);
+size_t ffn_tensor_h_bytes(int S, int E, int I);
 cudaError_t launch_moe_ffn_tensor(const FfnArgs& a, cudaStream_t stream, const DeviceInfo& dev);
 
 // Fused single-token layer step (route + gate/up + down in one cooperative launch).

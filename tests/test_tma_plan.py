@@ -333,7 +333,7 @@ def test_tensor_path_plan_fits_and_is_aligned():
             for cols in (H, I):
                 assert cols // 8 >= TC_KTILE // 8 and (cols * 2) % 16 == 0
             for rb, rows_per_cta, mstep, mtot, epi in (
-                    (nbytes(H), TC_ROWS // 2, TC_ROWS // 2, I, nt * 64 * 4 + nt * 64 * 2),
+                    (nbytes(H), TC_ROWS // 2, TC_ROWS // 2, I, nt * 64 * (4 + 4 + 2)),
                     (nbytes(I), TC_ROWS, TC_ROWS, H, nt * TC_ROWS * 4)):
                 stage_off, total = tc_smem(rb, nt)
                 assert total + 1280 <= 232448, (H, I, nt, total)
@@ -344,3 +344,24 @@ def test_tensor_path_plan_fits_and_is_aligned():
                         _check((e * mtot + m0) * rb, size, (e + 1) * mtot * rb, f"tc H={H} I={I}")
     assert not tc_shape_ok(2080, 512) and not tc_shape_ok(2048, 520) and not tc_shape_ok(40, 24)
     assert not tc_shape_ok(128, 64)
+
+
+def test_tensor_path_operand_blocks_are_aligned_and_in_bounds():
+    """The B operand of a tile lives in global memory as [K / 8][NT][8] bf16 (the
+    gather kernel writes x that way, the gate/up epilogue h); each K tile's stage is
+    one bulk copy of up to 10 chunks, fewer at the K tail.  Every copy starts on a
+    16-byte boundary, has a multiple of 16 bytes and stays inside its tile's block."""
+    for nt in (16, 128):
+        for K in (128, 192, 384, 512, 2048):
+            block = K * nt * 2
+            KT = -(-K // TC_KTILE)
+            covered = 0
+            for j in range(KT):
+                left = K // 8 - j * (TC_KTILE // 8)
+                nbytes = min(left, TC_KTILE // 8) * nt * 16
+                off = j * (TC_KTILE // 8) * nt * 16
+                for tile in (0, 1, 5):
+                    _check(tile * block + off, nbytes, (tile + 1) * block, f"B nt={nt} K={K} j={j}")
+                assert nbytes <= tc_stage_b(nt)
+                covered += nbytes
+            assert covered == block
