@@ -227,6 +227,7 @@ int maple_moe_ffn(const maple_experts* ex, const uint16_t* x, const int32_t* idx
     a.n_active = reinterpret_cast<int32_t*>(base + L.n_active);
     a.h = reinterpret_cast<float*>(base + L.h);
     a.tile_off = reinterpret_cast<int32_t*>(base + L.tile_off);
+    a.chunks = reinterpret_cast<int32_t*>(base + L.chunks);
     a.xs = reinterpret_cast<uint16_t*>(base + L.xs);
     a.hs = reinterpret_cast<uint16_t*>(base + L.hs);
     a.ys = reinterpret_cast<float*>(base + L.ys);

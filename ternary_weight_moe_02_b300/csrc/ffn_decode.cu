@@ -507,9 +507,11 @@ FfnWorkspaceLayout ffn_workspace_layout(int T, int k, int E, int H, int I) {
     L.h = o;
     o = align_up(o + 4 * S * (size_t)I, 256);
     L.tensor = ffn_use_tensor(T, k, E, H, I);
-    L.tile_off = L.xs = L.hs = L.ys = o;
+    L.tile_off = L.chunks = L.xs = L.hs = L.ys = o;
     if (L.tensor) {
         o = align_up(o + 4 * ((size_t)E + 1), 256);
+        L.chunks = o;
+        o = align_up(o + group_chunked_bytes((int)S, E), 256);
         L.xs = o;
         o = align_up(o + ffn_tensor_x_bytes((int)S, E, H), 256);
         L.hs = o;

@@ -484,8 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_down_kernel(TcArgs a) {
     tc_release(tmem, Cfg::kTmemCols);
 }
 
-// One CTA per tile: the tile's token rows of x, chunk-major ([H / 8][NT][8]), rows
-// past the tile's tokens zero.
+// One CTA per tile: the tile's token rows of x, chunk-major ([H / 8][NT][8]).  Rows
+// past the tile's tokens are left as they are: they only reach output columns that
+// the epilogues never store.
 template <int NT>
 __global__ void __launch_bounds__(256) tc_gather_kernel(TcArgs a) {
     pdl_wait();
@@ -494,11 +495,9 @@ __global__ void __launch_bounds__(256) tc_gather_kernel(TcArgs a) {
     if (!tc_tile<NT>(a, blockIdx.x, e, n0, nv, pos0)) return;
     const int H8 = a.H / 8;
     uint4* blk = reinterpret_cast<uint4*>(a.xs + (size_t)blockIdx.x * a.H * NT);
-    for (int i = threadIdx.x; i < H8 * NT; i += blockDim.x) {
-        const int c = i / NT, r = i - c * NT;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r < nv) v = reinterpret_cast<const uint4*>(a.x + (int64_t)(a.perm[pos0 + r] / a.k) * a.H)[c];
-        blk[i] = v;
+    for (int i = threadIdx.x; i < H8 * nv; i += blockDim.x) {
+        const int c = i / nv, r = i - c * nv;
+        blk[c * NT + r] = reinterpret_cast<const uint4*>(a.x + (int64_t)(a.perm[pos0 + r] / a.k) * a.H)[c];
     }
 }
 
@@ -624,8 +623,11 @@ cudaError_t launch_tc_ffn(const TcArgs& a, int S, cudaStream_t stream) {
 cudaError_t launch_moe_ffn_tensor(const FfnArgs& f, cudaStream_t stream, const DeviceInfo& dev) {
     const int S = f.T * f.k;
     const int nt = ffn_tensor_tile_tokens(S, f.E);
-    cudaError_t err = launch_group_tokens(f.idx, S, f.k, f.E, f.counts, f.offsets, f.perm, f.active,
-                                          f.n_active, stream, dev);
+    // one CTA groups a few thousand slots fastest; beyond that, chunks in parallel
+    cudaError_t err = S > 4096 ? launch_group_tokens_chunked(f.idx, S, f.E, f.counts, f.offsets, f.perm, f.active,
+                                                             f.n_active, f.chunks, stream)
+                               : launch_group_tokens(f.idx, S, f.k, f.E, f.counts, f.offsets, f.perm, f.active,
+                                                     f.n_active, stream, dev);
     if (err != cudaSuccess) return err;
     err = launch_pdl(tc_tile_prefix_kernel, dim3(1), dim3(1024), 0, stream, (const int32_t*)f.counts, f.E, nt,
                      f.tile_off);

@@ -124,7 +124,137 @@ __global__ void __launch_bounds__(kGroupThreads)
     }
 }
 
+// Multi-CTA grouping for many slots (same result as group_tokens_kernel): chunks of
+// kChunk slots; (1) a histogram per chunk, (2) one CTA turns them into counts,
+// offsets, the active list and each chunk's base position per expert, (3) each chunk
+// places its slots stably (match.any ranks inside a warp, per-warp counts across the
+// chunk's warps).
+constexpr int kChunk = 1024;
+
+__global__ void __launch_bounds__(kChunk) group_hist_kernel(const int32_t* __restrict__ idx, int S, int E,
+                                                            int32_t* __restrict__ chunk_counts) {
+    extern __shared__ int32_t hist[];  // [E]
+    for (int e = threadIdx.x; e < E; e += kChunk) hist[e] = 0;
+    __syncthreads();
+    pdl_wait();
+    pdl_launch_dependents();
+    const int s = blockIdx.x * kChunk + threadIdx.x;
+    if (s < S) {
+        const int e = idx[s];
+        if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kChunk) chunk_counts[(int64_t)blockIdx.x * E + e] = hist[e];
+}
+
+// One CTA of 1024 threads, thread e < E owns expert e.  chunk_counts is turned into the
+// chunks' base positions in place.
+__global__ void __launch_bounds__(kGroupThreads)
+    group_scan_kernel(int32_t* __restrict__ chunk_counts, int C, int E, int32_t* __restrict__ counts,
+                      int32_t* __restrict__ offsets, int32_t* __restrict__ active, int32_t* __restrict__ n_active) {
+    __shared__ int32_t scan_part[kGroupWarps];
+    __shared__ int32_t scan_flag[kGroupWarps];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int c_tot = 0;
+    if (tid < E)
+        for (int c = 0; c < C; ++c) c_tot += chunk_counts[(int64_t)c * E + tid];
+    const int f = c_tot > 0 ? 1 : 0;
+    int ci = c_tot, fi = f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int cn = __shfl_up_sync(kFullMask, ci, o);
+        const int fn = __shfl_up_sync(kFullMask, fi, o);
+        if (lane >= o) {
+            ci += cn;
+            fi += fn;
+        }
+    }
+    if (lane == 31) {
+        scan_part[warp] = ci;
+        scan_flag[warp] = fi;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int p = scan_part[lane], q = scan_flag[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int pn = __shfl_up_sync(kFullMask, p, o);
+            const int qn = __shfl_up_sync(kFullMask, q, o);
+            if (lane >= o) {
+                p += pn;
+                q += qn;
+            }
+        }
+        scan_part[lane] = p;
+        scan_flag[lane] = q;
+    }
+    __syncthreads();
+    const int excl_c = (warp > 0 ? scan_part[warp - 1] : 0) + ci - c_tot;
+    const int excl_f = (warp > 0 ? scan_flag[warp - 1] : 0) + fi - f;
+    if (tid < E) {
+        counts[tid] = c_tot;
+        offsets[tid] = excl_c;
+        if (active != nullptr && f) active[excl_f] = tid;
+        int base = excl_c;
+        for (int c = 0; c < C; ++c) {
+            const int n = chunk_counts[(int64_t)c * E + tid];
+            chunk_counts[(int64_t)c * E + tid] = base;
+            base += n;
+        }
+    }
+    if (tid == E - 1) {
+        offsets[E] = excl_c + c_tot;
+        if (n_active != nullptr) *n_active = excl_f + f;
+    }
+}
+
+__global__ void __launch_bounds__(kChunk) group_place_kernel(const int32_t* __restrict__ idx, int S, int E,
+                                                             const int32_t* __restrict__ chunk_base,
+                                                             int32_t* __restrict__ perm) {
+    extern __shared__ int32_t warp_cnt[];  // [kChunk / 32][E]
+    constexpr int kW = kChunk / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < kW * E; i += kChunk) warp_cnt[i] = 0;
+    __syncthreads();
+    pdl_wait();
+    pdl_launch_dependents();
+    const int s = blockIdx.x * kChunk + tid;
+    int e = s < S ? idx[s] : -1;
+    const bool valid = e >= 0 && e < E;
+    if (!valid) e = -1;
+    const unsigned peers = __match_any_sync(kFullMask, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (valid && rank == 0) warp_cnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    if (valid) {
+        int pre = 0;
+        for (int w2 = 0; w2 < warp; ++w2) pre += warp_cnt[w2 * E + e];
+        perm[chunk_base[(int64_t)blockIdx.x * E + e] + pre + rank] = s;
+    }
+}
+
 }  // namespace
+
+size_t group_chunked_bytes(int S, int E) { return sizeof(int32_t) * (size_t)((S + kChunk - 1) / kChunk) * E; }
+
+cudaError_t launch_group_tokens_chunked(const int32_t* idx, int S, int E, int32_t* counts, int32_t* offsets,
+                                        int32_t* perm, int32_t* active, int32_t* n_active, int32_t* chunk_scratch,
+                                        cudaStream_t stream) {
+    const int C = (S + kChunk - 1) / kChunk;
+    cudaError_t err = launch_pdl(group_hist_kernel, dim3(C), dim3(kChunk), sizeof(int32_t) * (size_t)E, stream, idx,
+                                 S, E, chunk_scratch);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(group_scan_kernel, dim3(1), dim3(kGroupThreads), 0, stream, chunk_scratch, C, E, counts, offsets,
+                     active, n_active);
+    if (err != cudaSuccess) return err;
+    const size_t smem = sizeof(int32_t) * (size_t)(kChunk / 32) * E;
+    err = ensure_dynamic_smem(group_place_kernel, smem);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(group_place_kernel, dim3(C), dim3(kChunk), smem, stream, idx, S, E,
+                      (const int32_t*)chunk_scratch, perm);
+}
 
 size_t group_tokens_smem_bytes(int E) { return sizeof(int32_t) * (size_t)E * (2 + kGroupWarps); }
 

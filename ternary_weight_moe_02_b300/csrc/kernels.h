@@ -36,6 +36,12 @@ cudaError_t launch_group_tokens(const int32_t* idx, int S, int k, int E, int32_t
                                 int32_t* offsets, int32_t* perm, int32_t* active,
                                 int32_t* n_active, cudaStream_t stream, const DeviceInfo& dev);
 size_t group_tokens_smem_bytes(int E);
+// The same grouping spread over chunks of 1024 slots (for many slots); chunk_scratch
+// holds group_chunked_bytes(S, E) bytes.
+size_t group_chunked_bytes(int S, int E);
+cudaError_t launch_group_tokens_chunked(const int32_t* idx, int S, int E, int32_t* counts, int32_t* offsets,
+                                        int32_t* perm, int32_t* active, int32_t* n_active, int32_t* chunk_scratch,
+                                        cudaStream_t stream);
 
 struct FfnArgs {
     const uint8_t* gate;
@@ -59,6 +65,7 @@ struct FfnArgs {
     int32_t* n_active; // [1]
     float* h;          // [T*k][I] (bf16 [T*k][I] on the tensor path)
     int32_t* tile_off; // [E+1] tensor path only
+    int32_t* chunks;   // grouping scratch of the tensor path
     uint16_t* xs;      // tensor path only: per tile, the tokens' x rows, chunk-major
     uint16_t* hs;      // tensor path only: per tile, the tokens' h rows, chunk-major
     float* ys;         // [T*k][H] tensor path only
@@ -67,7 +74,7 @@ struct FfnArgs {
 };
 
 struct FfnWorkspaceLayout {
-    size_t counts, offsets, perm, active, n_active, h, tile_off, xs, hs, ys, total;
+    size_t counts, offsets, perm, active, n_active, h, tile_off, chunks, xs, hs, ys, total;
     bool tensor;
 };
 FfnWorkspaceLayout ffn_workspace_layout(int T, int k, int E, int H, int I);

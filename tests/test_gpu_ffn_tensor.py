@@ -88,6 +88,23 @@ def test_tensor_path_several_token_tiles_per_expert():
     assert_ffn_close(y, _oracle(packed, x, idx, w32), "two token tiles")
 
 
+def test_tensor_path_many_slots_chunked_grouping():
+    """5600 slots (700 tokens, top-8, 16 experts): the grouping runs over six chunks of
+    1024 slots (the last one partial) and the tiles are 128 tokens wide."""
+    E, H, I, T, k = 16, 256, 128, 700, 8
+    packed, ex = _layer(E, H, I, seed=17)
+    x = synth.tokens(T, H, seed=17)
+    idx, w32 = _random_routing(T, E, k, seed=17)
+    idx[5, 3] = -1  # an invalid slot inside the first chunk
+    w32[5, 3] = 0.0
+    y1 = _run(ex, x, idx, w32)
+    y2 = _run(ex, x, idx, w32)
+    assert np.array_equal(y1, y2)
+    valid = (idx >= 0) & (idx < E)
+    y_ref = _oracle(packed, x, np.where(valid, idx, 0).astype(np.int32), np.where(valid, w32, 0))
+    assert_ffn_close(y1, y_ref, "chunked grouping")
+
+
 def test_tensor_path_is_the_automatic_choice_for_dense_loads():
     """Without the override, 96 tokens on 16 experts (48 slots per expert) take the
     tensor path; the result matches the oracle and repeats bit for bit."""
