@@ -34,9 +34,9 @@ N_TOKENS = 1000
 LAYERS = 64
 METRIC = "ternary MoE layer tokens/s (batch 1 & 64 decode); packed-weight HBM GB/s vs peak"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+# the batch-1 layer kernel and the device helpers it is built from
 LAYER_KERNEL_SOURCES = ("ternary_weight_moe_02_b300/csrc/layer_decode.cu",
-                        "ternary_weight_moe_02_b300/csrc/common.cuh",
-                        "ternary_weight_moe_02_b300/csrc/kernels.h")
+                        "ternary_weight_moe_02_b300/csrc/common.cuh")
 EXPERT_BYTES = 2 * I * ((H + 4) // 5) + H * ((I + 4) // 5) + 4 * (2 * I + H)  # 643,072
 
 
@@ -323,7 +323,8 @@ def run_gpu(args, world, rank, local):
     e2e_s = _max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
     e2e_value = world * n_e2e / e2e_s
 
-    secondary = run_secondary(maple, synth, layers, dev, stream) if args.secondary else None
+    legs = tuple(args.legs.split(",")) if args.legs else SECONDARY_LEGS
+    secondary = run_secondary(maple, synth, layers, dev, stream, legs) if args.secondary else None
 
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -356,7 +357,10 @@ def run_gpu(args, world, rank, local):
 
 # ------------------------------------------------------------- secondary workloads
 
-def run_secondary(maple, synth, layers, dev, stream):
+SECONDARY_LEGS = ("decode_b8", "decode_b64", "prefill_4096", "ternarize_pack")
+
+
+def run_secondary(maple, synth, layers, dev, stream, legs=SECONDARY_LEGS):
     """Other configurations of the same path, measured briefly (not the headline):
     decode batches over 24 stacked layers with a N(0,0.5) router bias, the 4096-token
     prefill with a Zipf(1.1) bias, and ternarize + pack throughput on whole layers."""
@@ -382,6 +386,8 @@ def run_secondary(maple, synth, layers, dev, stream):
         return a.elapsed_time(b) / 1e3 / (reps * n_steps)
 
     for T in (8, 64):
+        if f"decode_b{T}" not in legs:
+            continue
         xs = [synth.tokens(T, H, seed=100 + l, device=dev) for l in range(n_stack)]
         biases = [synth.bias_normal(E, seed=200 + l).to(dev) for l in range(n_stack)]
         logits = torch.empty((T, E), device=dev)
@@ -399,6 +405,8 @@ def run_secondary(maple, synth, layers, dev, stream):
         out[f"decode_b{T}"] = {"value": T / sec, "unit": "tokens/s", "ms_per_layer": sec * 1e3,
                                "layers": n_stack, "bias": "N(0, 0.5) per expert"}
 
+    if "prefill_4096" not in legs and "ternarize_pack" not in legs:
+        return out
     T = 4096
     x = synth.tokens(T, H, seed=300, device=dev)
     bias = synth.bias_zipf(E, seed=0, gamma=1.0).to(dev)
@@ -412,10 +420,13 @@ def run_secondary(maple, synth, layers, dev, stream):
     def prefill(i):
         ex, router = layers[i % n_stack]
         maple.maple_moe_layer(x, router, bias, ex, K_TOP, logits, idx, w, y, ws, stream=stream)
-    sec = timed_graph(prefill, 2, reps=2)
-    flops = 2 * 3 * I * H * T * K_TOP
-    out["prefill_4096"] = {"value": T / sec, "unit": "tokens/s", "ms_per_layer": sec * 1e3,
-                           "dense_equiv_tflops": flops / sec / 1e12, "bias": "Zipf(1.1) ranking"}
+    if "prefill_4096" in legs:
+        sec = timed_graph(prefill, 2, reps=2)
+        flops = 2 * 3 * I * H * T * K_TOP
+        out["prefill_4096"] = {"value": T / sec, "unit": "tokens/s", "ms_per_layer": sec * 1e3,
+                               "dense_equiv_tflops": flops / sec / 1e12, "bias": "Zipf(1.1) ranking"}
+    if "ternarize_pack" not in legs:
+        return out
 
     # ternarize + pack of whole layers (all 768 matrices of a layer per chunk)
     n_pack = 2
@@ -508,6 +519,8 @@ def main():
     ap.add_argument("--chunk", type=int, default=1000, help="steps per captured graph")
     ap.add_argument("--ref-tokens", type=int, default=4, help="oracle tokens per reference step")
     ap.add_argument("--cpu-tokens", type=int, default=40, help="oracle tokens for cpu_baseline")
+    ap.add_argument("--legs", default="", help="comma-separated subset of the secondary legs "
+                    + ",".join(SECONDARY_LEGS))
     ap.add_argument("--secondary", type=int, default=1,
                     help="also time decode b8/b64, the 4096-token prefill and ternarize+pack")
     args = ap.parse_args()
