@@ -203,9 +203,11 @@ MAPLE_API int maple_moe_layer(const uint16_t* x, const uint16_t* Wr, const float
  * a packaging of maple_moe_ffn, with the same arguments (minus ws / ws_bytes), the
  * same limits and the same result.
  * Scratch lives in one static 2 MiB device array per GPU, held from the library's
- * load until process exit.  A call whose maple_moe_ffn_workspace_size(T, k, ex)
- * exceeds 2 MiB (at Maple's shapes: T > 127 with k = 8, I = 512) returns
- * MAPLE_ERR_WORKSPACE and launches nothing.  The first call on a device looks up the
+ * load until process exit.  The call always takes the CUDA-core FFN kernels (the
+ * grouped tensor-core path's operand blocks would not fit), whose scratch is the
+ * [T*k][I] fp32 h array plus index arrays: a call needing more than 2 MiB (at
+ * Maple's shapes: T > 127 with k = 8, I = 512) returns MAPLE_ERR_WORKSPACE and
+ * launches nothing.  The first call on a device looks up the
  * array's device address (cudaGetSymbolAddress) and should come before any stream
  * capture.  The array is shared by every call and keeps the previous call's
  * contents (none of it needs clearing); calls that overlap on the GPU race on it,

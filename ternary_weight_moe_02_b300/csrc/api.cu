@@ -178,13 +178,25 @@ int maple_group_tokens(const int32_t* idx, int32_t T, int32_t k, int32_t E, int3
 }
 
 size_t maple_moe_ffn_workspace_size(int32_t T, int32_t k, const maple_experts* ex) {
-    if (!ex || T < 0 || k < 1 || ex->E < 1 || ex->H < 1 || ex->I < 1) return 0;
-    return maple::ffn_workspace_layout(T, k, ex->E, ex->H, ex->I).total;
+    return maple::moe_ffn_workspace_bytes(T, k, ex, true);
 }
 
 int maple_moe_ffn(const maple_experts* ex, const uint16_t* x, const int32_t* idx,
                   const float* w, int32_t T, int32_t k, float* y, void* ws, size_t ws_bytes,
                   void* stream) {
+    return maple::moe_ffn_entry(ex, x, idx, w, T, k, y, ws, ws_bytes, stream, true);
+}
+
+}  // extern "C"
+
+size_t maple::moe_ffn_workspace_bytes(int T, int k, const maple_experts* ex, bool allow_tensor) {
+    if (!ex || T < 0 || k < 1 || ex->E < 1 || ex->H < 1 || ex->I < 1) return 0;
+    const bool tensor = allow_tensor && maple::ffn_use_tensor(T, k, ex->E, ex->H, ex->I);
+    return maple::ffn_workspace_layout(T, k, ex->E, ex->H, ex->I, tensor).total;
+}
+
+int maple::moe_ffn_entry(const maple_experts* ex, const uint16_t* x, const int32_t* idx, const float* w, int T,
+                         int k, float* y, void* ws, size_t ws_bytes, void* stream, bool allow_tensor) {
     if (!ex) return fail(MAPLE_ERR_INVALID_ARG, "moe_ffn: null experts");
     const int E = ex->E, H = ex->H, I = ex->I;
     if (T < 0 || k < 1 || E < 1 || H < 1 || I < 1) return fail(MAPLE_ERR_INVALID_ARG, "moe_ffn: T=%d k=%d E=%d H=%d I=%d", T, k, E, H, I);
@@ -198,7 +210,8 @@ int maple_moe_ffn(const maple_experts* ex, const uint16_t* x, const int32_t* idx
         !aligned(ex->s_up, 16) || !aligned(ex->s_down, 16) || !aligned(x, 16) || !aligned(ws, 16))
         return fail(MAPLE_ERR_MISALIGNED, "moe_ffn: packed weights, scales, x and ws need 16-byte alignment");
     if (!aligned(idx, 4) || !aligned(w, 4) || !aligned(y, 4)) return fail(MAPLE_ERR_MISALIGNED, "moe_ffn: idx, w, y need 4-byte alignment");
-    const maple::FfnWorkspaceLayout L = maple::ffn_workspace_layout(T, k, E, H, I);
+    const bool tensor = allow_tensor && maple::ffn_use_tensor(T, k, E, H, I);
+    const maple::FfnWorkspaceLayout L = maple::ffn_workspace_layout(T, k, E, H, I, tensor);
     if (!ws || ws_bytes < L.total) return fail(MAPLE_ERR_WORKSPACE, "moe_ffn: workspace %zu bytes < %zu needed", ws_bytes, L.total);
     maple::DeviceInfo dev;
     if (int st = get_device(&dev, "moe_ffn")) return st;
@@ -228,14 +241,19 @@ int maple_moe_ffn(const maple_experts* ex, const uint16_t* x, const int32_t* idx
     a.h = reinterpret_cast<float*>(base + L.h);
     a.tile_off = reinterpret_cast<int32_t*>(base + L.tile_off);
     a.chunks = reinterpret_cast<int32_t*>(base + L.chunks);
-    a.xs = reinterpret_cast<uint16_t*>(base + L.xs);
-    a.hs = reinterpret_cast<uint16_t*>(base + L.hs);
+    a.xs = reinterpret_cast<uint8_t*>(base + L.xs);
+    a.hs = reinterpret_cast<uint8_t*>(base + L.hs);
+    a.xscale = reinterpret_cast<float*>(base + L.xscale);
+    a.hscale = reinterpret_cast<float*>(base + L.hscale);
     a.ys = reinterpret_cast<float*>(base + L.ys);
     a.status = dev.status;
+    a.tensor = tensor ? 1 : 0;
     cudaError_t err = maple::launch_moe_ffn(a, (cudaStream_t)stream, dev);
     if (err != cudaSuccess) return cuda_fail(err, "moe_ffn launch");
     return ok();
 }
+
+extern "C" {
 
 // Workspace of maple_moe_layer: 256 bytes of barrier counters, then the FFN workspace.
 size_t maple_moe_layer_workspace_size(int32_t T, int32_t k, const maple_experts* ex) {
@@ -266,7 +284,7 @@ int maple_moe_layer(const uint16_t* x, const uint16_t* Wr, const float* bias,
     if (int st = get_device(&dev, "moe_layer")) return st;
     char* base = static_cast<char*>(ws);
     if (T == 1 && maple::layer_b1_supported(H, I, E, k, dev)) {
-        const maple::FfnWorkspaceLayout L = maple::ffn_workspace_layout(T, k, E, H, I);
+        const maple::FfnWorkspaceLayout L = maple::ffn_workspace_layout(T, k, E, H, I, false);
         maple::LayerLaunch p;
         p.x = x;
         p.Wr = Wr;

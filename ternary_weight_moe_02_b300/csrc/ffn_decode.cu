@@ -490,7 +490,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 }  // namespace
 
-FfnWorkspaceLayout ffn_workspace_layout(int T, int k, int E, int H, int I) {
+FfnWorkspaceLayout ffn_workspace_layout(int T, int k, int E, int H, int I, bool tensor) {
     const size_t S = (size_t)T * (size_t)k;
     FfnWorkspaceLayout L{};
     size_t o = 0;
@@ -506,16 +506,20 @@ FfnWorkspaceLayout ffn_workspace_layout(int T, int k, int E, int H, int I) {
     o = align_up(o + 4, 256);
     L.h = o;
     o = align_up(o + 4 * S * (size_t)I, 256);
-    L.tensor = ffn_use_tensor(T, k, E, H, I);
-    L.tile_off = L.chunks = L.xs = L.hs = L.ys = o;
+    L.tensor = tensor;
+    L.tile_off = L.chunks = L.xs = L.hs = L.xscale = L.hscale = L.ys = o;
     if (L.tensor) {
-        o = align_up(o + 4 * ((size_t)E + 1), 256);
+        o = align_up(o + 4 * ((size_t)E + 1 + (size_t)ffn_tensor_max_tiles((int)S, E)), 256);
         L.chunks = o;
         o = align_up(o + group_chunked_bytes((int)S, E), 256);
         L.xs = o;
         o = align_up(o + ffn_tensor_x_bytes((int)S, E, H), 256);
         L.hs = o;
         o = align_up(o + ffn_tensor_h_bytes((int)S, E, I), 256);
+        L.xscale = o;
+        o = align_up(o + ffn_tensor_scale_bytes((int)S, E), 256);
+        L.hscale = o;
+        o = align_up(o + ffn_tensor_scale_bytes((int)S, E), 256);
         L.ys = o;
         o = align_up(o + 4 * S * (size_t)H, 256);
     }
@@ -527,7 +531,7 @@ cudaError_t launch_moe_ffn(const FfnArgs& args, cudaStream_t stream, const Devic
     FfnArgs a = args;
     const int64_t down_bytes = (int64_t)a.H * ((a.I + 4) / 5);
     a.prefetch_down = (down_bytes % 16 == 0 && a.H % 4 == 0) ? 1 : 0;
-    if (ffn_use_tensor(a.T, a.k, a.E, a.H, a.I)) return launch_moe_ffn_tensor(a, stream, dev);
+    if (a.tensor) return launch_moe_ffn_tensor(a, stream, dev);
     const int S = a.T * a.k;
     const int slot_mode = a.T == 1 ? 1 : 0;
     if (!slot_mode) {

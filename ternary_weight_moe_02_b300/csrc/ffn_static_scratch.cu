@@ -11,8 +11,10 @@
 // In host code the array's name is only a host-side stand-in, not a device address,
 // so the device address is looked up with cudaGetSymbolAddress, once per device,
 // with that device current, on the first call made on that device; that first call
-// should therefore come before any stream capture.  After the look-up every call
-// forwards to maple_moe_ffn with the array as its workspace.  Nothing in the array
+// should therefore come before any stream capture.  After the look-up every call runs
+// maple_moe_ffn's checks and kernels with the array as its workspace, always on the
+// CUDA-core path: the grouped tensor-core path needs per-tile operand blocks far
+// larger than the array.  Nothing in the array
 // needs to start at zero: every kernel writes what it later reads, so the contents
 // left by the previous call are simply overwritten.  All calls share the one array,
 // so calls that overlap on the GPU (other streams, other host threads) race on it
@@ -43,8 +45,8 @@ extern "C" MAPLE_API int maple_moe_ffn_static_scratch(const maple_experts* ex, c
     // Argument checks are maple_moe_ffn's own; a call it rejects (or an empty one,
     // T == 0) is forwarded without scratch, so it reports exactly as it would.
     if (!ex || T <= 0 || k < 1 || ex->E < 1 || ex->I < 1)
-        return maple_moe_ffn(ex, x, idx, w, T, k, y, nullptr, 0, stream);
-    const size_t need = maple_moe_ffn_workspace_size(T, k, ex);
+        return maple::moe_ffn_entry(ex, x, idx, w, T, k, y, nullptr, 0, stream, false);
+    const size_t need = maple::moe_ffn_workspace_bytes(T, k, ex, false);
     if (need > kStaticScratchBytes)
         return maple::report_error(MAPLE_ERR_WORKSPACE,
                                    "moe_ffn_static_scratch: T=%d k=%d I=%d needs %zu bytes of "
@@ -74,5 +76,5 @@ extern "C" MAPLE_API int maple_moe_ffn_static_scratch(const maple_experts* ex, c
         }
         scratch = g_scratch_addr[dev];
     }
-    return maple_moe_ffn(ex, x, idx, w, T, k, y, scratch, kStaticScratchBytes, stream);
+    return maple::moe_ffn_entry(ex, x, idx, w, T, k, y, scratch, kStaticScratchBytes, stream, false);
 }

@@ -4,31 +4,39 @@
 // sections "The claim, verified from the bytes" (one scale per output row, trits
 // -1/0/+1) and "The shipped code does no quantization" (the expert body
 // down(act(clamp(gate x, max=7)) * clamp(up x, -7, 7))).  The pages give no kernel for
-// many tokens per expert; a trit is exact in bf16, so the sums can run on the tensor
-// cores with fp32 accumulation.
+// many tokens per expert.  Here the sums run on the tensor cores as fp8 (e4m3) MMAs
+// with fp32 accumulation, without rounding the operands:
+//   * a trit -1 / 0 / +1 is exact in e4m3;
+//   * a bf16 row (of x, or of h) whose largest magnitude lies in [2^e, 2^(e+1)) gets the
+//     power-of-two scale s = 2^(e - 7); each value v is split into two e4m3 values with
+//     v = s (hi + lo): hi is v / s rounded to e4m3 (four significant bits) and lo the
+//     rest, also an e4m3 value.  Both are exact whenever |v / s| >= 2^-2 (bf16 carries
+//     eight significant bits); smaller values keep their bits down to s 2^-9;
+//   * the MMA multiplies the trits by the hi and by the lo rows as separate columns of
+//     one product, and the epilogue adds the two accumulators and applies s.
 //
 // Per expert e with n_e routed tokens (slots grouped by expert, tiles of NT tokens;
 // NT = 128 for prefill-sized calls, 16 for decode batches):
-//   gate/up CTA: D[128 x NT] = A . X^T, A = 64 gate rows and the same 64 up rows of e,
-//     X = the tokens' bf16 activations (gathered once per call into expert order,
-//     loaded by TMA); fp32 accumulation in tensor memory.  Epilogue:
-//     h = silu(min(s_g g, clamp)) * clamp(s_u u, -clamp, clamp), rounded to bf16, stored
-//     per slot in expert order.
-//   down CTA: D[128 x NT] = A_down . H^T over I; epilogue w_slot * s_d * D stored per
+//   split x: each tile's token rows of x into hi/lo rows and scales;
+//   gate/up CTA: D[128 x 2NT] = A . B^T, A = 64 gate rows and the same 64 up rows of e,
+//     B = the tile's hi rows then its lo rows; epilogue
+//     h = silu(min(s_g g, clamp)) * clamp(s_u u, -clamp, clamp), rounded to bf16 and
+//     stored by grouped position;
+//   split h: each tile's h rows into hi/lo rows and scales, as for x;
+//   down CTA: D[128 x 2NT] = A_down . B^T over I; epilogue w_slot * s_d * s_h * D per
 //     slot (fp32); a combine kernel adds each token's k slots in order 0..k-1.
 //
 // A is decoded from the packed bytes straight into tensor memory: thread r of lane
-// quarter r / 32 owns weight row r (TMEM lane r) and writes its K values as bf16 +-0.5
-// or 0 (half the trit, exact; the epilogues scale by 2 s), two per 32-bit column, with
-// tcgen05.st; the MMA reads A from tensor memory.  B (tokens) sits in shared memory
-// K-major without swizzle: element (n, k) of a stage at (k / 8) * (NT * 16) + n * 16 +
-// (k % 8) * 2.  The gather kernel (for x) and the gate/up epilogue (for h) store each
-// tile's rows in global memory in that same order (chunk-major, [tile][K/8][NT][8]),
-// so a stage is one contiguous block loaded by one 1-D bulk copy.  K tiles hold 80
-// values (16 packed bytes per row).
-// Eight producer warps fill a ring of four stages; one thread issues five tcgen05.mma
-// (K = 16 each) per stage and commits them to the stage's "empty" mbarrier, which the
-// producers wait for before refilling the stage.  All waits are bounded.
+// quarter r / 32 owns weight row r (TMEM lane r) and writes its K values as e4m3, four
+// per 32-bit column (K order from the low byte), with tcgen05.st; the MMA reads A from
+// tensor memory.  B sits in shared memory K-major without swizzle: byte (n, k) of a
+// stage at (k / 16) * (2NT * 16) + n * 16 + k % 16.  The split kernels store each
+// tile's rows in global memory in that order ([K / 16][2NT][16] bytes), so a K tile's
+// B stage is one contiguous block loaded by one 1-D bulk copy.  K tiles hold 160 values
+// (32 packed bytes per row).  Eight producer warps fill a ring of four stages; one
+// thread issues five tcgen05.mma.kind::f8f6f4 (K = 32 each) per stage and commits them
+// to the stage's "empty" mbarrier, which the producers wait for before refilling the
+// stage.  All waits are bounded.
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdlib.h>
@@ -42,25 +50,25 @@ namespace maple {
 namespace {
 
 constexpr int kRows = 128;                 // MMA M: weight rows per CTA
-constexpr int kKTile = 80;                 // K values per stage (16 packed bytes)
-constexpr int kChunks = kKTile / 8;        // 16-byte core-matrix columns per B stage
+constexpr int kKTile = 160;                // K values per stage (32 packed bytes)
+constexpr int kChunks = kKTile / 16;       // 16-byte core-matrix columns per B stage
 constexpr int kMaxStages = 4;
 constexpr int kAStride = 48;               // TMEM column stride between A stages (40 used)
-constexpr int kLutReps = 4;                // copies of the decode table, by lane & 3
-constexpr int kLutBytes = 256 * kLutReps * 8;  // 8 KB
+constexpr int kLutReps = 16;               // copies of the decode table, by lane & 15
+constexpr int kLutBytes = 256 * kLutReps * 8;  // 32 KB
 constexpr int kProducerWarps = 8;          // decode A, load B; warp 8 issues the MMAs
 constexpr int kThreads = (kProducerWarps + 1) * 32;
 
 template <int NT>
 struct TileCfg {
-    static constexpr int kStages = 4;                                    // ring depth
-    static constexpr int kStageB = kChunks * NT * 16;                    // bytes of a B stage
-    static constexpr int kABase = NT < 32 ? 32 : NT;                     // first A column
+    static constexpr int kN = 2 * NT;                                    // MMA N: hi and lo rows
+    static constexpr int kStageB = kChunks * kN * 16;                    // bytes of a B stage
+    static constexpr int kStages = NT >= 128 ? 3 : 4;                    // ring depth (shared memory)
+    static constexpr int kABase = kN < 32 ? 32 : kN;                     // first A column
     static constexpr int kUsedCols = kABase + kStages * kAStride;
     static constexpr int kTmemCols = kUsedCols <= 256 ? 256 : 512;       // power of two
-    // instruction descriptor: D fp32, A and B bf16, both K-major, N = NT, M = 128
-    static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NT >> 3) << 17) |
-                                       ((uint32_t)(kRows >> 4) << 24);
+    // instruction descriptor: D fp32, A and B e4m3 (format 0), both K-major, N, M = 128
+    static constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
 };
 
 // ----------------------------------------------------------------- tcgen05 helpers
@@ -86,12 +94,12 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[tmem] . B[smem descriptor]
-__device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                           uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] . B[smem descriptor], e4m3 x e4m3 -> fp32
+__device__ __forceinline__ void mma_f8_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
     asm volatile(
         "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
         "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -117,64 +125,151 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t* w) {
                  : "memory");
 }
 
-// 8 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
-    uint32_t r[8];
+// 8 or 16 consecutive 32-bit columns of this thread's TMEM lane; complete after
+// tmem_wait_ld
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                  : "r"(taddr)
                  : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// ----------------------------------------------------------------- e4m3 split
+
+// Two floats to two e4m3, rounded to nearest even with saturation; byte 0 from a.
+__device__ __forceinline__ uint32_t e4m3x2_from(float a, float b) {
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(b), "f"(a));
+    return d;
+}
+
+// The two e4m3 values in bytes 0 and 1 of p, exactly, as floats.
+__device__ __forceinline__ void e4m3x2_to(uint32_t p, float& a, float& b) {
+    asm("{\n.reg .b32 h2;\n.reg .b16 lo, hi;\n"
+        "cvt.rn.f16x2.e4m3x2 h2, %2;\n"
+        "mov.b32 {lo, hi}, h2;\n"
+        "cvt.f32.f16 %0, lo;\n"
+        "cvt.f32.f16 %1, hi;\n}\n"
+        : "=f"(a), "=f"(b)
+        : "h"((uint16_t)p));
+}
+
+// The split scale 2^(e - 7) of a row whose largest magnitude m lies in [2^e, 2^(e+1))
+// (1 for an all-zero row; e held to [-100, 127] so that 1 / s stays finite).
+__device__ __forceinline__ float split_scale(float m) {
+    if (!(m > 0.f)) return 1.f;
+    int e = (int)((__float_as_uint(m) >> 23) & 0xFF) - 127;
+    e = e < -100 ? -100 : (e > 127 ? 127 : e);
+    return ldexpf(1.f, e - 7);
+}
+
+// Eight values (already divided by the row's scale) into eight hi and eight lo bytes.
+__device__ __forceinline__ void split8(const float* v, uint2& hi, uint2& lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        h[p] = e4m3x2_from(v[2 * p], v[2 * p + 1]);
+        float b0, b1;
+        e4m3x2_to(h[p], b0, b1);
+        l[p] = e4m3x2_from(v[2 * p] - b0, v[2 * p + 1] - b1);
+    }
+    hi = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+    lo = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+}
+
 // ----------------------------------------------------------------- decode table
 
-// For each code, the high bytes of the five bf16 values +-0.5 / 0 of its trits (0xBF
-// for -1, 0x00 for 0, 0x3F for +1; the low byte of those bf16 values is zero), bytes
-// 5-7 zero; the invalid codes 243..255 give five zeros.  kLutReps copies interleaved by
-// entry ([code][copy]) so that the 8-byte loads of a half-warp spread over more banks.
-__device__ __forceinline__ void build_half_lut(uint2* lut, int tid, int nthreads) {
-    for (int i = tid; i < 256 * kLutReps; i += nthreads) {
-        const int c = i / kLutReps;
+// For each code, the e4m3 values of its five trits (0xB8 = -1, 0x00 = 0, 0x38 = +1) in
+// bytes 0-4, bytes 5-7 zero; the invalid codes 243..255 give five zeros.  kLutReps
+// copies interleaved by entry ([code][copy], 8 bytes): copy lane & 15 of a warp's 32
+// loads falls in bank pair 2 (lane & 15), so a load takes the minimum two wavefronts.
+// Built at compile time; every CTA bulk-copies it into shared memory.
+struct F8LutImage {
+    uint32_t word[256 * kLutReps * 2];
+};
+
+constexpr F8LutImage make_f8_lut_image() {
+    F8LutImage t{};
+    for (int c = 0; c < 256; ++c) {
         uint32_t b[5] = {0u, 0u, 0u, 0u, 0u};
         if (c < 243) {
             int code = c;
-#pragma unroll
-            for (int t = 0; t < 5; ++t) {
+            for (int i = 0; i < 5; ++i) {
                 const int d = code % 3;
                 code /= 3;
-                b[t] = d == 0 ? 0xBFu : (d == 2 ? 0x3Fu : 0u);
+                b[i] = d == 0 ? 0xB8u : (d == 2 ? 0x38u : 0u);
             }
         }
-        lut[i] = make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4]);
+        for (int r = 0; r < kLutReps; ++r) {
+            t.word[2 * (c * kLutReps + r)] = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+            t.word[2 * (c * kLutReps + r) + 1] = b[4];
+        }
+    }
+    return t;
+}
+
+__device__ __align__(16) const F8LutImage g_f8_lut_image = make_f8_lut_image();
+static_assert(sizeof(F8LutImage) == kLutBytes, "table image size");
+
+// Bytes [A, A + 16) of the packed rows (base 16-byte aligned) as four words, from five
+// aligned word loads and funnel shifts.  Reads up to 3 bytes past A + 16.
+__device__ __forceinline__ void load_bytes16(const uint8_t* base, uint32_t A, uint32_t* a) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(base + (A & ~3u));
+    const uint32_t sh = (A & 3u) * 8;
+    uint32_t t[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) t[i] = w[i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = __funnelshift_r(t[i], t[i + 1], sh);
+}
+
+// Decodes bytes [b0, b0 + 16) of the row at byte offset row_off of the packed rows
+// (bytes at or past rb read as the all-zero code 121) into 20 words of four e4m3 each,
+// in K order: every four codes (twenty values) become five words by byte permutes of
+// their table entries.
+template <bool kTail>
+__device__ __forceinline__ void decode_half_tile_impl(const uint8_t* packed, uint32_t row_off, int rb, int b0,
+                                                      const uint2* lut_rep, uint32_t* words) {
+    uint32_t a[4];
+    load_bytes16(packed, row_off + (uint32_t)b0, a);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        uint2 en[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t c = (a[g] >> (8 * i)) & 0xFFu;
+            if (kTail && b0 + 4 * g + i >= rb) c = 121u;
+            en[i] = lut_rep[c * kLutReps];
+        }
+        words[5 * g + 0] = en[0].x;                                // values 0-3 of code 0
+        words[5 * g + 1] = __byte_perm(en[0].y, en[1].x, 0x6540);  // 0.4, 1.0, 1.1, 1.2
+        words[5 * g + 2] = __byte_perm(__byte_perm(en[1].x, en[1].y, 0x0043), en[2].x, 0x5410);  // 1.3, 1.4, 2.0, 2.1
+        words[5 * g + 3] = __byte_perm(__byte_perm(en[2].x, en[2].y, 0x0432), en[3].x, 0x4210);  // 2.2-2.4, 3.0
+        words[5 * g + 4] = __byte_perm(en[3].x, en[3].y, 0x4321);  // 3.1-3.4
     }
 }
 
-// Decodes packed bytes [16 kt + 8 h, +8) of one row (bytes at or past rb read as the
-// all-zero code 121) into 20 words of two bf16 each (K order).  Two bytes (ten values)
-// become five words by byte permutes of their two table entries.
-__device__ __forceinline__ void decode_half_tile(const uint8_t* row, int rb, int kt, int h, const uint2* lut,
-                                                 int rep, uint32_t* words) {
-    const int b0 = 16 * kt + 8 * h;
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const int ba = b0 + 2 * p, bb = ba + 1;
-        const int ca = ba < rb ? row[ba] : 121;
-        const int cb = bb < rb ? row[bb] : 121;
-        const uint2 ea = lut[ca * kLutReps + rep];
-        const uint2 eb = lut[cb * kLutReps + rep];
-        words[5 * p + 0] = __byte_perm(ea.x, ea.y, 0x1505);  // 0, a0, 0, a1
-        words[5 * p + 1] = __byte_perm(ea.x, ea.y, 0x3525);  // 0, a2, 0, a3
-        words[5 * p + 2] = __byte_perm(ea.y, eb.x, 0x4101);  // 0, a4, 0, b0
-        words[5 * p + 3] = __byte_perm(eb.x, eb.y, 0x2515);  // 0, b1, 0, b2
-        words[5 * p + 4] = __byte_perm(eb.x, eb.y, 0x4535);  // 0, b3, 0, b4
-    }
+// Bytes [32 kt + 16 h, +16) of a row: the masked variant only for the row's last tile.
+__device__ __forceinline__ void decode_half_tile(const uint8_t* packed, uint32_t row_off, int rb, int kt, int h,
+                                                 const uint2* lut_rep, uint32_t* words) {
+    const int b0 = 32 * kt + 16 * h;
+    if (b0 + 16 <= rb)
+        decode_half_tile_impl<false>(packed, row_off, rb, b0, lut_rep, words);
+    else
+        decode_half_tile_impl<true>(packed, row_off, rb, b0, lut_rep, words);
 }
 
 struct TcArgs {
@@ -193,8 +288,12 @@ struct TcArgs {
     const int32_t* offsets;
     const int32_t* perm;
     const int32_t* tile_off;  // [E + 1] prefix of ceil(counts / NT)
-    uint16_t* xs;             // [tile][H / 8][NT][8] bf16: each tile's token rows
-    uint16_t* hs;             // [tile][I / 8][NT][8] bf16: each tile's h rows
+    const int32_t* tile_e;    // [tiles] expert of each tile
+    uint8_t* xs;              // [tile][H / 16][2NT][16] e4m3: each tile's x rows, hi then lo
+    uint8_t* hs;              // [tile][I / 16][2NT][16] e4m3: each tile's h rows, hi then lo
+    float* xscale;            // [tile][NT] split scales of the x rows
+    float* hscale;            // [tile][NT] split scales of the h rows
+    uint16_t* hrow;           // [T k][I] bf16 h by grouped position
     float* ys;                // [T k][H] fp32, per original slot
     float* y;                 // [T][H]
     int T;
@@ -218,15 +317,7 @@ __host__ __device__ constexpr size_t tc_smem_bytes(int row_bytes) {
 template <int NT>
 __device__ __forceinline__ bool tc_tile(const TcArgs& a, int tile, int& e, int& n0, int& nv, int& pos0) {
     if (tile >= __ldcg(a.tile_off + a.E)) return false;
-    int lo = 0, hi = a.E - 1;  // largest e with tile_off[e] <= tile
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldcg(a.tile_off + mid) <= tile)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    e = lo;
+    e = __ldcg(a.tile_e + tile);
     n0 = (tile - __ldcg(a.tile_off + e)) * NT;
     const int left = __ldcg(a.counts + e) - n0;
     nv = left < NT ? left : NT;
@@ -235,8 +326,8 @@ __device__ __forceinline__ bool tc_tile(const TcArgs& a, int tile, int& e, int& 
 }
 
 // Barriers of a grouped CTA: full[s] (one arrival per producer thread once its A words
-// are in tensor memory), bfull[s] (the B tile's TMA bytes), empty[s] (MMA commit),
-// done (commit after the last MMA), packed (bulk copy of the CTA's packed rows).
+// are in tensor memory), bfull[s] (the B stage's bulk-copy bytes), empty[s] (MMA
+// commit), done (commit after the last MMA), packed (bulk copy of the packed rows).
 struct TcBars {
     uint64_t full[kMaxStages];
     uint64_t bfull[kMaxStages];
@@ -246,47 +337,54 @@ struct TcBars {
 };
 
 // Warp-specialised main loop.  Warp w < 8 produces: its thread owns row 32 (w & 3) +
-// lane (the warp's TMEM lane quarter) and decodes half w >> 2 of that row's 16 bytes of
-// each K tile into A stage s (tensor memory), then arrives on full[s]; thread 0 also
-// copies the stage's B block (this K tile's chunks of the tile's operand block bsrc,
-// fewer at the K tail) with one bulk copy onto bfull[s].
-// Warp 8 lane 0 waits for both, issues the stage's five MMAs and commits empty[s]; its
-// last commit goes to done.  Returns false if a bounded wait gave up.
+// lane (the warp's TMEM lane quarter) and decodes half w >> 2 of that row's 32 bytes of
+// each K tile into A stage s (tensor memory), decoding the next K tile while the
+// current one's stores complete, then arrives on full[s]; thread 0 also copies the
+// stage's B block (this K tile's chunks of the tile's operand block bsrc, fewer at the
+// K tail) with one bulk copy onto bfull[s], the first S of them up front.  Warp 8 lane 0 waits for both, issues the
+// stage's five MMAs and commits empty[s]; its last commit goes to done.  Returns false
+// if a bounded wait gave up.
 template <int NT>
-__device__ bool tc_mainloop(unsigned char* smem, const uint8_t* packed, int rb, int Kdim, const uint16_t* bsrc,
+__device__ bool tc_mainloop(unsigned char* smem, const uint8_t* packed, int rb, int Kdim, const uint8_t* bsrc,
                             uint32_t tmem, TcBars& bars, int* status) {
     using Cfg = TileCfg<NT>;
     constexpr int S = Cfg::kStages;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint2* lut = reinterpret_cast<const uint2*>(smem);
+    const uint2* lut_rep = reinterpret_cast<const uint2*>(smem) + (lane & (kLutReps - 1));
     unsigned char* stages = smem + tc_stage_offset(rb);
     const int KT = (Kdim + kKTile - 1) / kKTile;
     bool ok = true;
-    int issued = 0;  // B tiles thread 0 has loaded
+    int issued = 0;  // B stages thread 0 has loaded
+    // B stage j: this K tile's chunks of the operand block (fewer at the K tail)
+    auto load_b = [&](int j) {
+        const int s = j % S;
+        const int left = Kdim / 16 - j * kChunks;
+        const uint32_t bytes = (uint32_t)((left < kChunks ? left : kChunks) * Cfg::kN * 16);
+        mbar_arrive_expect_tx(&bars.bfull[s], bytes);
+        bulk_copy_g2s(stages + s * Cfg::kStageB, bsrc + (size_t)j * Cfg::kStageB, bytes, &bars.bfull[s]);
+        issued = j + 1;
+    };
     if (warp < kProducerWarps) {
         const int q = warp & 3, h = warp >> 2, r = 32 * q + lane;
-        const uint8_t* my_row = packed + r * rb;
+        const uint32_t row_off = (uint32_t)(r * rb);
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
-        // tile j + 1 is decoded while tile j's tensor-memory stores complete
+        if (tid == 0)
+            for (int j = 0; j < S && j < KT; ++j) load_b(j);  // every stage starts free
         uint32_t cur[20], nxt[20];
-        decode_half_tile(my_row, rb, 0, h, lut, lane & (kLutReps - 1), cur);
+        decode_half_tile(packed, row_off, rb, 0, h, lut_rep, cur);
         for (int j = 0; j < KT && ok; ++j) {
             const int s = j % S;
-            if (j >= S && !mbar_wait_bounded(&bars.empty[s], (uint32_t)(((j - S) / S) & 1), status)) {
-                ok = false;
-                break;
-            }
-            if (tid == 0) {
-                const int left = Kdim / 8 - j * kChunks;
-                const uint32_t bytes = (uint32_t)((left < kChunks ? left : kChunks) * NT * 16);
-                mbar_arrive_expect_tx(&bars.bfull[s], bytes);
-                bulk_copy_g2s(stages + s * Cfg::kStageB, bsrc + (size_t)j * kChunks * NT * 8, bytes, &bars.bfull[s]);
-                issued = j + 1;
+            if (j >= S) {
+                if (!mbar_wait_bounded(&bars.empty[s], (uint32_t)(((j - S) / S) & 1), status)) {
+                    ok = false;
+                    break;
+                }
+                if (tid == 0) load_b(j);
             }
             const uint32_t col = (uint32_t)(Cfg::kABase + s * kAStride + 20 * h);
             tmem_st16(lane_base + col, cur);
             tmem_st4(lane_base + col + 16, cur + 16);
-            if (j + 1 < KT) decode_half_tile(my_row, rb, j + 1, h, lut, lane & (kLutReps - 1), nxt);
+            if (j + 1 < KT) decode_half_tile(packed, row_off, rb, j + 1, h, lut_rep, nxt);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             mbar_arrive(&bars.full[s]);
@@ -305,9 +403,9 @@ __device__ bool tc_mainloop(unsigned char* smem, const uint8_t* packed, int rb, 
             const uint32_t a0 = tmem + (uint32_t)(Cfg::kABase + s * kAStride);
             const uint32_t b0 = smem_addr(stages + s * Cfg::kStageB);
 #pragma unroll
-            for (int qk = 0; qk < kKTile / 16; ++qk) {
-                const uint64_t bd = smem_desc(b0 + qk * 2 * (NT * 16), NT * 16, 128);
-                mma_tmem_a(tmem, a0 + 8 * qk, bd, Cfg::kIdesc, (j | qk) != 0 ? 1u : 0u);
+            for (int qk = 0; qk < kKTile / 32; ++qk) {
+                const uint64_t bd = smem_desc(b0 + qk * 2 * (Cfg::kN * 16), Cfg::kN * 16, 128);
+                mma_f8_tmem_a(tmem, a0 + 8 * qk, bd, Cfg::kIdesc, (j | qk) != 0 ? 1u : 0u);
             }
             mma_commit(j == KT - 1 ? &bars.done : &bars.empty[s]);
         }
@@ -324,19 +422,34 @@ __device__ bool tc_mainloop(unsigned char* smem, const uint8_t* packed, int rb, 
     return !__syncthreads_or(!ok);
 }
 
-// CTA prologue shared by both stages: decode table, zeroed B stages, barriers, TMEM
-// (warp 8), and the bulk copy of the CTA's packed rows (nrows_copy rows of rb bytes
-// from src0 and, when src1 is set, as many from src1).
-__device__ bool tc_prologue(unsigned char* smem, TcBars& bars, uint32_t* tmem_slot, uint32_t tmem_cols,
-                            const uint8_t* src0, const uint8_t* src1, int nrows_copy, int rb, size_t stage_bytes,
-                            int* status) {
+// CTA prologue shared by both stages: one mbarrier for the bulk copies of the decode
+// table and of the CTA's packed rows (nrows_copy rows of rb bytes from src0 and, when
+// src1 is set, as many from src1), issued first; then, while they land, the other
+// barriers, TMEM (warp 8), and zeros for the B chunks that no copy fills before the
+// MMA reads them: the K tail of the last K tile when that tile is its stage's first
+// use (a stage used before holds finite values of the same token rows, which meet zero
+// A values there).
+template <int NT>
+__device__ bool tc_prologue(unsigned char* smem, TcBars& bars, uint32_t* tmem_slot, const uint8_t* src0,
+                            const uint8_t* src1, int nrows_copy, int rb, int Kdim, int* status) {
+    using Cfg = TileCfg<NT>;
     const int tid = threadIdx.x;
-    build_half_lut(reinterpret_cast<uint2*>(smem), tid, blockDim.x);
-    // zero the B stages: the K tail's chunks are never copied, and the MMA multiplies
-    // them by zero A values, which must not meet NaN bit patterns
-    uint4* st4 = reinterpret_cast<uint4*>(smem + tc_stage_offset(rb));
-    for (size_t i = tid; i < stage_bytes / 16; i += blockDim.x) st4[i] = make_uint4(0u, 0u, 0u, 0u);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (tid == 0) {
+        mbar_init(&bars.packed, 1);
+        const uint32_t bytes = (uint32_t)(nrows_copy * rb);
+        mbar_arrive_expect_tx(&bars.packed, (src1 ? 2 * bytes : bytes) + (uint32_t)kLutBytes);
+        bulk_copy_g2s(smem + tc_packed_offset(), src0, bytes, &bars.packed);
+        if (src1) bulk_copy_g2s(smem + tc_packed_offset() + bytes, src1, bytes, &bars.packed);
+        bulk_copy_g2s(smem, &g_f8_lut_image, (uint32_t)kLutBytes, &bars.packed);
+    }
+    const int KT = (Kdim + kKTile - 1) / kKTile;
+    const int left = Kdim / 16 - (KT - 1) * kChunks;  // chunks of the last K tile
+    if (KT - 1 < Cfg::kStages && left < kChunks) {
+        uint4* z = reinterpret_cast<uint4*>(smem + tc_stage_offset(rb) + (size_t)(KT - 1) * Cfg::kStageB +
+                                            (size_t)left * Cfg::kN * 16);
+        for (int i = tid; i < (kChunks - left) * Cfg::kN; i += blockDim.x) z[i] = make_uint4(0u, 0u, 0u, 0u);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
     if (tid == 0) {
         for (int i = 0; i < kMaxStages; ++i) {
             mbar_init(&bars.full[i], kProducerWarps * 32);
@@ -344,13 +457,8 @@ __device__ bool tc_prologue(unsigned char* smem, TcBars& bars, uint32_t* tmem_sl
             mbar_init(&bars.empty[i], 1);
         }
         mbar_init(&bars.done, 1);
-        mbar_init(&bars.packed, 1);
-        const uint32_t bytes = (uint32_t)(nrows_copy * rb);
-        mbar_arrive_expect_tx(&bars.packed, src1 ? 2 * bytes : bytes);
-        bulk_copy_g2s(smem + tc_packed_offset(), src0, bytes, &bars.packed);
-        if (src1) bulk_copy_g2s(smem + tc_packed_offset() + bytes, src1, bytes, &bars.packed);
     }
-    if ((tid >> 5) == kProducerWarps) tmem_alloc(tmem_slot, tmem_cols);
+    if ((tid >> 5) == kProducerWarps) tmem_alloc(tmem_slot, Cfg::kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -364,67 +472,108 @@ __device__ __forceinline__ void tc_release(uint32_t tmem, uint32_t tmem_cols) {
     if ((threadIdx.x >> 5) == kProducerWarps) tmem_dealloc(tmem, tmem_cols);
 }
 
+// Columns [c0, c0 + CB) of this thread's lane plus columns [NT + c0, NT + c0 + CB):
+// the hi and lo accumulators of CB tokens, summed (all loads issued, then one wait).
+template <int NT, int CB>
+__device__ __forceinline__ void tmem_ld_sum(uint32_t lane_addr, int c0, float* v) {
+    constexpr int W = CB % 16 == 0 ? 16 : 8;
+    uint32_t hi[CB], lo[CB];
+#pragma unroll
+    for (int i = 0; i < CB; i += W) {
+        if constexpr (W == 16) {
+            tmem_ld16(lane_addr + (uint32_t)(c0 + i), hi + i);
+            tmem_ld16(lane_addr + (uint32_t)(NT + c0 + i), lo + i);
+        } else {
+            tmem_ld8(lane_addr + (uint32_t)(c0 + i), hi + i);
+            tmem_ld8(lane_addr + (uint32_t)(NT + c0 + i), lo + i);
+        }
+    }
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < CB; ++i) v[i] = __uint_as_float(hi[i]) + __uint_as_float(lo[i]);
+}
+
 // gate/up: grid (I / 64, max tiles); rows 0..63 of the CTA are gate rows m0..m0+63 of
 // the expert, rows 64..127 the same up rows.
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) tc_gateup_kernel(TcArgs a) {
     using Cfg = TileCfg<NT>;
-    constexpr int CW = NT / 2;  // columns per epilogue warp (two warps per lane quarter)
+    constexpr int CW = NT / 2;             // token columns per epilogue warp
+    constexpr int CB = CW < 32 ? CW : 32;  // columns per tensor-memory read block
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ TcBars bars;
     __shared__ uint32_t tmem_slot;
-    __shared__ float s_scale[kRows];  // 2 s of rows 0..127 (gate rows, then up rows)
+    __shared__ float s_xs[NT];        // split scales of the tile's x rows
     int e, n0, nv, pos0;
     if (!tc_tile<NT>(a, blockIdx.y, e, n0, nv, pos0)) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, I = a.I, Bh = (H + 4) / 5;
     const int m0 = blockIdx.x * (kRows / 2);
     const int tile = blockIdx.y;
-    if (tid < kRows)
-        s_scale[tid] = 2.f * (tid < kRows / 2 ? a.s_gate[(int64_t)e * I + m0 + tid]
-                                             : a.s_up[(int64_t)e * I + m0 + tid - kRows / 2]);
+    // loads whose first use is the epilogue: in flight through the main loop
+    float row_scale = 0.f;  // s of the epilogue row 32 (w & 3) + lane (gate rows, then up rows)
+    if (warp < kProducerWarps) {
+        const int r = 32 * (warp & 3) + lane;
+        row_scale = r < kRows / 2 ? a.s_gate[(int64_t)e * I + m0 + r] : a.s_up[(int64_t)e * I + m0 + r - kRows / 2];
+    }
     const uint8_t* gsrc = a.gate + ((int64_t)e * I + m0) * Bh;
     const uint8_t* usrc = a.up + ((int64_t)e * I + m0) * Bh;
     // everything up to here reads data no kernel of this call writes
-    bool ok = tc_prologue(smem, bars, &tmem_slot, Cfg::kTmemCols, gsrc, usrc, kRows / 2, Bh,
-                          (size_t)Cfg::kStages * Cfg::kStageB, a.status);
+    bool ok = tc_prologue<NT>(smem, bars, &tmem_slot, gsrc, usrc, kRows / 2, Bh, H, a.status);
     const uint32_t tmem = tmem_slot;
-    pdl_wait();  // the gathered x of the previous kernel
+    pdl_wait();  // the split x of the previous kernel
     pdl_launch_dependents();
-    if (ok) ok = tc_mainloop<NT>(smem, smem + tc_packed_offset(), Bh, H, a.xs + (size_t)tile * H * NT, tmem, bars, a.status);
-    if (ok) {
-        // epilogue: warps 0-7 read rows 32 (w & 3) + lane and columns CW (w >> 2) .. +CW,
-        // store min(2 s_g g, clamp) (gate rows) or clamp(2 s_u u) (up rows); then every
-        // thread forms h = silu(g) u for its share of the tile and rounds it to bf16
-        unsigned char* epi = smem + tc_packed_offset();
-        float* G = reinterpret_cast<float*>(epi);                             // [NT][64]
-        float* U = G + NT * 64;                                               // [NT][64]
-        uint16_t* Hs = reinterpret_cast<uint16_t*>(U + NT * 64);              // [NT][64]
-        if (warp < kProducerWarps) {
-            const int q = warp & 3, c0 = CW * (warp >> 2), r = 32 * q + lane;
-            const uint32_t addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
-            const float sc = s_scale[r];
-            float v[CW];
+    const float x_scale = tid < NT ? a.xscale[(size_t)tile * NT + tid] : 0.f;
+    if (ok)
+        ok = tc_mainloop<NT>(smem, smem + tc_packed_offset(), Bh, H, a.xs + (size_t)tile * H * Cfg::kN, tmem, bars,
+                             a.status);
+    if (tid < NT) s_xs[tid] = x_scale;
+    __syncthreads();
+    // Epilogue.  Warp w < 8 reads TMEM lanes 32 (w & 3) .. +31: rows j = 32 (w & 1) + lane
+    // of the gate side (w & 2 clear) or of the up side, tokens [CW (w >> 2), +CW) in
+    // blocks of CB, as min(s_g s_x g, clamp) or clamp(s_u s_x u, -clamp, clamp).  Of each
+    // block the gate warp keeps the first half of the tokens and the up warp (the other
+    // side of the same rows and tokens) the second half; each hands the other half to
+    // its partner through shared memory.  Each then forms h = silu(g) u for its own
+    // tokens, rounds it to bf16 and stores it by grouped position.
+    constexpr int NB = CW / CB, HB = CB / 2;
+    float* X = reinterpret_cast<float*>(smem + tc_packed_offset());  // [NT][64] exchange
+    float own[NB][HB];
+    const int q = warp & 3, j = 32 * (q & 1) + lane;
+    const bool up_side = (q & 2) != 0;
+    if (ok && warp < kProducerWarps) {
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
 #pragma unroll
-            for (int i = 0; i < CW; i += 8) tmem_ld8(addr + i, v + i);
-            if (q < 2) {
+        for (int b = 0; b < NB; ++b) {
+            const int c0 = CW * (warp >> 2) + b * CB;
+            float v[CB];
+            tmem_ld_sum<NT, CB>(lane_addr, c0, v);
 #pragma unroll
-                for (int i = 0; i < CW; ++i) G[(c0 + i) * 64 + r] = fminf(sc * v[i], a.clamp);
-            } else {
+            for (int i = 0; i < CB; ++i) {
+                const float t = row_scale * s_xs[c0 + i] * v[i];
+                v[i] = fminf(up_side ? fmaxf(t, -a.clamp) : t, a.clamp);
+            }
 #pragma unroll
-                for (int i = 0; i < CW; ++i) U[(c0 + i) * 64 + r - 64] = fminf(fmaxf(sc * v[i], -a.clamp), a.clamp);
+            for (int i = 0; i < HB; ++i) {
+                own[b][i] = up_side ? v[HB + i] : v[i];
+                X[(c0 + (up_side ? i : HB + i)) * 64 + j] = up_side ? v[i] : v[HB + i];
             }
         }
-        __syncthreads();
-        for (int i = tid; i < nv * 64; i += kThreads)
-            Hs[i] = __bfloat16_as_ushort(__float2bfloat16_rn(silu_f(G[i]) * U[i]));
-        __syncthreads();
-        // the tile's h rows, chunk-major: chunk m0 / 8 + part, row nn
-        uint16_t* hblk = a.hs + (size_t)tile * I * NT;
-        for (int i = tid; i < nv * 8; i += kThreads) {
-            const int part = i / nv, nn = i - part * nv;
-            *reinterpret_cast<uint4*>(hblk + ((size_t)(m0 / 8 + part) * NT + nn) * 8) =
-                *reinterpret_cast<const uint4*>(Hs + nn * 64 + 8 * part);
+    }
+    __syncthreads();
+    if (ok && warp < kProducerWarps) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+#pragma unroll
+            for (int i = 0; i < HB; ++i) {
+                const int tok = CW * (warp >> 2) + b * CB + (up_side ? HB + i : i);
+                const float other = X[tok * 64 + j];
+                const float g = up_side ? other : own[b][i];
+                const float u = up_side ? own[b][i] : other;
+                // silu with the fast exponential and reciprocal: h is rounded to bf16 next
+                const __nv_bfloat16 hb = __float2bfloat16_rn(g * __frcp_rn(1.f + __expf(-g)) * u);
+                if (tok < nv) a.hrow[(int64_t)(pos0 + tok) * I + m0 + j] = __bfloat16_as_ushort(hb);
+            }
         }
     }
     tc_release(tmem, Cfg::kTmemCols);
@@ -435,69 +584,165 @@ template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) tc_down_kernel(TcArgs a) {
     using Cfg = TileCfg<NT>;
     constexpr int CW = NT / 2;
+    constexpr int CB = CW < 32 ? CW : 32;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ TcBars bars;
     __shared__ uint32_t tmem_slot;
     __shared__ int s_slot[NT];
-    __shared__ float s_w[NT];
-    __shared__ float s_scale[kRows];
+    __shared__ float s_w[NT];   // routing weight of the slot, times its h split scale
     int e, n0, nv, pos0;
     if (!tc_tile<NT>(a, blockIdx.y, e, n0, nv, pos0)) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, I = a.I, Bi = (I + 4) / 5;
     const int m0 = blockIdx.x * kRows;
-    if (tid < NT) {
-        const int slot = tid < nv ? __ldcg(a.perm + pos0 + tid) : 0;
-        s_slot[tid] = slot;
-        s_w[tid] = tid < nv ? __ldcg(a.w + slot) : 0.f;
+    const int tile = blockIdx.y;
+    // loads whose first use is the epilogue: in flight through the main loop
+    int slot = 0;
+    float w_slot = 0.f;
+    if (tid < nv) {
+        slot = __ldcg(a.perm + pos0 + tid);
+        w_slot = __ldcg(a.w + slot);
     }
-    if (tid < kRows) s_scale[tid] = 2.f * a.s_down[(int64_t)e * H + m0 + tid];
+    const float row_scale = warp < kProducerWarps ? a.s_down[(int64_t)e * H + m0 + 32 * (warp & 3) + lane] : 0.f;
     const uint8_t* dsrc = a.down + ((int64_t)e * H + m0) * Bi;
     // everything up to here reads data no kernel of this call writes after the grouping
-    bool ok = tc_prologue(smem, bars, &tmem_slot, Cfg::kTmemCols, dsrc, nullptr, kRows, Bi,
-                          (size_t)Cfg::kStages * Cfg::kStageB, a.status);
+    bool ok = tc_prologue<NT>(smem, bars, &tmem_slot, dsrc, nullptr, kRows, Bi, I, a.status);
     const uint32_t tmem = tmem_slot;
-    pdl_wait();  // h of the gate/up kernel
+    pdl_wait();  // the split h of the previous kernel
     pdl_launch_dependents();
+    const float h_scale = tid < NT ? a.hscale[(size_t)tile * NT + tid] : 0.f;
     if (ok)
-        ok = tc_mainloop<NT>(smem, smem + tc_packed_offset(), Bi, I, a.hs + (size_t)blockIdx.y * I * NT, tmem, bars,
+        ok = tc_mainloop<NT>(smem, smem + tc_packed_offset(), Bi, I, a.hs + (size_t)tile * I * Cfg::kN, tmem, bars,
                              a.status);
-    if (ok) {
-        float* Ys = reinterpret_cast<float*>(smem + tc_packed_offset());  // [NT][kRows]
-        if (warp < kProducerWarps) {
-            const int q = warp & 3, c0 = CW * (warp >> 2), r = 32 * q + lane;
-            const uint32_t addr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
-            const float sd = s_scale[r];
-            float v[CW];
+    if (tid < NT) {
+        s_slot[tid] = slot;
+        s_w[tid] = w_slot * h_scale;
+    }
+    __syncthreads();
+    // epilogue: warp w < 8 reads rows 32 (w & 3) + lane and tokens [CW (w >> 2), +CW)
+    // and stores w_slot s_h s_d D straight to the slots' rows (a warp's 32 rows of one
+    // token are 128 contiguous bytes)
+    if (ok && warp < kProducerWarps) {
+        const int q = warp & 3, r = 32 * q + lane;
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
 #pragma unroll
-            for (int i = 0; i < CW; i += 8) tmem_ld8(addr + i, v + i);
+        for (int cb = 0; cb < CW; cb += CB) {
+            const int c0 = CW * (warp >> 2) + cb;
+            float v[CB];
+            tmem_ld_sum<NT, CB>(lane_addr, c0, v);
 #pragma unroll
-            for (int i = 0; i < CW; ++i) Ys[(c0 + i) * kRows + r] = s_w[c0 + i] * (sd * v[i]);
-        }
-        __syncthreads();
-        for (int i = tid; i < nv * (kRows / 4); i += kThreads) {
-            const int nn = i / (kRows / 4), part = i % (kRows / 4);
-            *reinterpret_cast<float4*>(a.ys + (int64_t)s_slot[nn] * H + m0 + 4 * part) =
-                *reinterpret_cast<const float4*>(Ys + nn * kRows + 4 * part);
+            for (int i = 0; i < CB; ++i)
+                if (c0 + i < nv) a.ys[(int64_t)s_slot[c0 + i] * H + m0 + r] = s_w[c0 + i] * (row_scale * v[i]);
         }
     }
     tc_release(tmem, Cfg::kTmemCols);
 }
 
-// One CTA per tile: the tile's token rows of x, chunk-major ([H / 8][NT][8]).  Rows
-// past the tile's tokens are left as they are: they only reach output columns that
-// the epilogues never store.
+__device__ __forceinline__ void bf16x8_to_f32(uint4 p, float* v) {
+    v[0] = bf16_lo(p.x);
+    v[1] = bf16_hi(p.x);
+    v[2] = bf16_lo(p.y);
+    v[3] = bf16_hi(p.y);
+    v[4] = bf16_lo(p.z);
+    v[5] = bf16_hi(p.z);
+    v[6] = bf16_lo(p.w);
+    v[7] = bf16_hi(p.w);
+}
+
+// Largest |v| of a bf16 row of `cols` values (a multiple of 8) by one warp, as fp32 bits.
+__device__ __forceinline__ uint32_t warp_row_absmax(const uint4* row, int cols, int lane) {
+    uint32_t m = 0;
+    for (int c = lane; c < cols / 8; c += 32) {
+        const uint4 p = row[c];
+        const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            m = max(m, (w4[i] & 0x7fffu) << 16);
+            m = max(m, w4[i] & 0x7fff0000u);
+        }
+    }
+    return __reduce_max_sync(kFullMask, m);
+}
+
+// Splits row n of a tile (bf16, `cols` values, split scale s) into its hi row n and lo
+// row NT + n of the tile's operand block ([cols / 16][2NT][16] bytes), chunk by chunk:
+// thread (n, p) takes chunks p, p + P, ... of 16 values, so that a warp's lanes
+// (consecutive rows of one chunk) store contiguous 16-byte rows.
+template <int NT>
+__device__ __forceinline__ void split_row_chunks(const uint4* row, int cols, float s, uint8_t* blk, int n, int p,
+                                                 int P) {
+    const float inv = 1.f / s;  // a power of two: exact
+#pragma unroll 4
+    for (int c = p; c < cols / 16; c += P) {
+        float v[16];
+        bf16x8_to_f32(row[2 * c], v);
+        bf16x8_to_f32(row[2 * c + 1], v + 8);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] *= inv;
+        uint2 h0, l0, h1, l1;
+        split8(v, h0, l0);
+        split8(v + 8, h1, l1);
+        uint8_t* chunk = blk + (size_t)c * (2 * NT * 16);
+        *reinterpret_cast<uint4*>(chunk + n * 16) = make_uint4(h0.x, h0.y, h1.x, h1.y);
+        *reinterpret_cast<uint4*>(chunk + (NT + n) * 16) = make_uint4(l0.x, l0.y, l1.x, l1.y);
+    }
+}
+
+// One CTA per tile: the tile's tokens' x rows split into hi and lo rows, and their
+// scales.  Row maxima first (one warp per row), then the split (thread per row and
+// chunk phase).  Rows past the tile's tokens
+// are left as they are: they only reach accumulator columns that the epilogues never
+// store.
 template <int NT>
 __global__ void __launch_bounds__(256) tc_gather_kernel(TcArgs a) {
+    __shared__ float s_scale[NT];
     pdl_wait();
     pdl_launch_dependents();
     int e, n0, nv, pos0;
     if (!tc_tile<NT>(a, blockIdx.x, e, n0, nv, pos0)) return;
-    const int H8 = a.H / 8;
-    uint4* blk = reinterpret_cast<uint4*>(a.xs + (size_t)blockIdx.x * a.H * NT);
-    for (int i = threadIdx.x; i < H8 * nv; i += blockDim.x) {
-        const int c = i / nv, r = i - c * nv;
-        blk[c * NT + r] = reinterpret_cast<const uint4*>(a.x + (int64_t)(a.perm[pos0 + r] / a.k) * a.H)[c];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint8_t* blk = a.xs + (size_t)blockIdx.x * a.H * (2 * NT);
+    for (int n = warp; n < nv; n += 8) {
+        const uint4* xr = reinterpret_cast<const uint4*>(a.x + (int64_t)(a.perm[pos0 + n] / a.k) * a.H);
+        const uint32_t m = warp_row_absmax(xr, a.H, lane);
+        if (lane == 0) {
+            const float sc = split_scale(__uint_as_float(m));
+            s_scale[n] = sc;
+            a.xscale[(size_t)blockIdx.x * NT + n] = sc;
+        }
+    }
+    __syncthreads();
+    const int n = tid % NT;
+    if (n < nv) {
+        const uint4* xr = reinterpret_cast<const uint4*>(a.x + (int64_t)(a.perm[pos0 + n] / a.k) * a.H);
+        split_row_chunks<NT>(xr, a.H, s_scale[n], blk, n, tid / NT, 256 / NT);
+    }
+}
+
+// One CTA per tile: the tile's h rows (bf16, by grouped position) split into hi and lo
+// rows with the scale of each row's largest |h|, found first as in the x split.
+template <int NT>
+__global__ void __launch_bounds__(256) tc_split_h_kernel(TcArgs a) {
+    __shared__ float s_scale[NT];
+    pdl_wait();
+    pdl_launch_dependents();
+    int e, n0, nv, pos0;
+    if (!tc_tile<NT>(a, blockIdx.x, e, n0, nv, pos0)) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint8_t* blk = a.hs + (size_t)blockIdx.x * a.I * (2 * NT);
+    for (int n = warp; n < nv; n += 8) {
+        const uint32_t m = warp_row_absmax(reinterpret_cast<const uint4*>(a.hrow + (int64_t)(pos0 + n) * a.I), a.I, lane);
+        if (lane == 0) {
+            const float sc = split_scale(__uint_as_float(m));
+            s_scale[n] = sc;
+            a.hscale[(size_t)blockIdx.x * NT + n] = sc;
+        }
+    }
+    __syncthreads();
+    const int n = tid % NT;
+    if (n < nv) {
+        const uint4* hr = reinterpret_cast<const uint4*>(a.hrow + (int64_t)(pos0 + n) * a.I);
+        split_row_chunks<NT>(hr, a.I, s_scale[n], blk, n, tid / NT, 256 / NT);
     }
 }
 
@@ -526,9 +771,11 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(TcArgs a) {
     }
 }
 
-// tile_off[e] = sum over e' < e of ceil(counts[e'] / nt); one CTA, E <= 1024.
+// tile_off[e] = sum over e' < e of ceil(counts[e'] / nt), and tile_e[t] = e for the
+// tiles t of expert e; one CTA, E <= 1024.
 __global__ void __launch_bounds__(1024) tc_tile_prefix_kernel(const int32_t* __restrict__ counts, int E, int nt,
-                                                              int32_t* __restrict__ tile_off) {
+                                                              int32_t* __restrict__ tile_off,
+                                                              int32_t* __restrict__ tile_e) {
     __shared__ int32_t part[32];
     pdl_wait();
     pdl_launch_dependents();
@@ -555,6 +802,7 @@ __global__ void __launch_bounds__(1024) tc_tile_prefix_kernel(const int32_t* __r
     const int excl = (warp > 0 ? part[warp - 1] : 0) + incl - v;
     if (tid < E) tile_off[tid] = excl;
     if (tid == E - 1) tile_off[E] = excl + v;
+    for (int t = 0; t < v; ++t) tile_e[excl + t] = tid;
 }
 
 }  // namespace
@@ -572,8 +820,7 @@ int ffn_tensor_max_tiles(int S, int E) {
 
 // MAPLE_FFN_PATH=tensor or =cores forces a path (for parity tests of both on the same
 // inputs); otherwise the tensor path runs once there are at least half as many slots
-// as experts (on the Maple layer, 16 tokens and up: measured faster than the CUDA-core
-// kernels from there on, slower below).
+// as experts (on the Maple layer, 16 tokens and up).
 bool ffn_use_tensor(int T, int k, int E, int H, int I) {
     if (!ffn_tensor_shape_ok(H, I) || T < 1) return false;
     const char* env = getenv("MAPLE_FFN_PATH");
@@ -583,19 +830,24 @@ bool ffn_use_tensor(int T, int k, int E, int H, int I) {
 }
 
 // H a multiple of the 128 down rows of a CTA, I of the 64 gate (and up) rows; both at
-// least 128 so that a B box (10 chunks of 8 values) fits inside a row.
+// least 128, and at most 2080 so that a CTA's packed rows and its four B stages fit in
+// shared memory.
 bool ffn_tensor_shape_ok(int H, int I) {
     return H % kRows == 0 && I % (kRows / 2) == 0 && H >= 128 && I >= 128 && H <= 2080 && I <= 2080;
 }
 
+// Operand blocks: per tile, 2NT rows (hi, lo) of H (x) or I (h) e4m3 values.
 size_t ffn_tensor_x_bytes(int S, int E, int H) {
-    const int nt = ffn_tensor_tile_tokens(S, E);
-    return (size_t)ffn_tensor_max_tiles(S, E) * H * nt * 2;
+    return (size_t)ffn_tensor_max_tiles(S, E) * H * 2 * ffn_tensor_tile_tokens(S, E);
 }
 
 size_t ffn_tensor_h_bytes(int S, int E, int I) {
-    const int nt = ffn_tensor_tile_tokens(S, E);
-    return (size_t)ffn_tensor_max_tiles(S, E) * I * nt * 2;
+    return (size_t)ffn_tensor_max_tiles(S, E) * I * 2 * ffn_tensor_tile_tokens(S, E);
+}
+
+// Split scales: one fp32 per tile row.
+size_t ffn_tensor_scale_bytes(int S, int E) {
+    return sizeof(float) * (size_t)ffn_tensor_max_tiles(S, E) * ffn_tensor_tile_tokens(S, E);
 }
 
 namespace {
@@ -615,6 +867,8 @@ cudaError_t launch_tc_ffn(const TcArgs& a, int S, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     err = launch_pdl(gu, dim3(a.I / (kRows / 2), tiles), dim3(kThreads), smem_gu, stream, a);
     if (err != cudaSuccess) return err;
+    err = launch_pdl(tc_split_h_kernel<NT>, dim3(tiles), dim3(256), 0, stream, a);
+    if (err != cudaSuccess) return err;
     return launch_pdl(dn, dim3(a.H / kRows, tiles), dim3(kThreads), smem_dn, stream, a);
 }
 
@@ -630,7 +884,7 @@ cudaError_t launch_moe_ffn_tensor(const FfnArgs& f, cudaStream_t stream, const D
                                                      f.n_active, stream, dev);
     if (err != cudaSuccess) return err;
     err = launch_pdl(tc_tile_prefix_kernel, dim3(1), dim3(1024), 0, stream, (const int32_t*)f.counts, f.E, nt,
-                     f.tile_off);
+                     f.tile_off, f.tile_off + f.E + 1);
     if (err != cudaSuccess) return err;
     TcArgs a;
     a.gate = f.gate;
@@ -651,8 +905,12 @@ cudaError_t launch_moe_ffn_tensor(const FfnArgs& f, cudaStream_t stream, const D
     a.offsets = f.offsets;
     a.perm = f.perm;
     a.tile_off = f.tile_off;
+    a.tile_e = f.tile_off + f.E + 1;
     a.xs = f.xs;
     a.hs = f.hs;
+    a.xscale = f.xscale;
+    a.hscale = f.hscale;
+    a.hrow = reinterpret_cast<uint16_t*>(f.h);
     a.ys = f.ys;
     a.y = f.y;
     a.T = f.T;

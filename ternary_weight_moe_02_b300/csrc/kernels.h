@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+struct maple_experts;
+
 namespace maple {
 
 // Sets the per-thread text behind maple_last_error() and returns `status`.
@@ -64,32 +66,44 @@ struct FfnArgs {
     int32_t* active;   // [E]
     int32_t* n_active; // [1]
     float* h;          // [T*k][I] (bf16 [T*k][I] on the tensor path)
-    int32_t* tile_off; // [E+1] tensor path only
+    int32_t* tile_off; // tensor path only: [E+1] tile prefix, then [max tiles] expert of each tile
     int32_t* chunks;   // grouping scratch of the tensor path
-    uint16_t* xs;      // tensor path only: per tile, the tokens' x rows, chunk-major
-    uint16_t* hs;      // tensor path only: per tile, the tokens' h rows, chunk-major
+    uint8_t* xs;       // tensor path only: per tile, the tokens' x rows split into e4m3 hi/lo rows
+    uint8_t* hs;       // tensor path only: per tile, the tokens' h rows split likewise
+    float* xscale;     // tensor path only: split scale of each tile row of xs
+    float* hscale;     // tensor path only: split scale of each tile row of hs
     float* ys;         // [T*k][H] tensor path only
     int* status;       // device status word
     int prefetch_down; // 1 if the down rows may be bulk-prefetched (16-byte multiples)
+    int tensor;        // 1: grouped tensor-core path (the workspace holds its regions)
 };
 
 struct FfnWorkspaceLayout {
-    size_t counts, offsets, perm, active, n_active, h, tile_off, chunks, xs, hs, ys, total;
+    size_t counts, offsets, perm, active, n_active, h, tile_off, chunks, xs, hs, xscale, hscale, ys, total;
     bool tensor;
 };
-FfnWorkspaceLayout ffn_workspace_layout(int T, int k, int E, int H, int I);
+// `tensor`: lay out the regions of the grouped tensor-core path too.
+FfnWorkspaceLayout ffn_workspace_layout(int T, int k, int E, int H, int I, bool tensor);
 
 cudaError_t launch_moe_ffn(const FfnArgs& a, cudaStream_t stream, const DeviceInfo& dev);
 
 // Grouped tensor-core FFN (tcgen05): shapes it takes, the path choice for a call, and
-// the launch (group, tile prefix, gate/up, down, combine).
+// the launch (group, tile prefix, split x, gate/up, split h, down, combine).
 bool ffn_tensor_shape_ok(int H, int I);
 bool ffn_use_tensor(int T, int k, int E, int H, int I);
 int ffn_tensor_tile_tokens(int S, int E);
 int ffn_tensor_max_tiles(int S, int E);
 size_t ffn_tensor_x_bytes(int S, int E, int H);
 size_t ffn_tensor_h_bytes(int S, int E, int I);
+size_t ffn_tensor_scale_bytes(int S, int E);
 cudaError_t launch_moe_ffn_tensor(const FfnArgs& a, cudaStream_t stream, const DeviceInfo& dev);
+
+// maple_moe_ffn with the path choice made by the caller: allow_tensor = false keeps the
+// call on the CUDA-core kernels (the allocation-free entry point, whose scratch is
+// small).  moe_ffn_workspace_bytes is the workspace such a call needs.
+size_t moe_ffn_workspace_bytes(int T, int k, const ::maple_experts* ex, bool allow_tensor);
+int moe_ffn_entry(const ::maple_experts* ex, const uint16_t* x, const int32_t* idx, const float* w, int T, int k,
+                  float* y, void* ws, size_t ws_bytes, void* stream, bool allow_tensor);
 
 // Fused single-token layer step (route + gate/up + down in one cooperative launch).
 struct LayerLaunch {

@@ -1,5 +1,6 @@
-"""GPU parity of the grouped tensor-core FFN path (tcgen05 MMAs on trits decoded to
-bf16) against the CPU oracle, element by element: |y_gpu - y| <= 2e-3 * max|y| + 1e-5
+"""GPU parity of the grouped tensor-core FFN path (tcgen05 fp8 MMAs: trits decoded to
+e4m3, each bf16 activation row split exactly into two e4m3 rows under a power-of-two
+scale) against the CPU oracle, element by element: |y_gpu - y| <= 2e-3 * max|y| + 1e-5
 ("Maple-Preview ...", section "The shipped code does no quantization").  This path
 rounds h to bf16 before the down projection; the bound above covers it.
 
@@ -146,6 +147,28 @@ def test_tensor_path_invalid_ids_and_clamp():
     valid = (idx >= 0) & (idx < E)
     y_ref = _oracle(packed, x, np.where(valid, idx, 0).astype(np.int32), np.where(valid, w32, 0))
     assert_ffn_close(y, y_ref, "tensor invalid ids, clamped")
+
+
+def test_tensor_path_rows_of_very_different_magnitude():
+    """Each token row gets its own split scale: rows scaled by 2^-24 .. 2^9 (and one
+    all-zero row) each match the oracle within 4e-3 of that row's own largest output.
+    One scale shared by the tile would flush the small rows to zero (errors of order
+    one).  The bound is twice the whole-output one because, taken row by row, the
+    rounding of h to bf16 alone reaches 2.6e-3 of a row's largest output on these
+    shapes (fp64 model of that single rounding)."""
+    E, H, I, T, k = 8, 256, 128, 12, 4
+    packed, ex = _layer(E, H, I, seed=31)
+    scale = torch.tensor([2.0 ** (3 * t - 24) for t in range(T)]).unsqueeze(1)
+    x = (synth.tokens(T, H, seed=31).float() * scale).to(torch.bfloat16)
+    x[4] = 0
+    idx, w32 = _random_routing(T, E, k, seed=31)
+    with ffn_path("tensor"):
+        y = _run(ex, x, idx, w32)
+    y_ref = _oracle(packed, x, idx, w32)
+    assert np.all(y[4] == 0)
+    for t in range(T):
+        tol = 4e-3 * np.abs(y_ref[t]).max() + 1e-30
+        assert np.abs(y[t] - y_ref[t]).max() <= tol, (t, np.abs(y[t] - y_ref[t]).max(), tol)
 
 
 def test_tensor_path_all_zero_weights_give_zero():

@@ -8,6 +8,7 @@ a misaligned bulk copy faults the GPU, so this runs on the CPU first."""
 import itertools
 
 import numpy as np
+import torch
 
 GU_ROWS = 8      # row pairs per gate/up CTA
 DN_ROWS = 16     # output rows per down CTA
@@ -283,12 +284,14 @@ def test_integer_pack_unit_matches_the_oracle_packing():
     assert checked > 2500
 
 
-TC_ROWS, TC_KTILE, TC_LUT = 128, 80, 256 * 4 * 8
+TC_ROWS, TC_KTILE, TC_LUT = 128, 160, 256 * 16 * 8
 TC_A_STRIDE = 48
+TC_STATIC_SMEM = 1152  # largest static shared memory of the grouped kernels (ptxas -v)
 
 
 def tc_stage_b(nt):
-    return TC_KTILE // 8 * nt * 16
+    """A B stage: 10 core-matrix columns of 16 e4m3 values for 2 NT rows (hi, lo)."""
+    return TC_KTILE // 16 * 2 * nt * 16
 
 
 def tc_shape_ok(H, I):
@@ -297,7 +300,7 @@ def tc_shape_ok(H, I):
 
 
 def tc_stages(nt):
-    return 4
+    return 3 if nt >= 128 else 4
 
 
 def tc_smem(row_bytes, nt):
@@ -306,37 +309,45 @@ def tc_smem(row_bytes, nt):
 
 
 def tc_tmem(nt):
-    a_base = 32 if nt < 32 else nt
+    a_base = max(2 * nt, 32)
     used = a_base + tc_stages(nt) * TC_A_STRIDE
     return a_base, used, 256 if used <= 256 else 512
 
 
 def test_tensor_path_plan_fits_and_is_aligned():
     """The grouped tcgen05 kernels (csrc/ffn_tensor.cu), for both token-tile widths:
-    shared memory within the opt-in limit for every accepted shape and the epilogue
-    buffers inside it, the packed-row bulk copies 16-byte aligned, every MMA read of a
-    B stage (5 MMAs of K = 16, NT/8 row groups at 128 B, 2 core-matrix columns at
-    NT * 16 B) inside the stage, and the tensor-memory columns (accumulator, A stages
-    of 40 columns at a 48-column stride, four stages) inside the power-of-two
-    allocation."""
+    shared memory within the opt-in limit for every accepted shape (two CTAs per SM
+    for the 16-token tiles) and the epilogue buffers inside it, the packed-row bulk copies 16-byte aligned, every MMA read of a
+    B stage (5 MMAs of K = 32, 2NT/8 row groups at 128 B, 2 core-matrix columns at
+    2NT * 16 B) inside the stage, and the tensor-memory columns (accumulator of 2NT
+    columns, A stages of 40 columns at a 48-column stride, three or four stages) inside
+    the power-of-two allocation."""
     shapes = [(H, I) for H in range(128, 2081, 128) for I in range(128, 2081, 64)]
     for nt in (16, 128):
         a_base, used, alloc = tc_tmem(nt)
-        assert nt <= a_base and a_base % 16 == 0
-        assert a_base + (tc_stages(nt) - 1) * TC_A_STRIDE + TC_KTILE // 2 <= used <= alloc
+        assert 2 * nt <= a_base and a_base % 16 == 0
+        assert a_base + (tc_stages(nt) - 1) * TC_A_STRIDE + TC_KTILE // 4 <= used <= alloc
         assert alloc in (256, 512) and (nt == 16) == (alloc == 256)
         sb = tc_stage_b(nt)
-        for q in range(TC_KTILE // 16):
-            assert q * 2 * nt * 16 + nt * 16 + (nt // 8 - 1) * 128 + 127 < sb
+        n = 2 * nt
+        for q in range(TC_KTILE // 32):
+            assert q * 2 * n * 16 + n * 16 + (n // 8 - 1) * 128 + 127 < sb
         for H, I in shapes:
             assert tc_shape_ok(H, I)
             for cols in (H, I):
-                assert cols // 8 >= TC_KTILE // 8 and (cols * 2) % 16 == 0
+                assert cols % 16 == 0
             for rb, rows_per_cta, mstep, mtot, epi in (
-                    (nbytes(H), TC_ROWS // 2, TC_ROWS // 2, I, nt * 64 * (4 + 4 + 2)),
-                    (nbytes(I), TC_ROWS, TC_ROWS, H, nt * TC_ROWS * 4)):
+                    (nbytes(H), TC_ROWS // 2, TC_ROWS // 2, I, nt * 64 * 4),
+                    (nbytes(I), TC_ROWS, TC_ROWS, H, 0)):
                 stage_off, total = tc_smem(rb, nt)
-                assert total + 1280 <= 232448, (H, I, nt, total)
+                assert total + TC_STATIC_SMEM <= 232448, (H, I, nt, total)
+                if nt == 16:  # two CTAs per SM (228 KB, 1 KB reserved per CTA)
+                    assert 2 * (total + TC_STATIC_SMEM + 1024) <= 233472, (H, I, total)
+                # the producers' word loads: 5 aligned words from byte 127 rb + 32 kt + 16 h
+                K = H if rb == nbytes(H) else I
+                kt_last = -(-K // TC_KTILE) - 1
+                far = ((127 * rb + 32 * kt_last + 16) & ~3) + 20
+                assert TC_LUT + far <= total, (H, I, nt)
                 assert TC_LUT + epi <= total
                 size = rows_per_cta * rb
                 for e in (0, 1, 7):
@@ -347,21 +358,93 @@ def test_tensor_path_plan_fits_and_is_aligned():
 
 
 def test_tensor_path_operand_blocks_are_aligned_and_in_bounds():
-    """The B operand of a tile lives in global memory as [K / 8][NT][8] bf16 (the
-    gather kernel writes x that way, the gate/up epilogue h); each K tile's stage is
-    one bulk copy of up to 10 chunks, fewer at the K tail.  Every copy starts on a
-    16-byte boundary, has a multiple of 16 bytes and stays inside its tile's block."""
+    """The B operand of a tile lives in global memory as [K / 16][2NT][16] e4m3 bytes
+    (the split kernels write x and h that way: hi rows 0..NT-1, lo rows NT..2NT-1); each
+    K tile's stage is one bulk copy of up to 10 chunks, fewer at the K tail.  Every copy
+    starts on a 16-byte boundary, has a multiple of 16 bytes and stays inside its tile's
+    block, and the split kernels' 8-byte stores stay inside the block too."""
     for nt in (16, 128):
         for K in (128, 192, 384, 512, 2048):
-            block = K * nt * 2
+            block = K * 2 * nt
             KT = -(-K // TC_KTILE)
             covered = 0
             for j in range(KT):
-                left = K // 8 - j * (TC_KTILE // 8)
-                nbytes = min(left, TC_KTILE // 8) * nt * 16
-                off = j * (TC_KTILE // 8) * nt * 16
+                left = K // 16 - j * (TC_KTILE // 16)
+                nb = min(left, TC_KTILE // 16) * 2 * nt * 16
+                off = j * tc_stage_b(nt)
                 for tile in (0, 1, 5):
-                    _check(tile * block + off, nbytes, (tile + 1) * block, f"B nt={nt} K={K} j={j}")
-                assert nbytes <= tc_stage_b(nt)
-                covered += nbytes
+                    _check(tile * block + off, nb, (tile + 1) * block, f"B nt={nt} K={K} j={j}")
+                assert nb <= tc_stage_b(nt)
+                covered += nb
             assert covered == block
+            for c in range(K // 8):
+                for row in (0, nt - 1, nt, 2 * nt - 1):
+                    off = (c >> 1) * 2 * nt * 16 + (c & 1) * 8 + row * 16
+                    assert off % 8 == 0 and off + 8 <= block
+
+
+def _e4m3(v):
+    return torch.from_numpy(np.asarray(v, np.float32)).to(torch.float8_e4m3fn).float().numpy()
+
+
+def test_two_e4m3_split_is_exact_for_bf16_rows():
+    """The grouped kernels feed bf16 rows to fp8 MMAs as v = s (hi + lo), with s a power
+    of two that puts the row's largest magnitude in [2^7, 2^8), hi = e4m3(v / s) and lo =
+    e4m3(v / s - hi) (round to nearest even).  Over every finite bf16 value of that
+    range and below: the split is exact once |v / s| >= 2^-2, and below that it loses at
+    most half of e4m3's smallest step, 2^-10."""
+    bits = np.arange(0, 0x7F80, dtype=np.uint32)  # every non-negative finite bf16
+    v = (bits << 16).view(np.float32)
+    v = v[v < 256.0]
+    v = np.concatenate([v, -v])
+    hi = _e4m3(v)
+    lo = _e4m3(v - hi)
+    err = np.abs(hi.astype(np.float64) + lo - v)
+    big = np.abs(v) >= 0.25
+    assert np.all(err[big] == 0)
+    assert err.max() <= 2.0 ** -10
+    assert np.abs(hi).max() <= 256.0
+
+
+def test_grouped_decode_table_matches_the_oracle_unpack():
+    """The grouped kernels decode a packed byte c through a 256-entry table whose entry
+    c holds the e4m3 values of the five trits (0xB8 = -1, 0x00 = 0, 0x38 = +1) in bytes
+    0-4, and five zeros for the invalid codes 243..255; a word of the row's four next
+    e4m3 values is assembled by byte permutes.  The table's construction (digits by
+    repeated division) against oracle.unpack for every byte value, and the permutes
+    against plain concatenation."""
+    import oracle
+
+    e4m3_of = {-1: 0xB8, 0: 0x00, 1: 0x38}
+    table = []
+    for c in range(256):
+        b = [0] * 5
+        if c < 243:
+            code = c
+            for t in range(5):
+                b[t] = e4m3_of[code % 3 - 1]
+                code //= 3
+        table.append(b)
+    for c in range(256):
+        if c > 242:
+            assert table[c] == [0] * 5
+            continue
+        trits = oracle.unpack(np.array([[c]], np.uint8), 5)[0]
+        assert table[c] == [e4m3_of[int(t)] for t in trits], c
+
+    def perm(x, y, sel):
+        src = [(x >> (8 * i)) & 0xFF for i in range(4)] + [(y >> (8 * i)) & 0xFF for i in range(4)]
+        return sum(src[(sel >> (4 * i)) & 7] << (8 * i) for i in range(4))
+
+    def word(bs):
+        return sum(v << (8 * i) for i, v in enumerate(bs))
+    rng = np.random.default_rng(0)
+    for _ in range(300):
+        codes = rng.integers(0, 256, 4)
+        en = [(word(table[c][:4]), table[c][4]) for c in codes]
+        flat = sum((table[c] for c in codes), [])
+        words = [en[0][0], perm(en[0][1], en[1][0], 0x6540),
+                 perm(perm(en[1][0], en[1][1], 0x0043), en[2][0], 0x5410),
+                 perm(perm(en[2][0], en[2][1], 0x0432), en[3][0], 0x4210),
+                 perm(en[3][0], en[3][1], 0x4321)]
+        assert words == [word(flat[4 * i:4 * i + 4]) for i in range(5)]

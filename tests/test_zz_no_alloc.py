@@ -9,8 +9,10 @@ of the array's device address.
 
 Checks, through the C-ABI: two calls in a row (different inputs, so stale contents
 of the shared array would show) match maple_moe_ffn with a caller-provided workspace
-within the FFN tolerance |y - y_ref| <= 2e-3 max|y_ref| + 1e-5; a size beyond the
-array is rejected with MAPLE_ERR_WORKSPACE and leaves the output untouched."""
+within the FFN tolerance |y - y_ref| <= 2e-3 max|y_ref| + 1e-5 (the entry point always
+takes the CUDA-core kernels; the workspace call takes the tensor-core path at these
+sizes); the largest accepted size works and the next one is rejected with
+MAPLE_ERR_WORKSPACE, leaving the output untouched."""
 import numpy as np
 import pytest
 import torch
@@ -72,9 +74,16 @@ def test_static_scratch_rejects_sizes_beyond_the_array():
     from ternary_weight_moe_02_b300 import maple
     E, H, I, k = 16, 2048, 512, 8
     ex = _experts(E, H, I, seed=3)
-    T = 128  # 128 tokens x 8 slots x 512 rows x 4 B = 2 MiB of h alone
-    assert maple.maple_moe_ffn_workspace_size(T, k, ex) > 2 << 20
-    assert maple.maple_moe_ffn_workspace_size(127, k, ex) <= 2 << 20
+    # the entry point runs the CUDA-core kernels: 127 tokens fit, 128 tokens x 8 slots x
+    # 512 rows x 4 B = 2 MiB of h alone do not
+    x, idx, w = _inputs(127, E, H, k, seed=4)
+    y_ref = _with_workspace(ex, x, idx, w)
+    y = torch.full((127, H), float("nan"), device="cuda")
+    maple.maple_moe_ffn_static_scratch(ex, x, idx, w, y)
+    torch.cuda.synchronize()
+    ref = y_ref.cpu().numpy().astype(np.float64)
+    assert np.abs(y.cpu().numpy() - ref).max() <= 2e-3 * np.abs(ref).max() + 1e-5
+    T = 128
     x, idx, w = _inputs(T, E, H, k, seed=3)
     y = torch.full((T, H), 7.0, device="cuda")
     with pytest.raises(maple.MapleError) as err:
