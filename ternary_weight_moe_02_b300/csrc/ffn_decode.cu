@@ -509,7 +509,7 @@ FfnWorkspaceLayout ffn_workspace_layout(int T, int k, int E, int H, int I, bool 
     L.tensor = tensor;
     L.tile_off = L.chunks = L.xs = L.hs = L.xscale = L.hscale = L.ys = o;
     if (L.tensor) {
-        o = align_up(o + 4 * ((size_t)E + 1 + (size_t)ffn_tensor_max_tiles((int)S, E)), 256);
+        o = align_up(o + 4 * (((size_t)E + 1 + 3) & ~(size_t)3) + 16 * (size_t)ffn_tensor_max_tiles((int)S, E), 256);
         L.chunks = o;
         o = align_up(o + group_chunked_bytes((int)S, E), 256);
         L.xs = o;

@@ -288,7 +288,7 @@ struct TcArgs {
     const int32_t* offsets;
     const int32_t* perm;
     const int32_t* tile_off;  // [E + 1] prefix of ceil(counts / NT)
-    const int32_t* tile_e;    // [tiles] expert of each tile
+    const int4* tile_info;    // [tiles] expert, first token, tokens, first grouped position
     uint8_t* xs;              // [tile][H / 16][2NT][16] e4m3: each tile's x rows, hi then lo
     uint8_t* hs;              // [tile][I / 16][2NT][16] e4m3: each tile's h rows, hi then lo
     float* xscale;            // [tile][NT] split scales of the x rows
@@ -312,16 +312,18 @@ __host__ __device__ constexpr size_t tc_smem_bytes(int row_bytes) {
 }
 
 // Finds the expert and token range of grid row `tile`; false when past the last tile.
-// The tile table, counts and offsets come from kernels that completed before the
-// previous one started, so they are read (through L2) before this grid's PDL wait.
+// The tile table comes from a kernel that completed before the previous one started,
+// so it is read (through L2) before this grid's PDL wait; both loads are in flight at
+// once.
 template <int NT>
 __device__ __forceinline__ bool tc_tile(const TcArgs& a, int tile, int& e, int& n0, int& nv, int& pos0) {
-    if (tile >= __ldcg(a.tile_off + a.E)) return false;
-    e = __ldcg(a.tile_e + tile);
-    n0 = (tile - __ldcg(a.tile_off + e)) * NT;
-    const int left = __ldcg(a.counts + e) - n0;
-    nv = left < NT ? left : NT;
-    pos0 = __ldcg(a.offsets + e) + n0;
+    const int total = __ldcg(a.tile_off + a.E);
+    const int4 info = __ldcg(a.tile_info + tile);
+    if (tile >= total) return false;
+    e = info.x;
+    n0 = info.y;
+    nv = info.z;
+    pos0 = info.w;
     return nv > 0;
 }
 
@@ -570,8 +572,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gateup_kernel(TcArgs a) {
                 const float other = X[tok * 64 + j];
                 const float g = up_side ? other : own[b][i];
                 const float u = up_side ? own[b][i] : other;
-                // silu with the fast exponential and reciprocal: h is rounded to bf16 next
-                const __nv_bfloat16 hb = __float2bfloat16_rn(g * __frcp_rn(1.f + __expf(-g)) * u);
+                // silu with the fast exponential and division (a quotient of 0 once
+                // exp(-g) overflows): h is rounded to bf16 next
+                const __nv_bfloat16 hb = __float2bfloat16_rn(__fdividef(g, 1.f + __expf(-g)) * u);
                 if (tok < nv) a.hrow[(int64_t)(pos0 + tok) * I + m0 + j] = __bfloat16_as_ushort(hb);
             }
         }
@@ -625,14 +628,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_down_kernel(TcArgs a) {
     if (ok && warp < kProducerWarps) {
         const int q = warp & 3, r = 32 * q + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
+        float* yr = a.ys + m0 + r;
+        float v[CW];
 #pragma unroll
-        for (int cb = 0; cb < CW; cb += CB) {
-            const int c0 = CW * (warp >> 2) + cb;
-            float v[CB];
-            tmem_ld_sum<NT, CB>(lane_addr, c0, v);
+        for (int cb = 0; cb < CW; cb += CB) tmem_ld_sum<NT, CB>(lane_addr, CW * (warp >> 2) + cb, v + cb);
 #pragma unroll
-            for (int i = 0; i < CB; ++i)
-                if (c0 + i < nv) a.ys[(int64_t)s_slot[c0 + i] * H + m0 + r] = s_w[c0 + i] * (row_scale * v[i]);
+        for (int i = 0; i < CW; ++i) {
+            const int tok = CW * (warp >> 2) + i;
+            if (tok < nv) yr[(int64_t)s_slot[tok] * H] = s_w[tok] * (row_scale * v[i]);
         }
     }
     tc_release(tmem, Cfg::kTmemCols);
@@ -672,7 +675,7 @@ template <int NT>
 __device__ __forceinline__ void split_row_chunks(const uint4* row, int cols, float s, uint8_t* blk, int n, int p,
                                                  int P) {
     const float inv = 1.f / s;  // a power of two: exact
-#pragma unroll 4
+#pragma unroll 8
     for (int c = p; c < cols / 16; c += P) {
         float v[16];
         bf16x8_to_f32(row[2 * c], v);
@@ -688,61 +691,67 @@ __device__ __forceinline__ void split_row_chunks(const uint4* row, int cols, flo
     }
 }
 
-// One CTA per tile: the tile's tokens' x rows split into hi and lo rows, and their
-// scales.  Row maxima first (one warp per row), then the split (thread per row and
-// chunk phase).  Rows past the tile's tokens
-// are left as they are: they only reach accumulator columns that the epilogues never
-// store.
+// The split kernels run one CTA per 16 rows of a tile (grid: tiles x NT / 16): row
+// maxima first (one warp per two rows), then the split, thread (row, chunk phase) of
+// the CTA's 16 rows, so that a warp stores two 256-byte runs per step.
+constexpr int kSplitRows = 16;
+
+// One CTA per 16 rows of a tile: those tokens' x rows split into hi and lo rows, and
+// their scales.  Rows past the tile's tokens are left as they are: they only reach
+// accumulator columns that the epilogues never store.
 template <int NT>
 __global__ void __launch_bounds__(256) tc_gather_kernel(TcArgs a) {
-    __shared__ float s_scale[NT];
+    __shared__ float s_scale[kSplitRows];
+    __shared__ const uint4* s_row[kSplitRows];
     pdl_wait();
     pdl_launch_dependents();
     int e, n0, nv, pos0;
     if (!tc_tile<NT>(a, blockIdx.x, e, n0, nv, pos0)) return;
+    const int r0 = blockIdx.y * kSplitRows;
+    if (r0 >= nv) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint8_t* blk = a.xs + (size_t)blockIdx.x * a.H * (2 * NT);
-    for (int n = warp; n < nv; n += 8) {
+    for (int n = r0 + warp; n < nv && n < r0 + kSplitRows; n += 8) {
         const uint4* xr = reinterpret_cast<const uint4*>(a.x + (int64_t)(a.perm[pos0 + n] / a.k) * a.H);
         const uint32_t m = warp_row_absmax(xr, a.H, lane);
         if (lane == 0) {
             const float sc = split_scale(__uint_as_float(m));
-            s_scale[n] = sc;
+            s_scale[n - r0] = sc;
+            s_row[n - r0] = xr;
             a.xscale[(size_t)blockIdx.x * NT + n] = sc;
         }
     }
     __syncthreads();
-    const int n = tid % NT;
-    if (n < nv) {
-        const uint4* xr = reinterpret_cast<const uint4*>(a.x + (int64_t)(a.perm[pos0 + n] / a.k) * a.H);
-        split_row_chunks<NT>(xr, a.H, s_scale[n], blk, n, tid / NT, 256 / NT);
-    }
+    const int n = r0 + tid % kSplitRows;
+    if (n < nv) split_row_chunks<NT>(s_row[n - r0], a.H, s_scale[n - r0], blk, n, tid / kSplitRows, 256 / kSplitRows);
 }
 
-// One CTA per tile: the tile's h rows (bf16, by grouped position) split into hi and lo
-// rows with the scale of each row's largest |h|, found first as in the x split.
+// One CTA per 16 rows of a tile: those h rows (bf16, by grouped position) split into hi
+// and lo rows with the scale of each row's largest |h|, found first as in the x split.
 template <int NT>
 __global__ void __launch_bounds__(256) tc_split_h_kernel(TcArgs a) {
-    __shared__ float s_scale[NT];
+    __shared__ float s_scale[kSplitRows];
     pdl_wait();
     pdl_launch_dependents();
     int e, n0, nv, pos0;
     if (!tc_tile<NT>(a, blockIdx.x, e, n0, nv, pos0)) return;
+    const int r0 = blockIdx.y * kSplitRows;
+    if (r0 >= nv) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint8_t* blk = a.hs + (size_t)blockIdx.x * a.I * (2 * NT);
-    for (int n = warp; n < nv; n += 8) {
+    for (int n = r0 + warp; n < nv && n < r0 + kSplitRows; n += 8) {
         const uint32_t m = warp_row_absmax(reinterpret_cast<const uint4*>(a.hrow + (int64_t)(pos0 + n) * a.I), a.I, lane);
         if (lane == 0) {
             const float sc = split_scale(__uint_as_float(m));
-            s_scale[n] = sc;
+            s_scale[n - r0] = sc;
             a.hscale[(size_t)blockIdx.x * NT + n] = sc;
         }
     }
     __syncthreads();
-    const int n = tid % NT;
+    const int n = r0 + tid % kSplitRows;
     if (n < nv) {
         const uint4* hr = reinterpret_cast<const uint4*>(a.hrow + (int64_t)(pos0 + n) * a.I);
-        split_row_chunks<NT>(hr, a.I, s_scale[n], blk, n, tid / NT, 256 / NT);
+        split_row_chunks<NT>(hr, a.I, s_scale[n - r0], blk, n, tid / kSplitRows, 256 / kSplitRows);
     }
 }
 
@@ -771,11 +780,13 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(TcArgs a) {
     }
 }
 
-// tile_off[e] = sum over e' < e of ceil(counts[e'] / nt), and tile_e[t] = e for the
-// tiles t of expert e; one CTA, E <= 1024.
-__global__ void __launch_bounds__(1024) tc_tile_prefix_kernel(const int32_t* __restrict__ counts, int E, int nt,
+// tile_off[e] = sum over e' < e of ceil(counts[e'] / nt), and for each tile t of expert
+// e its record (e, first token n0 within the expert, tokens, grouped position of token
+// n0); one CTA, E <= 1024.
+__global__ void __launch_bounds__(1024) tc_tile_prefix_kernel(const int32_t* __restrict__ counts,
+                                                              const int32_t* __restrict__ offsets, int E, int nt,
                                                               int32_t* __restrict__ tile_off,
-                                                              int32_t* __restrict__ tile_e) {
+                                                              int4* __restrict__ tile_info) {
     __shared__ int32_t part[32];
     pdl_wait();
     pdl_launch_dependents();
@@ -802,7 +813,10 @@ __global__ void __launch_bounds__(1024) tc_tile_prefix_kernel(const int32_t* __r
     const int excl = (warp > 0 ? part[warp - 1] : 0) + incl - v;
     if (tid < E) tile_off[tid] = excl;
     if (tid == E - 1) tile_off[E] = excl + v;
-    for (int t = 0; t < v; ++t) tile_e[excl + t] = tid;
+    for (int t = 0; t < v; ++t) {
+        const int n0 = t * nt, left = counts[tid] - n0;
+        tile_info[excl + t] = make_int4(tid, n0, left < nt ? left : nt, offsets[tid] + n0);
+    }
 }
 
 }  // namespace
@@ -863,11 +877,11 @@ cudaError_t launch_tc_ffn(const TcArgs& a, int S, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     err = ensure_dynamic_smem(dn, smem_dn);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(tc_gather_kernel<NT>, dim3(tiles), dim3(256), 0, stream, a);
+    err = launch_pdl(tc_gather_kernel<NT>, dim3(tiles, NT / kSplitRows), dim3(256), 0, stream, a);
     if (err != cudaSuccess) return err;
     err = launch_pdl(gu, dim3(a.I / (kRows / 2), tiles), dim3(kThreads), smem_gu, stream, a);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(tc_split_h_kernel<NT>, dim3(tiles), dim3(256), 0, stream, a);
+    err = launch_pdl(tc_split_h_kernel<NT>, dim3(tiles, NT / kSplitRows), dim3(256), 0, stream, a);
     if (err != cudaSuccess) return err;
     return launch_pdl(dn, dim3(a.H / kRows, tiles), dim3(kThreads), smem_dn, stream, a);
 }
@@ -883,8 +897,9 @@ cudaError_t launch_moe_ffn_tensor(const FfnArgs& f, cudaStream_t stream, const D
                                : launch_group_tokens(f.idx, S, f.k, f.E, f.counts, f.offsets, f.perm, f.active,
                                                      f.n_active, stream, dev);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(tc_tile_prefix_kernel, dim3(1), dim3(1024), 0, stream, (const int32_t*)f.counts, f.E, nt,
-                     f.tile_off, f.tile_off + f.E + 1);
+    err = launch_pdl(tc_tile_prefix_kernel, dim3(1), dim3(1024), 0, stream, (const int32_t*)f.counts,
+                     (const int32_t*)f.offsets, f.E, nt, f.tile_off,
+                     reinterpret_cast<int4*>(f.tile_off + ((f.E + 1 + 3) & ~3)));
     if (err != cudaSuccess) return err;
     TcArgs a;
     a.gate = f.gate;
@@ -905,7 +920,7 @@ cudaError_t launch_moe_ffn_tensor(const FfnArgs& f, cudaStream_t stream, const D
     a.offsets = f.offsets;
     a.perm = f.perm;
     a.tile_off = f.tile_off;
-    a.tile_e = f.tile_off + f.E + 1;
+    a.tile_info = reinterpret_cast<const int4*>(f.tile_off + ((f.E + 1 + 3) & ~3));
     a.xs = f.xs;
     a.hs = f.hs;
     a.xscale = f.xscale;

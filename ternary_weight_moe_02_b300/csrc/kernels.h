@@ -66,7 +66,8 @@ struct FfnArgs {
     int32_t* active;   // [E]
     int32_t* n_active; // [1]
     float* h;          // [T*k][I] (bf16 [T*k][I] on the tensor path)
-    int32_t* tile_off; // tensor path only: [E+1] tile prefix, then [max tiles] expert of each tile
+    int32_t* tile_off; // tensor path only: [E+1] tile prefix, then from the next 16-byte boundary
+                       // [max tiles] int4 tile records
     int32_t* chunks;   // grouping scratch of the tensor path
     uint8_t* xs;       // tensor path only: per tile, the tokens' x rows split into e4m3 hi/lo rows
     uint8_t* hs;       // tensor path only: per tile, the tokens' h rows split likewise

@@ -284,7 +284,7 @@ def test_integer_pack_unit_matches_the_oracle_packing():
     assert checked > 2500
 
 
-TC_ROWS, TC_KTILE, TC_LUT = 128, 160, 256 * 16 * 8
+TC_ROWS, TC_KTILE = 128, 160
 TC_A_STRIDE = 48
 TC_STATIC_SMEM = 1152  # largest static shared memory of the grouped kernels (ptxas -v)
 
@@ -299,18 +299,27 @@ def tc_shape_ok(H, I):
             and H <= 2080 and I <= 2080)
 
 
-def tc_stages(nt):
+def tc_a_stages(nt):
     return 3 if nt >= 128 else 4
 
 
+def tc_b_stages(nt):
+    return tc_a_stages(nt)  # one ring: a K tile's A and B stages are freed together
+
+
+def tc_lut(nt):
+    """256 entries x 16 copies x 8 bytes."""
+    return 256 * 16 * 8
+
+
 def tc_smem(row_bytes, nt):
-    stage_off = -(-(TC_LUT + TC_ROWS * row_bytes) // 128) * 128
-    return stage_off, stage_off + tc_stages(nt) * tc_stage_b(nt)
+    stage_off = -(-(tc_lut(nt) + TC_ROWS * row_bytes) // 128) * 128
+    return stage_off, stage_off + tc_b_stages(nt) * tc_stage_b(nt)
 
 
 def tc_tmem(nt):
     a_base = max(2 * nt, 32)
-    used = a_base + tc_stages(nt) * TC_A_STRIDE
+    used = a_base + tc_a_stages(nt) * TC_A_STRIDE
     return a_base, used, 256 if used <= 256 else 512
 
 
@@ -321,12 +330,13 @@ def test_tensor_path_plan_fits_and_is_aligned():
     B stage (5 MMAs of K = 32, 2NT/8 row groups at 128 B, 2 core-matrix columns at
     2NT * 16 B) inside the stage, and the tensor-memory columns (accumulator of 2NT
     columns, A stages of 40 columns at a 48-column stride, three or four stages) inside
-    the power-of-two allocation."""
+    the power-of-two allocation.  B stages (shared memory) follow the same ring: three
+    stages of 40 KB for 128-token tiles, four of 5 KB for 16-token tiles."""
     shapes = [(H, I) for H in range(128, 2081, 128) for I in range(128, 2081, 64)]
     for nt in (16, 128):
         a_base, used, alloc = tc_tmem(nt)
         assert 2 * nt <= a_base and a_base % 16 == 0
-        assert a_base + (tc_stages(nt) - 1) * TC_A_STRIDE + TC_KTILE // 4 <= used <= alloc
+        assert a_base + (tc_a_stages(nt) - 1) * TC_A_STRIDE + TC_KTILE // 4 <= used <= alloc
         assert alloc in (256, 512) and (nt == 16) == (alloc == 256)
         sb = tc_stage_b(nt)
         n = 2 * nt
@@ -347,8 +357,8 @@ def test_tensor_path_plan_fits_and_is_aligned():
                 K = H if rb == nbytes(H) else I
                 kt_last = -(-K // TC_KTILE) - 1
                 far = ((127 * rb + 32 * kt_last + 16) & ~3) + 20
-                assert TC_LUT + far <= total, (H, I, nt)
-                assert TC_LUT + epi <= total
+                assert tc_lut(nt) + far <= total, (H, I, nt)
+                assert tc_lut(nt) % 128 == 0 and tc_lut(nt) + epi <= total
                 size = rows_per_cta * rb
                 for e in (0, 1, 7):
                     for m0 in range(0, mtot, mstep):
@@ -448,3 +458,32 @@ def test_grouped_decode_table_matches_the_oracle_unpack():
                  perm(perm(en[2][0], en[2][1], 0x0432), en[3][0], 0x4210),
                  perm(en[3][0], en[3][1], 0x4321)]
         assert words == [word(flat[4 * i:4 * i + 4]) for i in range(5)]
+
+
+def test_grouped_decode_81_entry_table_matches_the_oracle_unpack():
+    """The 128-token tiles decode a byte c as c = low + 81 q4 with q4 = (c * 203) >> 14:
+    the first four trits from entry `low` of an 82-entry table (entry 81 all zero, taken
+    for the invalid codes 243..255), the fifth from q4 (byte q4 of 0x003800B8 as e4m3:
+    -1, 0, +1, and 0 for q4 = 3).  Every byte value against oracle.unpack."""
+    import oracle
+
+    e4m3_of = {-1: 0xB8, 0: 0x00, 1: 0x38}
+    table = []
+    for low in range(82):
+        vals = [0] * 4
+        if low < 81:
+            code = low
+            for t in range(4):
+                vals[t] = e4m3_of[code % 3 - 1]
+                code //= 3
+        table.append(vals)
+    for c in range(256):
+        q4 = (c * 203) >> 14
+        entry = 81 if c > 242 else c - 81 * q4
+        assert 0 <= entry < 82 and q4 <= 3
+        vals = table[entry] + [(0x003800B8 >> (8 * q4)) & 0xFF]
+        if c > 242:
+            assert vals == [0] * 5, c
+            continue
+        trits = oracle.unpack(np.array([[c]], np.uint8), 5)[0]
+        assert vals == [e4m3_of[int(t)] for t in trits], (c, vals, trits)
