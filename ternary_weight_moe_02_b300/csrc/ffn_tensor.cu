@@ -224,27 +224,41 @@ constexpr F8LutImage make_f8_lut_image() {
 __device__ __align__(16) const F8LutImage g_f8_lut_image = make_f8_lut_image();
 static_assert(sizeof(F8LutImage) == kLutBytes, "table image size");
 
-// Bytes [A, A + 16) of the packed rows (base 16-byte aligned) as four words, from five
-// aligned word loads and funnel shifts.  Reads up to 3 bytes past A + 16.
-__device__ __forceinline__ void load_bytes16(const uint8_t* base, uint32_t A, uint32_t* a) {
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(base + (A & ~3u));
+// Shared-memory loads at 32-bit shared addresses (the decode's operands always live
+// in shared memory; the explicit form keeps them off the generic path).
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+// Bytes [A, A + 16) of the packed rows (shared address base_s, 16-byte aligned) as four
+// words, from five aligned word loads and funnel shifts.  Reads up to 3 bytes past
+// A + 16.
+__device__ __forceinline__ void load_bytes16(uint32_t base_s, uint32_t A, uint32_t* a) {
+    const uint32_t w = base_s + (A & ~3u);
     const uint32_t sh = (A & 3u) * 8;
     uint32_t t[5];
 #pragma unroll
-    for (int i = 0; i < 5; ++i) t[i] = w[i];
+    for (int i = 0; i < 5; ++i) t[i] = lds32(w + 4 * i);
 #pragma unroll
     for (int i = 0; i < 4; ++i) a[i] = __funnelshift_r(t[i], t[i + 1], sh);
 }
 
 // Decodes bytes [b0, b0 + 16) of the row at byte offset row_off of the packed rows
-// (bytes at or past rb read as the all-zero code 121) into 20 words of four e4m3 each,
-// in K order: every four codes (twenty values) become five words by byte permutes of
-// their table entries.
+// (shared address packed_s; bytes at or past rb read as the all-zero code 121) into 20
+// words of four e4m3 each, in K order: every four codes (twenty values) become five
+// words by byte permutes of their table entries (lut_s: this lane's copy of entry 0).
 template <bool kTail>
-__device__ __forceinline__ void decode_half_tile_impl(const uint8_t* packed, uint32_t row_off, int rb, int b0,
-                                                      const uint2* lut_rep, uint32_t* words) {
+__device__ __forceinline__ void decode_half_tile_impl(uint32_t packed_s, uint32_t row_off, int rb, int b0,
+                                                      uint32_t lut_s, uint32_t* words) {
     uint32_t a[4];
-    load_bytes16(packed, row_off + (uint32_t)b0, a);
+    load_bytes16(packed_s, row_off + (uint32_t)b0, a);
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
         uint2 en[4];
@@ -252,7 +266,7 @@ __device__ __forceinline__ void decode_half_tile_impl(const uint8_t* packed, uin
         for (int i = 0; i < 4; ++i) {
             uint32_t c = (a[g] >> (8 * i)) & 0xFFu;
             if (kTail && b0 + 4 * g + i >= rb) c = 121u;
-            en[i] = lut_rep[c * kLutReps];
+            en[i] = lds64(lut_s + c * (kLutReps * 8));
         }
         words[5 * g + 0] = en[0].x;                                // values 0-3 of code 0
         words[5 * g + 1] = __byte_perm(en[0].y, en[1].x, 0x6540);  // 0.4, 1.0, 1.1, 1.2
@@ -263,13 +277,13 @@ __device__ __forceinline__ void decode_half_tile_impl(const uint8_t* packed, uin
 }
 
 // Bytes [32 kt + 16 h, +16) of a row: the masked variant only for the row's last tile.
-__device__ __forceinline__ void decode_half_tile(const uint8_t* packed, uint32_t row_off, int rb, int kt, int h,
-                                                 const uint2* lut_rep, uint32_t* words) {
+__device__ __forceinline__ void decode_half_tile(uint32_t packed_s, uint32_t row_off, int rb, int kt, int h,
+                                                 uint32_t lut_s, uint32_t* words) {
     const int b0 = 32 * kt + 16 * h;
     if (b0 + 16 <= rb)
-        decode_half_tile_impl<false>(packed, row_off, rb, b0, lut_rep, words);
+        decode_half_tile_impl<false>(packed_s, row_off, rb, b0, lut_s, words);
     else
-        decode_half_tile_impl<true>(packed, row_off, rb, b0, lut_rep, words);
+        decode_half_tile_impl<true>(packed_s, row_off, rb, b0, lut_s, words);
 }
 
 struct TcArgs {
@@ -338,55 +352,58 @@ struct TcBars {
     uint64_t packed;
 };
 
-// Warp-specialised main loop.  Warp w < 8 produces: its thread owns row 32 (w & 3) +
-// lane (the warp's TMEM lane quarter) and decodes half w >> 2 of that row's 32 bytes of
-// each K tile into A stage s (tensor memory), decoding the next K tile while the
-// current one's stores complete, then arrives on full[s]; thread 0 also copies the
-// stage's B block (this K tile's chunks of the tile's operand block bsrc, fewer at the
-// K tail) with one bulk copy onto bfull[s], the first S of them up front.  Warp 8 lane 0 waits for both, issues the
-// stage's five MMAs and commits empty[s]; its last commit goes to done.  Returns false
-// if a bounded wait gave up.
-template <int NT>
-__device__ bool tc_mainloop(unsigned char* smem, const uint8_t* packed, int rb, int Kdim, const uint8_t* bsrc,
-                            uint32_t tmem, TcBars& bars, int* status) {
+// Warp-specialised main loop over the K tiles of one accumulator.  Warp w < 8
+// produces: its thread owns row 32 (w & 3) + lane (the warp's TMEM lane quarter) and
+// decodes half w >> 2 of that row's 32 bytes of each K tile into A stage s (tensor
+// memory), decoding the next K tile while the current one's stores complete, then
+// arrives on full[s].  Warp 8 lane 0 waits for A and B, issues the tile's five MMAs and
+// commits empty[s], and after the last tile also done.  The ring position of K tile kt
+// is j0 + kt (a CTA that runs several accumulators in turn keeps counting); done is
+// waited for with parity done_parity.
+// B: either streamed through the ring (thread 0 copies K tile kt's chunks of the
+// operand block bsrc, fewer at the K tail, into the tile's ring stage with one bulk
+// copy, the first S up front), or, with kResidentB, already loaded whole: stage kt
+// holds K tile kt and has completed bfull[kt] once.
+// Returns false if a bounded wait gave up.
+template <int NT, bool kResidentB>
+__device__ bool tc_mainloop(const unsigned char* lut_smem, const uint8_t* packed, unsigned char* stages, int rb,
+                            int Kdim, const uint8_t* bsrc, uint32_t tmem, TcBars& bars, int* status, int j0,
+                            uint32_t done_parity) {
     using Cfg = TileCfg<NT>;
     constexpr int S = Cfg::kStages;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint2* lut_rep = reinterpret_cast<const uint2*>(smem) + (lane & (kLutReps - 1));
-    unsigned char* stages = smem + tc_stage_offset(rb);
+    const uint32_t lut_s = smem_addr(lut_smem) + 8u * (uint32_t)(lane & (kLutReps - 1));
+    const uint32_t packed_s = smem_addr(packed);
     const int KT = (Kdim + kKTile - 1) / kKTile;
     bool ok = true;
-    int issued = 0;  // B stages thread 0 has loaded
-    // B stage j: this K tile's chunks of the operand block (fewer at the K tail)
-    auto load_b = [&](int j) {
-        const int s = j % S;
-        const int left = Kdim / 16 - j * kChunks;
+    int issued = 0;  // K tiles whose B thread 0 has loaded
+    auto load_b = [&](int kt) {
+        const int s = (j0 + kt) % S;
+        const int left = Kdim / 16 - kt * kChunks;
         const uint32_t bytes = (uint32_t)((left < kChunks ? left : kChunks) * Cfg::kN * 16);
         mbar_arrive_expect_tx(&bars.bfull[s], bytes);
-        bulk_copy_g2s(stages + s * Cfg::kStageB, bsrc + (size_t)j * Cfg::kStageB, bytes, &bars.bfull[s]);
-        issued = j + 1;
+        bulk_copy_g2s(stages + s * Cfg::kStageB, bsrc + (size_t)kt * Cfg::kStageB, bytes, &bars.bfull[s]);
+        issued = kt + 1;
     };
     if (warp < kProducerWarps) {
         const int q = warp & 3, h = warp >> 2, r = 32 * q + lane;
         const uint32_t row_off = (uint32_t)(r * rb);
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
-        if (tid == 0)
-            for (int j = 0; j < S && j < KT; ++j) load_b(j);  // every stage starts free
+        if (!kResidentB && tid == 0)
+            for (int kt = 0; kt < S && kt < KT; ++kt) load_b(kt);  // every stage starts free
         uint32_t cur[20], nxt[20];
-        decode_half_tile(packed, row_off, rb, 0, h, lut_rep, cur);
-        for (int j = 0; j < KT && ok; ++j) {
-            const int s = j % S;
-            if (j >= S) {
-                if (!mbar_wait_bounded(&bars.empty[s], (uint32_t)(((j - S) / S) & 1), status)) {
-                    ok = false;
-                    break;
-                }
-                if (tid == 0) load_b(j);
+        decode_half_tile(packed_s, row_off, rb, 0, h, lut_s, cur);
+        for (int kt = 0; kt < KT && ok; ++kt) {
+            const int j = j0 + kt, s = j % S;
+            if (j >= S && !mbar_wait_bounded(&bars.empty[s], (uint32_t)(((j - S) / S) & 1), status)) {
+                ok = false;
+                break;
             }
+            if (!kResidentB && kt >= S && tid == 0) load_b(kt);
             const uint32_t col = (uint32_t)(Cfg::kABase + s * kAStride + 20 * h);
             tmem_st16(lane_base + col, cur);
             tmem_st4(lane_base + col + 16, cur + 16);
-            if (j + 1 < KT) decode_half_tile(packed, row_off, rb, j + 1, h, lut_rep, nxt);
+            if (kt + 1 < KT) decode_half_tile(packed_s, row_off, rb, kt + 1, h, lut_s, nxt);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             mbar_arrive(&bars.full[s]);
@@ -394,31 +411,34 @@ __device__ bool tc_mainloop(unsigned char* smem, const uint8_t* packed, int rb, 
             for (int i = 0; i < 20; ++i) cur[i] = nxt[i];
         }
     } else if (tid == kProducerWarps * 32) {
-        for (int j = 0; j < KT; ++j) {
-            const int s = j % S;
-            const uint32_t par = (uint32_t)((j / S) & 1);
-            if (!mbar_wait_bounded(&bars.full[s], par, status) || !mbar_wait_bounded(&bars.bfull[s], par, status)) {
+        for (int kt = 0; kt < KT; ++kt) {
+            const int j = j0 + kt, s = j % S;
+            const int sb = kResidentB ? kt : s;
+            const uint32_t bpar = kResidentB ? 0u : (uint32_t)((j / S) & 1);
+            if (!mbar_wait_bounded(&bars.full[s], (uint32_t)((j / S) & 1), status) ||
+                !mbar_wait_bounded(&bars.bfull[sb], bpar, status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const uint32_t a0 = tmem + (uint32_t)(Cfg::kABase + s * kAStride);
-            const uint32_t b0 = smem_addr(stages + s * Cfg::kStageB);
+            const uint32_t b0 = smem_addr(stages + sb * Cfg::kStageB);
 #pragma unroll
             for (int qk = 0; qk < kKTile / 32; ++qk) {
                 const uint64_t bd = smem_desc(b0 + qk * 2 * (Cfg::kN * 16), Cfg::kN * 16, 128);
-                mma_f8_tmem_a(tmem, a0 + 8 * qk, bd, Cfg::kIdesc, (j | qk) != 0 ? 1u : 0u);
+                mma_f8_tmem_a(tmem, a0 + 8 * qk, bd, Cfg::kIdesc, (kt | qk) != 0 ? 1u : 0u);
             }
-            mma_commit(j == KT - 1 ? &bars.done : &bars.empty[s]);
+            mma_commit(&bars.empty[s]);
+            if (kt == KT - 1) mma_commit(&bars.done);
         }
     }
     __syncwarp();
     // every thread waits for the last MMA (the epilogue reads TMEM and reuses shared memory)
-    if (ok && !mbar_wait_bounded(&bars.done, 0, status)) ok = false;
-    if (!ok && tid == 0) {
+    if (ok && !mbar_wait_bounded(&bars.done, done_parity, status)) ok = false;
+    if (!kResidentB && !ok && tid == 0) {
         // the last B load of each stage may still be in flight: let it land first
         for (int t = issued - S > 0 ? issued - S : 0; t < issued; ++t)
-            mbar_wait_bounded(&bars.bfull[t % S], (uint32_t)((t / S) & 1), nullptr);
+            mbar_wait_bounded(&bars.bfull[(j0 + t) % S], (uint32_t)(((j0 + t) / S) & 1), nullptr);
     }
     tc_fence_after();
     return !__syncthreads_or(!ok);
@@ -527,8 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gateup_kernel(TcArgs a) {
     pdl_launch_dependents();
     const float x_scale = tid < NT ? a.xscale[(size_t)tile * NT + tid] : 0.f;
     if (ok)
-        ok = tc_mainloop<NT>(smem, smem + tc_packed_offset(), Bh, H, a.xs + (size_t)tile * H * Cfg::kN, tmem, bars,
-                             a.status);
+        ok = tc_mainloop<NT, false>(smem, smem + tc_packed_offset(), smem + tc_stage_offset(Bh), Bh, H,
+                                    a.xs + (size_t)tile * H * Cfg::kN, tmem, bars, a.status, 0, 0u);
     if (tid < NT) s_xs[tid] = x_scale;
     __syncthreads();
     // Epilogue.  Warp w < 8 reads TMEM lanes 32 (w & 3) .. +31: rows j = 32 (w & 1) + lane
@@ -615,8 +635,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_down_kernel(TcArgs a) {
     pdl_launch_dependents();
     const float h_scale = tid < NT ? a.hscale[(size_t)tile * NT + tid] : 0.f;
     if (ok)
-        ok = tc_mainloop<NT>(smem, smem + tc_packed_offset(), Bi, I, a.hs + (size_t)tile * I * Cfg::kN, tmem, bars,
-                             a.status);
+        ok = tc_mainloop<NT, false>(smem, smem + tc_packed_offset(), smem + tc_stage_offset(Bi), Bi, I,
+                                    a.hs + (size_t)tile * I * Cfg::kN, tmem, bars, a.status, 0, 0u);
     if (tid < NT) {
         s_slot[tid] = slot;
         s_w[tid] = w_slot * h_scale;
@@ -637,6 +657,148 @@ __global__ void __launch_bounds__(kThreads, 1) tc_down_kernel(TcArgs a) {
             const int tok = CW * (warp >> 2) + i;
             if (tok < nv) yr[(int64_t)s_slot[tok] * H] = s_w[tok] * (row_scale * v[i]);
         }
+    }
+    tc_release(tmem, Cfg::kTmemCols);
+}
+
+// Down for 16-token tiles whose whole h operand fits the B stages (K tiles <= stages):
+// grid (ceil(H / 128 / kDownBlocks), max tiles); the CTA computes kDownBlocks
+// consecutive 128-row blocks of down rows in turn.  The decode table, TMEM and the
+// barriers are set up once, the tile's h operand is loaded once and stays in shared
+// memory, and each block's packed rows (two buffers) are copied while the blocks
+// before it compute.  The A ring keeps counting across blocks.
+constexpr int kDownBlocks = 4;
+
+__host__ __device__ constexpr size_t tc_multi_packed_bytes(int row_bytes) {
+    return ((size_t)kRows * row_bytes + 127) / 128 * 128;
+}
+template <int NT>
+__host__ __device__ constexpr size_t tc_multi_smem_bytes(int row_bytes) {
+    return (size_t)kLutBytes + 2 * tc_multi_packed_bytes(row_bytes) + (size_t)TileCfg<NT>::kStages * TileCfg<NT>::kStageB;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 2) tc_down_multi_kernel(TcArgs a) {
+    using Cfg = TileCfg<NT>;
+    constexpr int CW = NT / 2;
+    constexpr int CB = CW < 32 ? CW : 32;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ TcBars bars;
+    __shared__ uint64_t pk[2];  // packed-row buffers
+    __shared__ uint32_t tmem_slot;
+    __shared__ int s_slot[NT];
+    __shared__ float s_w[NT];   // routing weight of the slot, times its h split scale
+    int e, n0, nv, pos0;
+    if (!tc_tile<NT>(a, blockIdx.y, e, n0, nv, pos0)) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.H, I = a.I, Bi = (I + 4) / 5;
+    const int tile = blockIdx.y;
+    const int KT = (I + kKTile - 1) / kKTile;  // at most Cfg::kStages (host check)
+    const int blk0 = blockIdx.x * kDownBlocks;
+    const int nblk = H / kRows - blk0 < kDownBlocks ? H / kRows - blk0 : kDownBlocks;
+    const uint32_t pbytes = (uint32_t)(kRows * Bi);
+    unsigned char* pkbuf[2] = {smem + kLutBytes, smem + kLutBytes + tc_multi_packed_bytes(Bi)};
+    unsigned char* stages = smem + kLutBytes + 2 * tc_multi_packed_bytes(Bi);
+    const uint8_t* dsrc = a.down + ((int64_t)e * H + (int64_t)blk0 * kRows) * Bi;  // block b at + b * pbytes
+    // loads whose first use is the epilogue
+    int slot = 0;
+    float w_slot = 0.f;
+    if (tid < nv) {
+        slot = __ldcg(a.perm + pos0 + tid);
+        w_slot = __ldcg(a.w + slot);
+    }
+    // prologue: decode table and the first two blocks' packed rows, barriers, the
+    // never-copied K tail of the last B stage zeroed, TMEM
+    int pk_last[2] = {-1, -1};  // (thread 0) last block copied into each buffer
+    if (tid == 0) {
+        mbar_init(&bars.packed, 1);
+        mbar_arrive_expect_tx(&bars.packed, (uint32_t)kLutBytes);
+        bulk_copy_g2s(smem, &g_f8_lut_image, (uint32_t)kLutBytes, &bars.packed);
+        mbar_init(&pk[0], 1);
+        mbar_init(&pk[1], 1);
+        for (int b = 0; b < 2 && b < nblk; ++b) {
+            mbar_arrive_expect_tx(&pk[b], pbytes);
+            bulk_copy_g2s(pkbuf[b], dsrc + (size_t)b * pbytes, pbytes, &pk[b]);
+            pk_last[b] = b;
+        }
+        for (int i = 0; i < kMaxStages; ++i) {
+            mbar_init(&bars.full[i], kProducerWarps * 32);
+            mbar_init(&bars.bfull[i], 1);
+            mbar_init(&bars.empty[i], 1);
+        }
+        mbar_init(&bars.done, 1);
+    }
+    const int left = I / 16 - (KT - 1) * kChunks;  // chunks of the last K tile
+    if (left < kChunks) {
+        uint4* z = reinterpret_cast<uint4*>(stages + (size_t)(KT - 1) * Cfg::kStageB + (size_t)left * Cfg::kN * 16);
+        for (int i = tid; i < (kChunks - left) * Cfg::kN; i += blockDim.x) z[i] = make_uint4(0u, 0u, 0u, 0u);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == kProducerWarps) tmem_alloc(&tmem_slot, Cfg::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    bool ok = !__syncthreads_or(!mbar_wait_bounded(&bars.packed, 0, a.status));
+    const uint32_t tmem = tmem_slot;
+    pdl_wait();  // the split h of the previous kernel
+    pdl_launch_dependents();
+    // the tile's whole h operand, one bulk copy per K tile
+    const uint8_t* bsrc = a.hs + (size_t)tile * I * Cfg::kN;
+    if (tid == 0) {
+        for (int kt = 0; kt < KT; ++kt) {
+            const int l = I / 16 - kt * kChunks;
+            const uint32_t bytes = (uint32_t)((l < kChunks ? l : kChunks) * Cfg::kN * 16);
+            mbar_arrive_expect_tx(&bars.bfull[kt], bytes);
+            bulk_copy_g2s(stages + (size_t)kt * Cfg::kStageB, bsrc + (size_t)kt * Cfg::kStageB, bytes, &bars.bfull[kt]);
+        }
+    }
+    const float h_scale = tid < NT ? a.hscale[(size_t)tile * NT + tid] : 0.f;
+    if (tid < NT) {
+        s_slot[tid] = slot;
+        s_w[tid] = w_slot * h_scale;
+    }
+    __syncthreads();
+    int b = 0;
+    for (; b < nblk && ok; ++b) {
+        const int m0 = (blk0 + b) * kRows;
+        const float row_scale =
+            warp < kProducerWarps ? a.s_down[(int64_t)e * H + m0 + 32 * (warp & 3) + lane] : 0.f;
+        ok = !__syncthreads_or(!mbar_wait_bounded(&pk[b & 1], (uint32_t)((b >> 1) & 1), a.status));
+        if (ok)
+            ok = tc_mainloop<NT, true>(smem, pkbuf[b & 1], stages, Bi, I, bsrc, tmem, bars, a.status, b * KT,
+                                       (uint32_t)(b & 1));
+        if (!ok) break;
+        // block b's packed rows are consumed (its last MMA is done): refill the buffer
+        if (tid == 0 && b + 2 < nblk) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive_expect_tx(&pk[b & 1], pbytes);
+            bulk_copy_g2s(pkbuf[b & 1], dsrc + (size_t)(b + 2) * pbytes, pbytes, &pk[b & 1]);
+            pk_last[b & 1] = b + 2;
+        }
+        // epilogue as in tc_down_kernel
+        if (warp < kProducerWarps) {
+            const int q = warp & 3, r = 32 * q + lane;
+            const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
+            float* yr = a.ys + m0 + r;
+            float v[CW];
+#pragma unroll
+            for (int cb = 0; cb < CW; cb += CB) tmem_ld_sum<NT, CB>(lane_addr, CW * (warp >> 2) + cb, v + cb);
+#pragma unroll
+            for (int i = 0; i < CW; ++i) {
+                const int tok = CW * (warp >> 2) + i;
+                if (tok < nv) yr[(int64_t)s_slot[tok] * H] = s_w[tok] * (row_scale * v[i]);
+            }
+        }
+        // the accumulator is drained before the next block's MMAs
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    if (!ok && tid == 0) {
+        // copies that may still be in flight land before the CTA leaves
+        for (int kt = 0; kt < KT; ++kt) mbar_wait_bounded(&bars.bfull[kt], 0, nullptr);
+        for (int x = 0; x < 2; ++x)
+            if (pk_last[x] >= b) mbar_wait_bounded(&pk[x], (uint32_t)((pk_last[x] >> 1) & 1), nullptr);
     }
     tc_release(tmem, Cfg::kTmemCols);
 }
@@ -870,9 +1032,14 @@ template <int NT>
 cudaError_t launch_tc_ffn(const TcArgs& a, int S, cudaStream_t stream) {
     const int tiles = ffn_tensor_max_tiles(S, a.E);
     const int Bh = (a.H + 4) / 5, Bi = (a.I + 4) / 5;
-    const size_t smem_gu = tc_smem_bytes<NT>(Bh), smem_dn = tc_smem_bytes<NT>(Bi);
+    // 16-token tiles whose whole h operand fits the B stages take the multi-block down
+    constexpr bool kSmallTile = NT == 16;
+    const bool multi = kSmallTile && (a.I + kKTile - 1) / kKTile <= TileCfg<NT>::kStages;
+    const size_t smem_gu = tc_smem_bytes<NT>(Bh);
+    const size_t smem_dn = multi ? tc_multi_smem_bytes<NT>(Bi) : tc_smem_bytes<NT>(Bi);
     auto gu = tc_gateup_kernel<NT>;
-    auto dn = tc_down_kernel<NT>;
+    auto dn = multi ? tc_down_multi_kernel<16> : tc_down_kernel<NT>;
+    const dim3 dn_grid(multi ? (a.H / kRows + kDownBlocks - 1) / kDownBlocks : a.H / kRows, tiles);
     cudaError_t err = ensure_dynamic_smem(gu, smem_gu);
     if (err != cudaSuccess) return err;
     err = ensure_dynamic_smem(dn, smem_dn);
@@ -883,7 +1050,7 @@ cudaError_t launch_tc_ffn(const TcArgs& a, int S, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     err = launch_pdl(tc_split_h_kernel<NT>, dim3(tiles, NT / kSplitRows), dim3(256), 0, stream, a);
     if (err != cudaSuccess) return err;
-    return launch_pdl(dn, dim3(a.H / kRows, tiles), dim3(kThreads), smem_dn, stream, a);
+    return launch_pdl(dn, dn_grid, dim3(kThreads), smem_dn, stream, a);
 }
 
 }  // namespace

@@ -487,3 +487,28 @@ def test_grouped_decode_81_entry_table_matches_the_oracle_unpack():
             continue
         trits = oracle.unpack(np.array([[c]], np.uint8), 5)[0]
         assert vals == [e4m3_of[int(t)] for t in trits], (c, vals, trits)
+
+
+def test_multi_block_down_plan_fits_and_is_aligned():
+    """The down kernel for 16-token tiles whose whole h operand fits the B stages (K tiles
+    of 160 values <= 4, i.e. I <= 640) walks 4 consecutive 128-row blocks: the decode
+    table, two packed-row buffers (rounded to 128 B) and four 5 KB B stages must fit two
+    CTAs per SM, and every block's packed-row copy (128 rows of ceil(I/5) bytes) must be
+    16-byte aligned and inside the expert's down matrix."""
+    nt, blocks = 16, 4
+    for H in range(128, 2081, 128):
+        for I in range(128, 641, 64):
+            if not tc_shape_ok(H, I):
+                continue
+            rb = nbytes(I)
+            assert -(-I // TC_KTILE) <= tc_a_stages(nt)
+            pk = -(-(TC_ROWS * rb) // 128) * 128
+            total = tc_lut(nt) + 2 * pk + tc_a_stages(nt) * tc_stage_b(nt)
+            assert 2 * (total + TC_STATIC_SMEM + 1024) <= 233472, (H, I, total)
+            nblk_all = H // TC_ROWS
+            for e in (0, 3):
+                for bx in range(-(-nblk_all // blocks)):
+                    blk0 = bx * blocks
+                    for b in range(min(blocks, nblk_all - blk0)):
+                        off = (e * H + (blk0 + b) * TC_ROWS) * rb
+                        _check(off, TC_ROWS * rb, (e + 1) * H * rb, f"multi down H={H} I={I}")
