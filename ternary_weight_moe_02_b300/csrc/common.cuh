@@ -404,14 +404,15 @@ __device__ __forceinline__ void down_group_partials(int k, int I, int Bi, const 
     }
 }
 
-// Raise a kernel's dynamic shared-memory limit when it needs more than the default
-// 48 KB.  The attribute is per device; the last size set per (kernel, device) is
-// remembered so that steady-state launches make no extra driver call.
-// Raises a kernel's dynamic shared-memory limit once per (kernel, device).  The cache
-// is keyed by the kernel's address: template instances share a function type.
+// Raises a kernel's dynamic shared-memory limit to `bytes`.  The attribute is per
+// device; the last size set per (kernel, device) is remembered, keyed by the kernel's
+// address (template instances share a function type), so that steady-state launches
+// make no extra driver call.
 template <typename Kernel>
 cudaError_t ensure_dynamic_smem(Kernel* kernel, size_t bytes) {
-    if (bytes <= 48 * 1024) return cudaSuccess;
+    // static and dynamic shared memory together may exceed the 48 KB default even when
+    // the dynamic part alone does not: opt in for any dynamic size
+    if (bytes == 0) return cudaSuccess;
     struct Entry {
         const void* fn;
         int dev;

@@ -512,3 +512,4 @@ def test_multi_block_down_plan_fits_and_is_aligned():
                     for b in range(min(blocks, nblk_all - blk0)):
                         off = (e * H + (blk0 + b) * TC_ROWS) * rb
                         _check(off, TC_ROWS * rb, (e + 1) * H * rb, f"multi down H={H} I={I}")
+
