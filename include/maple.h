@@ -157,6 +157,12 @@ MAPLE_API size_t maple_moe_ffn_workspace_size(int32_t T, int32_t k, const maple_
  * ("Maple-Preview ...", section "The shipped code does no quantization": the
  * MapleMLP forward with its clamps; "IA de 20B ...", section "Pesos ternarios":
  * skip / add / subtract.)
+ * Two internal paths give results within the same bound: with at least half as many
+ * slots as experts (2*T*k >= E) and H a multiple of 128, I of 64, both in [128, 2080],
+ * the sums run on the tensor cores (fp8 MMAs on trits and on exact two-part splits of
+ * the bf16 activations; h is rounded to bf16 between the two projections); otherwise
+ * on CUDA cores with fp32 h.  The environment variable MAPLE_FFN_PATH = tensor or
+ * cores forces one (when the shape allows it); the workspace size follows the choice.
  *   ex  : expert weights (see maple_experts)
  *   x   : [T][H] bf16, 16-byte aligned
  *   idx : [T][k] int32 (ids outside [0, E) contribute 0)   w : [T][k] fp32

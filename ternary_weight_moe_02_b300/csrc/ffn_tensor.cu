@@ -33,10 +33,11 @@
 // stage at (k / 16) * (2NT * 16) + n * 16 + k % 16.  The split kernels store each
 // tile's rows in global memory in that order ([K / 16][2NT][16] bytes), so a K tile's
 // B stage is one contiguous block loaded by one 1-D bulk copy.  K tiles hold 160 values
-// (32 packed bytes per row).  Eight producer warps fill a ring of four stages; one
-// thread issues five tcgen05.mma.kind::f8f6f4 (K = 32 each) per stage and commits them
-// to the stage's "empty" mbarrier, which the producers wait for before refilling the
-// stage.  All waits are bounded.
+// (32 packed bytes per row).  Eight producer warps fill a ring of stages (three for
+// 128-token tiles, four for 16-token tiles); one thread issues five
+// tcgen05.mma.kind::f8f6f4 (K = 32 each) per stage and commits them to the stage's
+// "empty" mbarrier, which the producers wait for before refilling the stage.  All waits
+// are bounded.
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdlib.h>
