@@ -133,6 +133,12 @@ def _max_over_ranks(v: float, world: int) -> float:
     return float(t.item())
 
 
+def _job_rate(units_per_rank: float, elapsed_s: float, world: int) -> float:
+    """Whole-job rate of `world` replicas that each processed units_per_rank units:
+    all units over the slowest rank's time (every rank gets the same value)."""
+    return world * units_per_rank / _max_over_ranks(elapsed_s, world)
+
+
 # ----------------------------------------------------------------------------- inputs
 
 def sources_sha256(paths) -> str:
@@ -256,7 +262,7 @@ def run_gpu(args, world, rank, local):
         _barrier(world)
     elapsed_s = ev0.elapsed_time(ev1) / 1e3
     elapsed_max = _max_over_ranks(elapsed_s, world)
-    value = world * args.steps / elapsed_max
+    value = _job_rate(args.steps, elapsed_s, world)
     launches = args.steps * 1  # moe_layer_b1_kernel: the whole step in one launch
 
     # The same steps through the two separate calls (route_topk, moe_ffn: 4 launches).
@@ -320,8 +326,7 @@ def run_gpu(args, world, rank, local):
             y_host.copy_(y, non_blocking=True)
         e1.record(stream)
     e1.synchronize()
-    e2e_s = _max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
-    e2e_value = world * n_e2e / e2e_s
+    e2e_value = _job_rate(n_e2e, e0.elapsed_time(e1) / 1e3, world)
 
     legs = tuple(args.legs.split(",")) if args.legs else SECONDARY_LEGS
     secondary = run_secondary(maple, synth, layers, dev, stream, legs) if args.secondary else None
