@@ -1000,6 +1000,9 @@ int ffn_tensor_max_tiles(int S, int E) {
 // as experts (on the Maple layer, 16 tokens and up).
 bool ffn_use_tensor(int T, int k, int E, int H, int I) {
     if (!ffn_tensor_shape_ok(H, I) || T < 1) return false;
+    // the grouped kernels put the tiles in gridDim.y (at most 65535); beyond that (more
+    // than about 8.3 million slots) the CUDA-core kernels run
+    if (ffn_tensor_max_tiles(T * k, E) > 65535) return false;
     const char* env = getenv("MAPLE_FFN_PATH");
     if (env != nullptr && strcmp(env, "tensor") == 0) return true;
     if (env != nullptr && strcmp(env, "cores") == 0) return false;

@@ -176,10 +176,11 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-cudaError_t launch_route_topk(const uint16_t* x, const uint16_t* Wr, const float* bias, int T,
-                              int H, int E, int k, float* logits, int32_t* idx, float* w,
-                              cudaStream_t stream, const DeviceInfo& dev) {
-    (void)dev;
+namespace {
+
+// One launch of each route kernel for at most kRouteChunk tokens.
+cudaError_t launch_route_chunk(const uint16_t* x, const uint16_t* Wr, const float* bias, int T, int H, int E,
+                               int k, float* logits, int32_t* idx, float* w, cudaStream_t stream) {
     const int vec = (H % 8 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
                     (reinterpret_cast<uintptr_t>(Wr) % 16 == 0);
     cudaError_t err;
@@ -202,6 +203,26 @@ cudaError_t launch_route_topk(const uint16_t* x, const uint16_t* Wr, const float
     if (E <= 256) return launch_pdl(route_select_kernel<8>, g2, dim3(256), 0, stream, cl, T, E, k, idx, w);
     if (E <= 512) return launch_pdl(route_select_kernel<16>, g2, dim3(256), 0, stream, cl, T, E, k, idx, w);
     return launch_pdl(route_select_kernel<32>, g2, dim3(256), 0, stream, cl, T, E, k, idx, w);
+}
+
+}  // namespace
+
+// The logits kernels put T / 8 token groups in gridDim.y (at most 65535): larger calls
+// run in chunks of kRouteChunk tokens (each token's logits are the same either way).
+cudaError_t launch_route_topk(const uint16_t* x, const uint16_t* Wr, const float* bias, int T,
+                              int H, int E, int k, float* logits, int32_t* idx, float* w,
+                              cudaStream_t stream, const DeviceInfo& dev) {
+    (void)dev;
+    constexpr int kRouteChunk = 65535 * 8;
+    int t0 = 0;
+    do {
+        const int n = T - t0 < kRouteChunk ? T - t0 : kRouteChunk;
+        const cudaError_t err = launch_route_chunk(x + (int64_t)t0 * H, Wr, bias, n, H, E, k, logits + (int64_t)t0 * E,
+                                                   idx + (int64_t)t0 * k, w + (int64_t)t0 * k, stream);
+        if (err != cudaSuccess) return err;
+        t0 += n;
+    } while (t0 < T);
+    return cudaSuccess;
 }
 
 }  // namespace maple
