@@ -362,13 +362,32 @@ def run_gpu(args, world, rank, local):
 
 # ------------------------------------------------------------- secondary workloads
 
-SECONDARY_LEGS = ("decode_b8", "decode_b64", "prefill_4096", "ternarize_pack")
+SECONDARY_LEGS = ("decode_b8", "decode_b32", "decode_b64", "prefill_4096", "ternarize_pack")
+
+
+def expert_bytes(H: int, I: int) -> int:
+    """Packed rows and fp32 scales of one expert: gate and up [I][ceil(H/5)], down
+    [H][ceil(I/5)], scales 2I + H (643,072 B at the Maple shape)."""
+    return 2 * I * ((H + 4) // 5) + H * ((I + 4) // 5) + 4 * (2 * I + H)
+
+
+def distinct_expert_bytes(idx_per_layer, E: int, H: int, I: int) -> int:
+    """Bytes of the distinct experts each layer's routing touches, summed over layers
+    (ids outside [0, E) touch nothing)."""
+    total = 0
+    for idx in idx_per_layer:
+        ids = idx.reshape(-1)
+        ids = ids[(ids >= 0) & (ids < E)]
+        total += int(torch.unique(ids).numel()) * expert_bytes(H, I)
+    return total
 
 
 def run_secondary(maple, synth, layers, dev, stream, legs=SECONDARY_LEGS):
     """Other configurations of the same path, measured briefly (not the headline):
-    decode batches over 24 stacked layers with a N(0,0.5) router bias, the 4096-token
-    prefill with a Zipf(1.1) bias, and ternarize + pack throughput on whole layers."""
+    decode batches of 8, 32 and 64 tokens over 24 stacked layers with a N(0,0.5) router
+    bias (with the packed-weight rate over the distinct experts each layer touches), the
+    4096-token prefill with a Zipf(1.1) bias, and ternarize + pack throughput on whole
+    layers."""
     out = {}
     n_stack = min(24, len(layers))
 
@@ -390,7 +409,7 @@ def run_secondary(maple, synth, layers, dev, stream, legs=SECONDARY_LEGS):
         b.synchronize()
         return a.elapsed_time(b) / 1e3 / (reps * n_steps)
 
-    for T in (8, 64):
+    for T in (8, 32, 64):
         if f"decode_b{T}" not in legs:
             continue
         xs = [synth.tokens(T, H, seed=100 + l, device=dev) for l in range(n_stack)]
@@ -407,8 +426,18 @@ def run_secondary(maple, synth, layers, dev, stream, legs=SECONDARY_LEGS):
             maple.maple_moe_layer(xs[i % n_stack], router, biases[i % n_stack], ex, K_TOP, logits, idx,
                                   w, y, ws, stream=stream)
         sec = timed_graph(layer, n_stack)
+        # the experts each layer's routing touches (routed again, outside the timed graph)
+        idx_layers = []
+        with torch.cuda.stream(stream):
+            for i in range(n_stack):
+                maple.maple_route_topk(xs[i], layers[i][1], biases[i], K_TOP, logits, idx, w, stream=stream)
+                idx_layers.append(idx.clone())
+        stream.synchronize()
+        packed = distinct_expert_bytes(idx_layers, E, H, I) / n_stack
         out[f"decode_b{T}"] = {"value": T / sec, "unit": "tokens/s", "ms_per_layer": sec * 1e3,
-                               "layers": n_stack, "bias": "N(0, 0.5) per expert"}
+                               "layers": n_stack, "bias": "N(0, 0.5) per expert",
+                               "distinct_expert_mb_per_layer": packed / 1e6,
+                               "packed_weight_gbs": packed / sec / 1e9}
 
     if "prefill_4096" not in legs and "ternarize_pack" not in legs:
         return out
