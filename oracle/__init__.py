@@ -5,7 +5,7 @@ of the benchmark may import this package; the product library never does.  The C
 source (``maple_oracle.c``) shares no code with the CUDA library.
 
 Passages each function follows are cited in the C source; in short:
-  * ternarize / pack / unpack -- "Maple-Preview: a 20B reasoning model where 97% of
+  * ternarize / ternary_exact / pack / unpack -- "Maple-Preview: a 20B reasoning model where 97% of
     the weights are -1, 0, or +1", sections "The claim, verified from the bytes" and
     "The 5.31 GB claim reconciles";
   * route -- same page, "The claim, verified from the bytes" (router kept in full
@@ -53,6 +53,7 @@ def _load():
             P = ctypes.c_void_p
             I64 = ctypes.c_int64
             lib.oracle_ternarize.argtypes = [P, I64, I64, P, P]
+            lib.oracle_ternary_exact.argtypes = [P, I64, I64, P, P, P]
             lib.oracle_pack.argtypes = [P, I64, I64, P]
             lib.oracle_unpack.argtypes = [P, I64, I64, P]
             lib.oracle_route.argtypes = [P, P, P, I64, I64, I64, I64, P, P, P]
@@ -61,7 +62,7 @@ def _load():
                                            P, P, P, I64, I64, P]
             lib.oracle_packed_row_bytes.argtypes = [I64]
             lib.oracle_packed_row_bytes.restype = I64
-            for name in ("oracle_ternarize", "oracle_pack", "oracle_unpack", "oracle_route",
+            for name in ("oracle_ternarize", "oracle_ternary_exact", "oracle_pack", "oracle_unpack", "oracle_route",
                          "oracle_group", "oracle_moe_ffn"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
@@ -100,6 +101,20 @@ def ternarize(w_bits: np.ndarray):
     if st != OK:
         raise OracleError(st, "ternarize")
     return q, s
+
+
+def ternary_exact(w_bits: np.ndarray):
+    """bf16 bits [rows, K] of already-ternary rows -> (trits int8 [rows, K] = sign(w),
+    scales fp32 [rows] = max|w|, number of rows that are not ternary)."""
+    w = _bf16_bits(w_bits)
+    rows, K = w.shape
+    q = np.empty((rows, K), np.int8)
+    s = np.empty(rows, np.float32)
+    bad = np.zeros(1, np.int64)
+    st = _load().oracle_ternary_exact(_ptr(w), rows, K, _ptr(q), _ptr(s), _ptr(bad))
+    if st != OK:
+        raise OracleError(st, "ternary_exact")
+    return q, s, int(bad[0])
 
 
 def pack(q: np.ndarray) -> np.ndarray:

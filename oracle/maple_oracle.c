@@ -87,6 +87,40 @@ int oracle_ternarize(const uint16_t* w, int64_t rows, int64_t K, int8_t* q, floa
 }
 
 /*
+ * Trits and scales of a matrix whose rows are already ternary.  The released
+ * checkpoint stores each expert weight as a bf16 value -s, 0 or +s of its row ("The
+ * claim, verified from the bytes": exactly three values per row), so the row's scale
+ * is its largest magnitude and each trit is the sign of its weight:
+ * s_r = max_j |w_rj| and q_rj = sign(w_rj) (0 for +0 and -0).  A row with two different
+ * nonzero magnitudes is not ternary: it is counted in *bad_rows and still gets the
+ * sign trits and the max scale.
+ */
+int oracle_ternary_exact(const uint16_t* w, int64_t rows, int64_t K, int8_t* q, float* s, int64_t* bad_rows) {
+    if (!w || !q || !s || !bad_rows || rows < 0 || K <= 0) return ORACLE_BAD_ARG;
+    *bad_rows = 0;
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t* wr = w + r * K;
+        double m = 0.0;
+        for (int64_t j = 0; j < K; ++j) {
+            double a = fabs(bf16_bits_to_double(wr[j]));
+            if (a > m) m = a;
+        }
+        int bad = 0;
+        for (int64_t j = 0; j < K; ++j) {
+            double v = bf16_bits_to_double(wr[j]);
+            int8_t t = 0;
+            if (v > 0.0) t = 1;
+            if (v < 0.0) t = -1;
+            if (t != 0 && fabs(v) != m) bad = 1;
+            q[r * K + j] = t;
+        }
+        s[r] = (float)m; /* a bf16 magnitude: exact in fp32 */
+        *bad_rows += bad;
+    }
+    return ORACLE_OK;
+}
+
+/*
  * Five trits per byte ("The 5.31 GB claim reconciles": 3^5 = 243 fits in 256).
  * byte = sum_{i=0..4} (q_{5b+i} + 1) * 3^i; missing tail trits count as 0.
  */

@@ -118,6 +118,55 @@ def test_ternarize_golden_examples():
         np.testing.assert_array_equal(q[0], [int(v) for v in qtxt.split()])
 
 
+def test_ternary_exact_golden_examples():
+    """Hand-worked already-ternary rows ("The claim, verified from the bytes")."""
+    for wtxt, stxt, qtxt, flag in _read_fixture("ternary_exact_examples.txt"):
+        w = [float(v) for v in wtxt.split()]
+        bits = _f32_bits_to_bf16_bits(w).reshape(1, -1)
+        q, s, bad = oracle.ternary_exact(bits)
+        assert s[0] == np.float32(float(stxt))
+        np.testing.assert_array_equal(q[0], [int(v) for v in qtxt.split()])
+        assert bad == int(flag)
+
+
+def test_ternary_exact_recovers_constructed_rows_and_relates_to_absmean():
+    """Rows built as a_r * q_r (q random trits with a random zero share, a a bf16
+    magnitude) come back as exactly q and a, none flagged.  Absmean ternarization of
+    the same rows gives the same trits and the scale (1 - z_r) a_r, z_r the row's zero
+    fraction (mean |w| over a row of a and 0 values)."""
+    rng = np.random.default_rng(5)
+    rows, K = 64, 517
+    q = rng.choice([-1, 0, 1], size=(rows, K), p=[0.3, 0.4, 0.3]).astype(np.int8)
+    q[3] = 0                   # an all-zero row: s = 0
+    q[4] = 0
+    q[4, 100] = -1             # a single nonzero weight
+    a = torch.tensor(rng.uniform(0.001, 2.0, rows), dtype=torch.float32).to(torch.bfloat16).float().numpy()
+    w = (a[:, None] * q).astype(np.float32)  # products of a bf16 value and +-1 / 0: bf16-exact
+    bits = _f32_bits_to_bf16_bits(w.reshape(-1)).reshape(rows, K)
+    qe, se, bad = oracle.ternary_exact(bits)
+    np.testing.assert_array_equal(qe, q)
+    expect_s = np.where(np.any(q != 0, axis=1), a, 0.0).astype(np.float32)
+    np.testing.assert_array_equal(se, expect_s)
+    assert bad == 0
+    np.testing.assert_array_equal(oracle.pack(qe), oracle.pack(q))
+    qa, sa = oracle.ternarize(bits)
+    np.testing.assert_array_equal(qa, q)
+    z = (q == 0).mean(axis=1)
+    np.testing.assert_allclose(sa, (1 - z) * expect_s, rtol=1e-6)
+
+
+def test_ternary_exact_flags_a_row_one_ulp_off():
+    """One nonzero magnitude moved by one bf16 ulp makes its row not ternary; sign trits
+    and the max scale stay."""
+    w = np.array([[0.5, -0.5, 0.0, 0.5], [0.5, -0.5, 0.0, 0.5]], np.float32)
+    bits = _f32_bits_to_bf16_bits(w.reshape(-1)).reshape(2, 4)
+    bits[1, 3] += 1  # 0.5 -> 0.50390625
+    q, s, bad = oracle.ternary_exact(bits)
+    assert bad == 1
+    np.testing.assert_array_equal(q, [[1, -1, 0, 1], [1, -1, 0, 1]])
+    assert s[0] == np.float32(0.5) and s[1] == np.float32(0.50390625)
+
+
 def test_ternarize_invariants_gaussian():
     """Three symmetric values per row, all present; closed-form scale and zero share."""
     rows, K, std = 256, 2048, 0.02
