@@ -362,7 +362,7 @@ def run_gpu(args, world, rank, local):
 
 # ------------------------------------------------------------- secondary workloads
 
-SECONDARY_LEGS = ("decode_b8", "decode_b32", "decode_b64", "prefill_4096", "ternarize_pack")
+SECONDARY_LEGS = ("decode_b8", "decode_b32", "decode_b64", "prefill_4096", "ternarize_pack", "pack_ternary")
 
 
 def expert_bytes(H: int, I: int) -> int:
@@ -386,8 +386,8 @@ def run_secondary(maple, synth, layers, dev, stream, legs=SECONDARY_LEGS):
     """Other configurations of the same path, measured briefly (not the headline):
     decode batches of 8, 32 and 64 tokens over 24 stacked layers with a N(0,0.5) router
     bias (with the packed-weight rate over the distinct experts each layer touches), the
-    4096-token prefill with a Zipf(1.1) bias, and ternarize + pack throughput on whole
-    layers."""
+    4096-token prefill with a Zipf(1.1) bias, ternarize + pack throughput on whole
+    layers, and (after it, on its output) the packing of already-ternary matrices."""
     out = {}
     n_stack = min(24, len(layers))
 
@@ -485,6 +485,34 @@ def run_secondary(maple, synth, layers, dev, stream, legs=SECONDARY_LEGS):
                              "ms_per_layer": sec * 1e3, "bytes_per_layer": bytes_moved,
                              "weights_per_layer": weights, "peak_source": f"{kind} hbm_gbs"}
     del wts
+    if "pack_ternary" not in legs:
+        return out
+
+    # packing of already-ternary bf16 matrices (a whole layer, as a released checkpoint
+    # stores them): the trits of the pack leg times each row's scale rounded to bf16
+    tern = {}
+    with torch.cuda.stream(stream):
+        for name, K in (("gate", H), ("up", H), ("down", I)):
+            f32 = torch.empty((pk[name].shape[0], K), device=dev)
+            maple.maple_unpack(pk[name], sc[name], K, f32, stream=stream)
+            tern[name] = f32.to(torch.bfloat16)
+            del f32
+    stream.synchronize()
+    pk2 = {name: torch.empty_like(t) for name, t in pk.items()}
+    sc2 = {name: torch.empty_like(t) for name, t in sc.items()}
+    bad = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def pack_ternary(i):
+        for name in ("gate", "up", "down"):
+            maple.maple_pack_ternary(tern[name], pk2[name], sc2[name], bad, stream=stream)
+    sec = timed_graph(pack_ternary, 1, reps=3)
+    same = all(torch.equal(pk2[name], pk[name]) for name in pk)
+    out["pack_ternary"] = {"value": bytes_moved / sec / 1e9, "unit": "GB/s",
+                           "frac_of_peak": bytes_moved / sec / 1e9 / peak,
+                           "ms_per_layer": sec * 1e3, "bytes_per_layer": bytes_moved,
+                           "non_ternary_rows": int(bad.item()), "bytes_equal_absmean_pack": same,
+                           "peak_source": f"{kind} hbm_gbs"}
+    del tern, pk2, sc2
     return out
 
 

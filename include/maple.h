@@ -105,6 +105,26 @@ MAPLE_API int maple_ternarize_pack(const uint16_t* W, int64_t rows, int64_t K, u
                          float* scales, void* stream);
 
 /*
+ * 5-trit packing of a bf16 row-major matrix W [rows x K] whose rows are already
+ * ternary, such as the expert weights of the released bf16 checkpoint, where each
+ * weight is -s, 0 or +s of its row.  Per row: s = max_j |w_j| (exact in fp32) and
+ * q_j = sign(w_j) (0 for +0 and -0), packed as by maple_ternarize_pack.  (Absmean
+ * ternarization of such a row gives the same trits but the scale (1 - z) s, z the
+ * row's share of zeros.)  ("Maple-Preview ...", section "The claim, verified from the
+ * bytes": exactly three values per row; "The 5.31 GB claim reconciles": five trits
+ * per byte.)
+ *   W        : [rows][K] bf16, finite, 2-byte aligned
+ *   packed   : [rows][ceil(K/5)] bytes, written
+ *   scales   : [rows] fp32, written
+ *   bad_rows : optional device int32 counter; the kernel adds the number of rows with
+ *              two different nonzero magnitudes (not ternary: they are still packed
+ *              with sign trits and the max scale).  May be NULL.
+ * Limits: rows >= 0 (0 is a no-op), 1 <= K <= 2^24.
+ */
+MAPLE_API int maple_pack_ternary(const uint16_t* W, int64_t rows, int64_t K, uint8_t* packed, float* scales,
+                                 int32_t* bad_rows, void* stream);
+
+/*
  * Dequantize packed rows back to fp32: W_out[r][j] = q_rj * s_r (inverse of the
  * packing above; a test and inspection helper, not on the hot path).
  *   packed : [rows][ceil(K/5)], scales : [rows], W_out : [rows][K] fp32 (written)

@@ -134,6 +134,21 @@ int maple_ternarize_pack(const uint16_t* W, int64_t rows, int64_t K, uint8_t* pa
     return ok();
 }
 
+int maple_pack_ternary(const uint16_t* W, int64_t rows, int64_t K, uint8_t* packed, float* scales,
+                       int32_t* bad_rows, void* stream) {
+    if (rows < 0 || K < 1) return fail(MAPLE_ERR_INVALID_ARG, "pack_ternary: rows=%lld K=%lld", (long long)rows, (long long)K);
+    if (K > (int64_t(1) << 24)) return fail(MAPLE_ERR_UNSUPPORTED_SHAPE, "pack_ternary: K=%lld > 2^24", (long long)K);
+    if (rows == 0) return ok();
+    if (!W || !packed || !scales) return fail(MAPLE_ERR_INVALID_ARG, "pack_ternary: null pointer");
+    if (!aligned(W, 2) || !aligned(scales, 4) || !aligned(bad_rows, 4))
+        return fail(MAPLE_ERR_MISALIGNED, "pack_ternary: W needs 2-byte, scales and bad_rows 4-byte alignment");
+    maple::DeviceInfo dev;
+    if (int st = get_device(&dev, "pack_ternary")) return st;
+    cudaError_t err = maple::launch_pack_ternary(W, rows, K, packed, scales, bad_rows, (cudaStream_t)stream, dev);
+    if (err != cudaSuccess) return cuda_fail(err, "pack_ternary launch");
+    return ok();
+}
+
 int maple_unpack(const uint8_t* packed, const float* scales, int64_t rows, int64_t K,
                  float* W_out, int32_t* bad_codes, void* stream) {
     if (rows < 0 || K < 1) return fail(MAPLE_ERR_INVALID_ARG, "unpack: rows=%lld K=%lld", (long long)rows, (long long)K);

@@ -24,6 +24,14 @@ cudaError_t device_info(DeviceInfo* info);
 cudaError_t launch_ternarize_pack(const uint16_t* W, int64_t rows, int64_t K, uint8_t* packed,
                                   float* scales, cudaStream_t stream, const DeviceInfo& dev);
 
+cudaError_t launch_pack_ternary(const uint16_t* W, int64_t rows, int64_t K, uint8_t* packed, float* scales,
+                                int32_t* bad_rows, cudaStream_t stream, const DeviceInfo& dev);
+// The staged pack kernel in its already-ternary form; *taken is false (and nothing is
+// launched) when the shape does not take the staged path.
+cudaError_t launch_pack_exact_staged(const uint16_t* W, int64_t rows, int64_t K, uint8_t* packed,
+                                     float* scales, int32_t* bad_rows, cudaStream_t stream, const DeviceInfo& dev,
+                                     bool* taken);
+
 cudaError_t launch_unpack(const uint8_t* packed, const float* scales, int64_t rows, int64_t K,
                           float* W_out, int32_t* bad_codes, cudaStream_t stream,
                           const DeviceInfo& dev);

@@ -166,6 +166,31 @@ __device__ __forceinline__ float group_row_abs_sum(const uint4* r4, int n4, int 
     return v;
 }
 
+// Largest and smallest nonzero magnitude (bf16 bits; 0x7fff when there is none) over
+// a row slot, as every lane of the row's G-lane group sees them (j: the lane's index
+// in the group).  Non-negative finite bf16 values order like their bit patterns.
+template <int G>
+__device__ __forceinline__ void group_row_mag_range(const uint4* r4, int n4, int j, uint32_t& mx, uint32_t& mn) {
+    uint32_t hi = 0u, lo = 0x7fffu;
+    for (int c = j; c < n4; c += G) {
+        const uint4 v = r4[c];
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t a = w4[i] & 0x7fffu, b = (w4[i] >> 16) & 0x7fffu;
+            hi = max(hi, max(a, b));
+            lo = min(lo, min(a != 0u ? a : 0x7fffu, b != 0u ? b : 0x7fffu));
+        }
+    }
+#pragma unroll
+    for (int o = G / 2; o >= 1; o >>= 1) {
+        hi = max(hi, __shfl_xor_sync(kFullMask, hi, o));
+        lo = min(lo, __shfl_xor_sync(kFullMask, lo, o));
+    }
+    mx = hi;
+    mn = lo;
+}
+
 // Packs the units j, j + G, ... of one row slot (two per loop trip).
 template <int G, bool kPairStores>
 __device__ __forceinline__ void group_pack_row(const uint32_t* row32, int units, int nb, int j,
@@ -188,10 +213,14 @@ __device__ __forceinline__ void group_pack_row(const uint32_t* row32, int units,
     if (u < units) store(u, pack_unit(row32 + 5 * u, c2));
 }
 
-template <int G, bool kPairStores>
+// kExact: the rows are already ternary (-s, 0, +s each): s = the largest magnitude,
+// trits = signs (the packing threshold is 0), and rows with two different nonzero
+// magnitudes are counted in *bad_rows (may be null).  Otherwise absmean.
+template <int G, bool kPairStores, bool kExact>
 __global__ void __launch_bounds__(kPkMaxWarps * 32)
     ternarize_pack_tma_kernel(const uint16_t* __restrict__ W, int64_t rows, int K,
-                              uint8_t* __restrict__ packed, float* __restrict__ scales, int* status) {
+                              uint8_t* __restrict__ packed, float* __restrict__ scales, int* status,
+                              int32_t* __restrict__ bad_rows) {
     constexpr int R = 32 / G;  // rows per block
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ __align__(8) uint64_t bars[kPkMaxWarps][2];
@@ -248,14 +277,28 @@ __global__ void __launch_bounds__(kPkMaxWarps * 32)
         // a group whose row is past the end (last block) sums its stale slot harmlessly
         // and stores nothing
         const unsigned char* rowp = stage0 + st * stagebytes + q * slot;
-        const float total = group_row_abs_sum<G>(reinterpret_cast<const uint4*>(rowp), K >> 3, j);
-        if (r < rows) {
-            const float s = __fdiv_rn(total, (float)K);
-            const uint32_t t16 = (__float_as_uint(0.5f * s) >> 16) & 0x7fffu;
-            const uint32_t c2 = (0x7fffu - t16) * 0x10001u;
-            group_pack_row<G, kPairStores>(reinterpret_cast<const uint32_t*>(rowp), units, nb, j, c2,
-                                           packed + r * nb);
-            if (j == 0) scales[r] = s;
+        if constexpr (kExact) {
+            uint32_t mx, mn;
+            group_row_mag_range<G>(reinterpret_cast<const uint4*>(rowp), K >> 3, j, mx, mn);
+            if (r < rows) {
+                // threshold 0: every nonzero magnitude gives the sign trit
+                group_pack_row<G, kPairStores>(reinterpret_cast<const uint32_t*>(rowp), units, nb, j,
+                                               0x7fffu * 0x10001u, packed + r * nb);
+                if (j == 0) {
+                    scales[r] = __uint_as_float(mx << 16);
+                    if (bad_rows != nullptr && mx != 0u && mn != mx) atomicAdd(bad_rows, 1);
+                }
+            }
+        } else {
+            const float total = group_row_abs_sum<G>(reinterpret_cast<const uint4*>(rowp), K >> 3, j);
+            if (r < rows) {
+                const float s = __fdiv_rn(total, (float)K);
+                const uint32_t t16 = (__float_as_uint(0.5f * s) >> 16) & 0x7fffu;
+                const uint32_t c2 = (0x7fffu - t16) * 0x10001u;
+                group_pack_row<G, kPairStores>(reinterpret_cast<const uint32_t*>(rowp), units, nb, j, c2,
+                                               packed + r * nb);
+                if (j == 0) scales[r] = s;
+            }
         }
         __syncwarp();  // every lane is done with this stage before it is refilled
         st ^= 1;
@@ -267,11 +310,11 @@ __global__ void __launch_bounds__(kPkMaxWarps * 32)
     }
 }
 
-template <int G, bool kPairStores>
+template <int G, bool kPairStores, bool kExact>
 cudaError_t launch_pack_tma(const uint16_t* W, int64_t rows, int K, uint8_t* packed, float* scales,
-                            int warps, cudaStream_t stream, const DeviceInfo& dev) {
+                            int32_t* bad_rows, int warps, cudaStream_t stream, const DeviceInfo& dev) {
     constexpr int R = 32 / G;
-    auto kernel = ternarize_pack_tma_kernel<G, kPairStores>;
+    auto kernel = ternarize_pack_tma_kernel<G, kPairStores, kExact>;
     const size_t smem = (size_t)warps * 2 * R * (2 * (size_t)K + kPkPad);
     cudaError_t err = ensure_dynamic_smem(kernel, smem);
     if (err != cudaSuccess) return err;
@@ -284,16 +327,44 @@ cudaError_t launch_pack_tma(const uint16_t* W, int64_t rows, int K, uint8_t* pac
     const int64_t cap = (int64_t)dev.sm_count * per_sm;
     const int grid = (int)(want < cap ? want : cap);
     return launch_pdl(kernel, dim3(grid), dim3(warps * 32), smem, stream, W, rows, K, packed, scales,
-                      dev.status);
+                      dev.status, bad_rows);
 }
 
-template <int G>
+template <int G, bool kExact>
 cudaError_t launch_pack_tma_g(const uint16_t* W, int64_t rows, int K, uint8_t* packed, float* scales,
-                              int warps, cudaStream_t stream, const DeviceInfo& dev) {
+                              int32_t* bad_rows, int warps, cudaStream_t stream, const DeviceInfo& dev) {
     const int nb = (K + 4) / 5;
     if (nb % 2 == 0 && reinterpret_cast<uintptr_t>(packed) % 2 == 0)
-        return launch_pack_tma<G, true>(W, rows, K, packed, scales, warps, stream, dev);
-    return launch_pack_tma<G, false>(W, rows, K, packed, scales, warps, stream, dev);
+        return launch_pack_tma<G, true, kExact>(W, rows, K, packed, scales, bad_rows, warps, stream, dev);
+    return launch_pack_tma<G, false, kExact>(W, rows, K, packed, scales, bad_rows, warps, stream, dev);
+}
+
+// The staged path (bulk copies of row blocks into shared memory) for W 16-byte aligned
+// and K a multiple of 8 up to kPkMaxK: rows per block R, the largest power of two <= 32
+// whose block is at most ~4 KB, and warps per CTA.  False when the shape does not take it.
+bool pack_staged_plan(const uint16_t* W, int64_t K, const DeviceInfo& dev, int& R, int& warps) {
+    const bool vec = (K % 8 == 0) && (reinterpret_cast<uintptr_t>(W) % 16 == 0);
+    if (!vec || K > kPkMaxK) return false;
+    const int rowbytes = 2 * (int)K;
+    R = 1;
+    while (R < 32 && 2 * R * rowbytes <= kPkStageBytes) R *= 2;
+    const size_t per_warp = (size_t)2 * R * (rowbytes + kPkPad);  // two stages
+    warps = (int)((dev.smem_optin - 1024) / per_warp);
+    warps = warps > kPkMaxWarps ? kPkMaxWarps : warps;
+    return warps >= 1;
+}
+
+template <bool kExact>
+cudaError_t launch_pack_staged(const uint16_t* W, int64_t rows, int64_t K, uint8_t* packed, float* scales,
+                               int32_t* bad_rows, int R, int warps, cudaStream_t stream, const DeviceInfo& dev) {
+    switch (R) {
+        case 1: return launch_pack_tma_g<32, kExact>(W, rows, (int)K, packed, scales, bad_rows, warps, stream, dev);
+        case 2: return launch_pack_tma_g<16, kExact>(W, rows, (int)K, packed, scales, bad_rows, warps, stream, dev);
+        case 4: return launch_pack_tma_g<8, kExact>(W, rows, (int)K, packed, scales, bad_rows, warps, stream, dev);
+        case 8: return launch_pack_tma_g<4, kExact>(W, rows, (int)K, packed, scales, bad_rows, warps, stream, dev);
+        case 16: return launch_pack_tma_g<2, kExact>(W, rows, (int)K, packed, scales, bad_rows, warps, stream, dev);
+        default: return launch_pack_tma_g<1, kExact>(W, rows, (int)K, packed, scales, bad_rows, warps, stream, dev);
+    }
 }
 
 __global__ void __launch_bounds__(256)
@@ -328,30 +399,23 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_ternarize_pack(const uint16_t* W, int64_t rows, int64_t K, uint8_t* packed,
                                   float* scales, cudaStream_t stream, const DeviceInfo& dev) {
     const int vec = (K % 8 == 0) && (reinterpret_cast<uintptr_t>(W) % 16 == 0);
-    if (vec && K <= kPkMaxK) {
-        // rows per block: the largest power of two <= 32 whose block is at most ~4 KB
-        const int rowbytes = 2 * (int)K;
-        int R = 1;
-        while (R < 32 && 2 * R * rowbytes <= kPkStageBytes) R *= 2;
-        const size_t per_warp = (size_t)2 * R * (rowbytes + kPkPad);  // two stages
-        int warps = (int)((dev.smem_optin - 1024) / per_warp);
-        warps = warps > kPkMaxWarps ? kPkMaxWarps : warps;
-        if (warps >= 1) {
-            switch (R) {
-                case 1: return launch_pack_tma_g<32>(W, rows, (int)K, packed, scales, warps, stream, dev);
-                case 2: return launch_pack_tma_g<16>(W, rows, (int)K, packed, scales, warps, stream, dev);
-                case 4: return launch_pack_tma_g<8>(W, rows, (int)K, packed, scales, warps, stream, dev);
-                case 8: return launch_pack_tma_g<4>(W, rows, (int)K, packed, scales, warps, stream, dev);
-                case 16: return launch_pack_tma_g<2>(W, rows, (int)K, packed, scales, warps, stream, dev);
-                default: return launch_pack_tma_g<1>(W, rows, (int)K, packed, scales, warps, stream, dev);
-            }
-        }
-    }
+    int R = 0, warps = 0;
+    if (pack_staged_plan(W, K, dev, R, warps))
+        return launch_pack_staged<false>(W, rows, K, packed, scales, nullptr, R, warps, stream, dev);
     const int64_t want = (rows + 7) / 8;
     const int64_t cap = (int64_t)dev.sm_count * 8;
     const int grid = (int)(want < cap ? want : cap);
     return launch_pdl(ternarize_pack_kernel, dim3(grid), dim3(256), 0, stream, W, rows, K, packed,
                       scales, vec);
+}
+
+cudaError_t launch_pack_exact_staged(const uint16_t* W, int64_t rows, int64_t K, uint8_t* packed,
+                                     float* scales, int32_t* bad_rows, cudaStream_t stream, const DeviceInfo& dev,
+                                     bool* taken) {
+    int R = 0, warps = 0;
+    *taken = pack_staged_plan(W, K, dev, R, warps);
+    if (!*taken) return cudaSuccess;
+    return launch_pack_staged<true>(W, rows, K, packed, scales, bad_rows, R, warps, stream, dev);
 }
 
 cudaError_t launch_unpack(const uint8_t* packed, const float* scales, int64_t rows, int64_t K,

@@ -31,7 +31,7 @@ MAPLE_ERR_BAD_CODE = -6
 MAPLE_ERR_WORKSPACE = -7
 
 EXPORTED = ("maple_version", "maple_status_string", "maple_last_error",
-            "maple_check_device_status", "maple_ternarize_pack",
+            "maple_check_device_status", "maple_ternarize_pack", "maple_pack_ternary",
             "maple_unpack", "maple_route_topk", "maple_group_tokens",
             "maple_moe_ffn_workspace_size", "maple_moe_ffn", "maple_moe_layer_workspace_size",
             "maple_moe_layer", "maple_moe_ffn_static_scratch")
@@ -55,6 +55,7 @@ _lib.maple_check_device_status.argtypes = [_P]
 _lib.maple_check_device_status.restype = ctypes.c_int
 _lib.maple_ternarize_pack.argtypes = [_P, _I64, _I64, _P, _P, _P]
 _lib.maple_unpack.argtypes = [_P, _P, _I64, _I64, _P, _P, _P]
+_lib.maple_pack_ternary.argtypes = [_P, _I64, _I64, _P, _P, _P, _P]
 _lib.maple_route_topk.argtypes = [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P]
 _lib.maple_group_tokens.argtypes = [_P, _I32, _I32, _I32, _P, _P, _P, _P]
 _lib.maple_moe_ffn_workspace_size.argtypes = [_I32, _I32, ctypes.POINTER(maple_experts)]
@@ -144,6 +145,20 @@ def maple_ternarize_pack(W, packed, scales, stream=None):
     _expect(scales, torch.float32, (rows,), "scales")
     _check(_lib.maple_ternarize_pack(_ptr(W), rows, K, _ptr(packed), _ptr(scales), _stream(stream)),
            "maple_ternarize_pack")
+
+
+def maple_pack_ternary(W, packed, scales, bad_rows=None, stream=None):
+    """W bf16 [rows, K] with already-ternary rows -> packed uint8 [rows, ceil(K/5)],
+    scales fp32 [rows] = max|w|; bad_rows: optional int32 [1] counter of rows that are
+    not ternary (added to)."""
+    rows, K = W.shape
+    _expect(W, torch.bfloat16, (rows, K), "W")
+    _expect(packed, torch.uint8, (rows, packed_row_bytes(K)), "packed")
+    _expect(scales, torch.float32, (rows,), "scales")
+    if bad_rows is not None:
+        _expect(bad_rows, torch.int32, (1,), "bad_rows")
+    _check(_lib.maple_pack_ternary(_ptr(W), rows, K, _ptr(packed), _ptr(scales), _ptr(bad_rows),
+                                   _stream(stream)), "maple_pack_ternary")
 
 
 def maple_unpack(packed, scales, K, W_out, bad_codes=None, stream=None):
