@@ -1,5 +1,5 @@
 """Host-side arithmetic of bench.py's decode legs (CPU): the bytes of one expert and of
-the distinct experts a layer's routing touches, against SURVEY-style hand counts
+the distinct experts a layer's routing touches, against hand counts
 ("Maple-Preview ...", section "The 5.31 GB claim reconciles": five trits per byte)."""
 import os
 import sys

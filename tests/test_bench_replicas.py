@@ -20,7 +20,7 @@ import torch.multiprocessing as mp
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 pytestmark = pytest.mark.skipif(torch.cuda.is_available(),
-                                reason="exercises the CPU (gloo) set-up; on a GPU box the ranks take NCCL")
+                                reason="exercises the CPU (gloo) set-up; with a GPU visible the ranks take NCCL")
 
 
 def _free_port() -> int:
