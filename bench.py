@@ -3,10 +3,11 @@
 
 Workload (the metric's configuration): hidden 2048, 256 experts, top-8, no shared
 expert, intermediate 512; ternary experts packed 5 trits/byte with fp32 row scales;
-bf16 router [256 x 2048]; one bf16 N(0,1) token per step.  One step = route_topk +
-moe_ffn for one token on one layer.  Steps cycle over 1000 distinct seeded tokens and
-over LAYERS independently seeded layers (10.5 GB packed), so a layer's experts are
-far out of L2 when it comes round again (inputs larger than L2, no flush).
+bf16 router [256 x 2048]; one bf16 N(0,1) token per step.  One step = route + expert
+FFN of one token on one layer (one maple_moe_layer call).  The timed steps walk over
+1000 distinct seeded tokens and LAYERS independently seeded layers (10.5 GB packed) in
+order, so a layer is revisited only after 63 others (inputs larger than L2); every
+timed graph is replayed once untimed first and L2 is flushed before the timed region.
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle instead, on a
 bounded sample of the same workload.  Under torchrun with N > 1 every rank runs an
@@ -32,6 +33,8 @@ sys.path.insert(0, ROOT)
 H, E, I, K_TOP = 2048, 256, 512, 8
 N_TOKENS = 1000
 LAYERS = 64
+L2_FLUSH_BYTES = 256 << 20  # twice the B300's 126 MB L2
+LAUNCHES_PER_STEP = 1       # maple_moe_layer at T = 1: one launch of the fused kernel
 METRIC = "ternary MoE layer tokens/s (batch 1 & 64 decode); packed-weight HBM GB/s vs peak"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
 # the batch-1 layer kernel and the device helpers it is built from
@@ -222,28 +225,41 @@ def run_gpu(args, world, rank, local):
         maple.maple_route_topk(x, router, None, K_TOP, logits, idx, wts, stream=s)
         maple.maple_moe_ffn(ex, x, idx, wts, y, ws_ffn, stream=s)
 
-    chunk = max(1, min(args.chunk, args.steps))
+    # The timed steps are one continuous walk i = 0 .. K-1 over layers i % n_layers and
+    # tokens i % N_TOKENS.  Graphs of `chunk` steps (a multiple of n_layers when K is
+    # larger, so that back-to-back replays continue the walk seamlessly) are replayed.
+    K = args.steps
+    chunk = K if K <= args.chunk else max(n_layers, args.chunk // n_layers * n_layers)
+    reps, rem = divmod(K, chunk)
+    l2_flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def capture(n_steps, start):
+    def flush():
+        # writes a buffer twice the size of L2: no layer data stays cached
+        l2_flush.zero_()
+
+    def capture(n_steps, start, fn=step):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             for i in range(3):  # warm the launch path before capture
-                step(start + i, stream)
+                fn(start + i, stream)
             stream.synchronize()
             with torch.cuda.graph(g, stream=stream):
                 for i in range(n_steps):
-                    step(start + i, stream)
+                    fn(start + i, stream)
         return g
 
     g_chunk = capture(chunk, 0)
-    rem = args.steps % chunk
     g_rem = capture(rem, 0) if rem else None
-    g_warm = capture(max(1, args.warmup), 0)
-    reps = args.steps // chunk
-
-    # graphs replay on the current stream: make it the one the events are recorded on
+    # warm-up on steps the timed walk does not start with (layers from the middle of the
+    # cycle), then one untimed replay of every timed graph (its first launch and upload),
+    # then an L2 flush: the timed region starts cold
+    g_warm = capture(args.warmup, K + n_layers // 2)
     with torch.cuda.stream(stream):
         g_warm.replay()
+        g_chunk.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        flush()
     torch.cuda.synchronize()
     _barrier(world)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -262,20 +278,16 @@ def run_gpu(args, world, rank, local):
         _barrier(world)
     elapsed_s = ev0.elapsed_time(ev1) / 1e3
     elapsed_max = _max_over_ranks(elapsed_s, world)
-    value = _job_rate(args.steps, elapsed_s, world)
-    launches = args.steps * 1  # moe_layer_b1_kernel: the whole step in one launch
+    value = _job_rate(K, elapsed_s, world)
+    launches = K * LAUNCHES_PER_STEP
 
-    # The same steps through the two separate calls (route_topk, moe_ffn: 4 launches).
-    n_two = min(args.steps, chunk)
-    g_two = torch.cuda.CUDAGraph()
+    # The same steps through the two separate calls (route_topk, moe_ffn), from a flushed
+    # L2 after one untimed replay.
+    n_two = min(K, chunk)
+    g_two = capture(n_two, 0, step_two_calls)
     with torch.cuda.stream(stream):
-        for i in range(3):
-            step_two_calls(i, stream)
-        stream.synchronize()
-        with torch.cuda.graph(g_two, stream=stream):
-            for i in range(n_two):
-                step_two_calls(i, stream)
         g_two.replay()
+        flush()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         g_two.replay()
@@ -283,9 +295,10 @@ def run_gpu(args, world, rank, local):
     t1.synchronize()
     two_call_value = n_two / (t0.elapsed_time(t1) / 1e3)
 
-    # Roofline pass: the same steps with events around each moe_ffn call (graph-captured),
-    # giving the live average duration of the dominant launch pair.
-    n_roof = min(args.steps, 2000)
+    # Roofline pass: the same walk with graph-captured events around each step's launch
+    # (the events are graph nodes of their own, so each launch runs alone), from a
+    # flushed L2, giving the live average duration of the dominant launch.
+    n_roof = min(K, 2000)
     pairs = [(torch.cuda.Event(enable_timing=True, external=True),
               torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n_roof)]
     g_roof = torch.cuda.CUDAGraph()
@@ -294,6 +307,7 @@ def run_gpu(args, world, rank, local):
             for i in range(n_roof):
                 step(i, stream, pairs[i])
     with torch.cuda.stream(stream):
+        flush()
         g_roof.replay()
     torch.cuda.synchronize()
     ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
@@ -303,33 +317,39 @@ def run_gpu(args, world, rank, local):
     alg_bytes = packed_bytes + E * H * 2 + H * 2 + H * 4 + E * 4 + K_TOP * 8
     achieved = alg_bytes / (ffn_ms / 1e3) / 1e9
 
-    # End-to-end through the public API with host buffers: pinned token -> device, route,
-    # FFN, y -> pinned host, every step.
-    n_e2e = min(args.steps, 2000)
+    # End-to-end through the public API with host buffers: every step, maple_moe_layer_host
+    # copies the step's token from pinned host memory, runs the layer and copies y back
+    # into pinned host memory.  The calls are bound (arguments checked and marshalled)
+    # before the timed region; the loop makes one C call per step.
+    n_e2e = min(K, 2000)
     x_host = x_all[:N_TOKENS].cpu().pin_memory()
     y_host = torch.empty((1, H), dtype=torch.float32).pin_memory()
     x_dev = torch.empty((1, H), dtype=torch.bfloat16, device=dev)
-    torch.cuda.synchronize()
+
+    def bound(i):
+        ex, router = layers[i % n_layers]
+        t = i % N_TOKENS
+        return maple.bind_moe_layer_host(x_host[t:t + 1], x_dev, router, None, ex, K_TOP, logits, idx, wts, y,
+                                         y_host, ws, stream=stream)
+    warm_calls = [bound(K + i) for i in range(3)]
+    calls = [bound(i) for i in range(n_e2e)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        for i in range(3):
-            x_dev.copy_(x_host[i:i + 1], non_blocking=True)
-            ex, router = layers[i % n_layers]
-            maple.maple_moe_layer(x_dev, router, None, ex, K_TOP, logits, idx, wts, y, ws, stream=stream)
-            y_host.copy_(y, non_blocking=True)
+        for c in warm_calls:
+            c()
+        flush()
         stream.synchronize()
         e0.record(stream)
-        for i in range(n_e2e):
-            x_dev.copy_(x_host[i % N_TOKENS: i % N_TOKENS + 1], non_blocking=True)
-            ex, router = layers[i % n_layers]
-            maple.maple_moe_layer(x_dev, router, None, ex, K_TOP, logits, idx, wts, y, ws, stream=stream)
-            y_host.copy_(y, non_blocking=True)
+        for c in calls:
+            c()
         e1.record(stream)
     e1.synchronize()
     e2e_value = _job_rate(n_e2e, e0.elapsed_time(e1) / 1e3, world)
 
     legs = tuple(args.legs.split(",")) if args.legs else SECONDARY_LEGS
-    secondary = run_secondary(maple, synth, layers, dev, stream, legs) if args.secondary else None
+    secondary = (run_secondary(maple, synth, layers, dev, stream, legs, flush=flush,
+                               cpu=(rank == 0 and world == 1 and args.cpu_tokens > 0))
+                 if args.secondary else None)
 
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -340,8 +360,10 @@ def run_gpu(args, world, rank, local):
                    "top_k": K_TOP, "moe_intermediate": I, "tokens_per_step": 1,
                    "distinct_tokens": N_TOKENS, "layers_cycled": n_layers,
                    "packed_gb": round(n_layers * E * EXPERT_BYTES / 1e9, 2),
-                   "l2": "inputs larger than L2 (layers cycled; no flush)",
-                   "graph": f"CUDA graph of {chunk} steps replayed", "parallelism": f"replicas{world}"},
+                   "l2": "inputs larger than L2 (64 layers walked in order, a layer revisited "
+                         "only after 63 others); L2 flushed before the timed region",
+                   "graph": f"CUDA graph of {chunk} steps, replayed once untimed first",
+                   "parallelism": f"replicas{world}"},
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "kernel": "moe_layer_b1_kernel (whole step, one launch)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -352,7 +374,8 @@ def run_gpu(args, world, rank, local):
         "two_call_path": {"value": two_call_value, "unit": "tokens/s",
                           "calls": "maple_route_topk + maple_moe_ffn (4 launches per step)"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "steps": n_e2e,
-                "h2d_bytes_per_step": H * 2, "d2h_bytes_per_step": H * 4},
+                "h2d_bytes_per_step": H * 2, "d2h_bytes_per_step": H * 4,
+                "call": "maple_moe_layer_host (token in from pinned host memory, y out to it)"},
         "clocks": clocks.summary(),
     }
     if secondary is not None:
@@ -362,7 +385,9 @@ def run_gpu(args, world, rank, local):
 
 # ------------------------------------------------------------- secondary workloads
 
-SECONDARY_LEGS = ("decode_b8", "decode_b32", "decode_b64", "prefill_4096", "ternarize_pack", "pack_ternary")
+SECONDARY_LEGS = ("decode_b1", "decode_b8", "decode_b32", "decode_b64", "prefill_4096", "ternarize_pack",
+                  "pack_ternary")
+DECODE_BATCHES = (1, 8, 32, 64)
 
 
 def expert_bytes(H: int, I: int) -> int:
@@ -382,12 +407,15 @@ def distinct_expert_bytes(idx_per_layer, E: int, H: int, I: int) -> int:
     return total
 
 
-def run_secondary(maple, synth, layers, dev, stream, legs=SECONDARY_LEGS):
+def run_secondary(maple, synth, layers, dev, stream, legs=SECONDARY_LEGS, flush=None, cpu=True):
     """Other configurations of the same path, measured briefly (not the headline):
-    decode batches of 8, 32 and 64 tokens over 24 stacked layers with a N(0,0.5) router
-    bias (with the packed-weight rate over the distinct experts each layer touches), the
-    4096-token prefill with a Zipf(1.1) bias, ternarize + pack throughput on whole
-    layers, and (after it, on its output) the packing of already-ternary matrices."""
+    decode batches of 1, 8, 32 and 64 tokens over 24 stacked layers with a N(0,0.5)
+    router bias (with the packed-weight rate over the distinct experts each layer
+    touches), the 4096-token prefill with a Zipf(1.1) bias, ternarize + pack throughput
+    on whole layers, and (after it, on its output) the packing of already-ternary
+    matrices.  Each timed graph replay starts from a flushed L2 (the flush is outside
+    the events).  With cpu=True each leg also carries the oracle's figure on a bounded
+    sample of the same workload (single-threaded, the sample stated)."""
     out = {}
     n_stack = min(24, len(layers))
 
@@ -401,15 +429,18 @@ def run_secondary(maple, synth, layers, dev, stream, legs=SECONDARY_LEGS):
                 for i in range(n_steps):
                     fn(i)
             g.replay()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(reps):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(reps)]
+            for a, b in evs:
+                if flush is not None:
+                    flush()
+                a.record(stream)
                 g.replay()
-            b.record(stream)
-        b.synchronize()
-        return a.elapsed_time(b) / 1e3 / (reps * n_steps)
+                b.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / 1e3 / (reps * n_steps)
 
-    for T in (8, 32, 64):
+    for T in DECODE_BATCHES:
         if f"decode_b{T}" not in legs:
             continue
         xs = [synth.tokens(T, H, seed=100 + l, device=dev) for l in range(n_stack)]
@@ -434,10 +465,13 @@ def run_secondary(maple, synth, layers, dev, stream, legs=SECONDARY_LEGS):
                 idx_layers.append(idx.clone())
         stream.synchronize()
         packed = distinct_expert_bytes(idx_layers, E, H, I) / n_stack
-        out[f"decode_b{T}"] = {"value": T / sec, "unit": "tokens/s", "ms_per_layer": sec * 1e3,
-                               "layers": n_stack, "bias": "N(0, 0.5) per expert",
-                               "distinct_expert_mb_per_layer": packed / 1e6,
-                               "packed_weight_gbs": packed / sec / 1e9}
+        leg = {"value": T / sec, "unit": "tokens/s", "ms_per_layer": sec * 1e3,
+               "layers": n_stack, "bias": "N(0, 0.5) per expert",
+               "distinct_expert_mb_per_layer": packed / 1e6,
+               "packed_weight_gbs": packed / sec / 1e9}
+        if cpu:
+            leg["cpu_baseline"] = oracle_decode_sample(T, min(T, 4), dev)
+        out[f"decode_b{T}"] = leg
 
     if "prefill_4096" not in legs and "ternarize_pack" not in legs:
         return out
@@ -459,6 +493,8 @@ def run_secondary(maple, synth, layers, dev, stream, legs=SECONDARY_LEGS):
         flops = 2 * 3 * I * H * T * K_TOP
         out["prefill_4096"] = {"value": T / sec, "unit": "tokens/s", "ms_per_layer": sec * 1e3,
                                "dense_equiv_tflops": flops / sec / 1e12, "bias": "Zipf(1.1) ranking"}
+        if cpu:
+            out["prefill_4096"]["cpu_baseline"] = oracle_prefill_sample(x, layers[0], bias, 32)
     if "ternarize_pack" not in legs:
         return out
 
@@ -484,6 +520,8 @@ def run_secondary(maple, synth, layers, dev, stream, legs=SECONDARY_LEGS):
                              "frac_of_peak": bytes_moved / sec / 1e9 / peak,
                              "ms_per_layer": sec * 1e3, "bytes_per_layer": bytes_moved,
                              "weights_per_layer": weights, "peak_source": f"{kind} hbm_gbs"}
+    if cpu:
+        out["ternarize_pack"]["cpu_baseline"] = oracle_pack_sample(wts[0], 96, exact=False)
     del wts
     if "pack_ternary" not in legs:
         return out
@@ -512,6 +550,8 @@ def run_secondary(maple, synth, layers, dev, stream, legs=SECONDARY_LEGS):
                            "ms_per_layer": sec * 1e3, "bytes_per_layer": bytes_moved,
                            "non_ternary_rows": int(bad.item()), "bytes_equal_absmean_pack": same,
                            "peak_source": f"{kind} hbm_gbs"}
+    if cpu:
+        out["pack_ternary"]["cpu_baseline"] = oracle_pack_sample(tern, 48, exact=True)
     del tern, pk2, sc2
     return out
 
@@ -546,6 +586,101 @@ def oracle_sample(n_tokens: int, seed_layer: int = 1000):
     return n_tokens / dt, dt
 
 
+def _oracle_layer(seed_layer: int, experts_needed, gen_dev):
+    """Oracle-packed experts (only those needed; the others are never read) and the bf16
+    router of the bench's layer `seed_layer` (weights drawn as build_layers draws them)."""
+    import oracle
+    from ternary_weight_moe_02_b300 import synth
+    w = synth.expert_weights(E, H, I, seed=seed_layer, device=gen_dev)
+    router = synth.bf16_bits(synth.router_weights(E, H, seed=seed_layer, device=gen_dev))
+    packed = {}
+    for name, rows, K in (("gate", I, H), ("up", I, H), ("down", H, I)):
+        packed[name] = np.full((E, rows, (K + 4) // 5), 121, np.uint8)
+        packed["s_" + name] = np.zeros((E, rows), np.float32)
+        for e in sorted(set(int(v) for v in experts_needed)):
+            p, s = oracle.ternarize_pack(synth.bf16_bits(w[name][e]))
+            packed[name][e], packed["s_" + name][e] = p, s
+    return packed, router
+
+
+def _oracle_route_ffn(packed, router, x_bits, bias):
+    import oracle
+    _, idx, wt = oracle.route(x_bits, router, bias, K_TOP)
+    oracle.moe_ffn(packed["gate"], packed["up"], packed["down"], packed["s_gate"], packed["s_up"],
+                   packed["s_down"], x_bits, idx, wt)
+
+
+def oracle_decode_sample(T: int, n_tokens: int, dev) -> dict:
+    """Oracle route + FFN of n_tokens of the decode leg's first stacked layer (its N(0,0.5)
+    bias and token batch), as layer-tokens/s: the oracle's cost is linear in tokens, so a
+    T-token layer step costs T times the per-token time, on each of the 24 layers."""
+    import oracle
+    from ternary_weight_moe_02_b300 import synth
+    gen_dev = dev if torch.cuda.is_available() else "cpu"
+    x = synth.bf16_bits(synth.tokens(T, H, seed=100, device=gen_dev))[:n_tokens]
+    bias = synth.bias_normal(E, seed=200).double().numpy()
+    router_bits = synth.bf16_bits(synth.router_weights(E, H, seed=1000, device=gen_dev))
+    _, idx0, _ = oracle.route(x, router_bits, bias, K_TOP)
+    packed, router = _oracle_layer(1000, idx0.reshape(-1), gen_dev)
+    t0 = time.perf_counter()
+    _oracle_route_ffn(packed, router, x, bias)
+    dt = time.perf_counter() - t0
+    return {"value": n_tokens / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_tokens} of the {T} tokens of one 256-expert layer (route + FFN, "
+                      f"{dt:.2f} s); per-token cost, the same on each of the 24 layers"}
+
+
+def oracle_prefill_sample(x, layer, bias, n_ffn: int) -> dict:
+    """Oracle of the 4096-token prefill: routing of all tokens timed in full, the FFN on
+    n_ffn tokens stratified by the load of their first expert, scaled to all tokens."""
+    import oracle
+    from ternary_weight_moe_02_b300 import synth
+    T = x.shape[0]
+    xb = synth.bf16_bits(x)
+    b = bias.double().cpu().numpy()
+    router = synth.bf16_bits(layer[1])
+    t0 = time.perf_counter()
+    _, idx, wt = oracle.route(xb, router, b, K_TOP)
+    t_route = time.perf_counter() - t0
+    load = np.bincount(idx.reshape(-1), minlength=E)
+    order = np.argsort(-load[idx[:, 0]], kind="stable")
+    pick = order[np.linspace(0, T - 1, n_ffn).astype(np.int64)]
+    ex = layer[0]
+    packed = {name: t.cpu().numpy() for name, t in zip(("gate", "up", "down", "s_gate", "s_up", "s_down"),
+                                                       ex.tensors)}
+    t0 = time.perf_counter()
+    oracle.moe_ffn(packed["gate"], packed["up"], packed["down"], packed["s_gate"], packed["s_up"],
+                   packed["s_down"], xb[pick], idx[pick], wt[pick])
+    t_ffn = time.perf_counter() - t0
+    est = t_route + t_ffn * T / n_ffn
+    return {"value": T / est, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"routing of all {T} tokens ({t_route:.1f} s) + the FFN on {n_ffn} tokens "
+                      f"stratified by expert load ({t_ffn:.1f} s), scaled to {T} tokens"}
+
+
+def oracle_pack_sample(wts, n_mats: int, exact: bool) -> dict:
+    """Oracle ternarize + pack (exact=False) or already-ternary pack (exact=True) of n_mats
+    of a layer's matrices (a third each of gate, up and down), as GB/s of the same
+    algorithmic bytes as the GPU leg (2 B read + 0.2 B written per weight + 4 B per row)."""
+    import oracle
+    from ternary_weight_moe_02_b300 import synth
+    per = max(1, n_mats // 3)
+    mats = []
+    for name, K in (("gate", H), ("up", H), ("down", I)):
+        src = wts[name].view(-1, I if name != "down" else H, K)
+        mats += [synth.bf16_bits(src[e]) for e in range(per)]
+    nbytes, dt = 0, 0.0
+    for m in mats:
+        t0 = time.perf_counter()
+        q, s = (oracle.ternary_exact(m)[:2] if exact else oracle.ternarize(m))
+        oracle.pack(q)
+        dt += time.perf_counter() - t0
+        rows, K = m.shape
+        nbytes += rows * K * 2 + rows * ((K + 4) // 5) + 4 * rows
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(mats)} matrices of one layer ({dt:.1f} s)"}
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return None
@@ -578,7 +713,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=1000)
     ap.add_argument("--impl", default="maple", choices=["maple", "reference"])
     ap.add_argument("--layers", type=int, default=LAYERS)
-    ap.add_argument("--chunk", type=int, default=1000, help="steps per captured graph")
+    ap.add_argument("--chunk", type=int, default=1024,
+                    help="steps per captured graph (rounded to a multiple of --layers)")
     ap.add_argument("--ref-tokens", type=int, default=4, help="oracle tokens per reference step")
     ap.add_argument("--cpu-tokens", type=int, default=40, help="oracle tokens for cpu_baseline")
     ap.add_argument("--legs", default="", help="comma-separated subset of the secondary legs "

@@ -89,6 +89,29 @@ MAPLE_API const char* maple_last_error(void);
 MAPLE_API int maple_check_device_status(void* stream);
 
 /*
+ * Failure injection, for tests of the error paths (no GPU fault, trap or hang is ever
+ * involved).  Each injection is one-shot and process-wide: the next call it applies to
+ * consumes it.  The pages have no counterpart; this is test support.
+ *   MAPLE_INJECT_NONE         cancel pending injections (value ignored).
+ *   MAPLE_INJECT_COPY_STALL   the next single-token maple_moe_layer launch of the fused
+ *                             kernel arms one bulk-copy barrier of its first CTA for 16
+ *                             bytes that no copy delivers, and limits every bounded wait
+ *                             of that launch to `value` polls (1..100000, each at most
+ *                             ~1 ms).  The wait gives up, the device status word records
+ *                             MAPLE_ERR_TIMEOUT (see maple_check_device_status), y rows
+ *                             of that CTA are NaN, and the kernel still ends normally;
+ *                             the next call needs no clean-up.
+ *   MAPLE_INJECT_LAUNCH_ERROR the next call that would launch kernels returns
+ *                             MAPLE_ERR_CUDA ("injected launch failure") and launches
+ *                             nothing, as a failed launch does.
+ * Returns MAPLE_OK, or MAPLE_ERR_INVALID_ARG for an unknown kind or value.
+ */
+#define MAPLE_INJECT_NONE 0
+#define MAPLE_INJECT_COPY_STALL 1
+#define MAPLE_INJECT_LAUNCH_ERROR 2
+MAPLE_API int maple_test_inject(int32_t kind, int32_t value);
+
+/*
  * Absmean ternarization + 5-trit packing of a bf16 row-major matrix W [rows x K].
  * Per row: s = (1/K) * sum_j |w_j| (fp32), q_j = clamp(round(w_j / s), -1, 1) with
  * round-half-to-even, i.e. q_j = sign(w_j) if |w_j| > s/2 else 0; s = 0 gives all 0.
@@ -181,8 +204,7 @@ MAPLE_API size_t maple_moe_ffn_workspace_size(int32_t T, int32_t k, const maple_
  * slots as experts (2*T*k >= E) and H a multiple of 128, I of 64, both in [128, 2080],
  * the sums run on the tensor cores (fp8 MMAs on trits and on exact two-part splits of
  * the bf16 activations; h is rounded to bf16 between the two projections); otherwise
- * on CUDA cores with fp32 h.  The environment variable MAPLE_FFN_PATH = tensor or
- * cores forces one (when the shape allows it); the workspace size follows the choice.
+ * on CUDA cores with fp32 h.  maple_moe_ffn_ex below names the path explicitly.
  *   ex  : expert weights (see maple_experts)
  *   x   : [T][H] bf16, 16-byte aligned
  *   idx : [T][k] int32 (ids outside [0, E) contribute 0)   w : [T][k] fp32
@@ -196,6 +218,30 @@ MAPLE_API int maple_moe_ffn(const maple_experts* ex, const uint16_t* x, const in
                   const float* w, int32_t T, int32_t k, float* y, void* ws, size_t ws_bytes,
                   void* stream);
 
+/* FFN paths of maple_moe_ffn_ex (maple_moe_ffn always takes MAPLE_FFN_AUTO). */
+#define MAPLE_FFN_AUTO 0   /* tensor cores when 2*T*k >= E and the shape allows it */
+#define MAPLE_FFN_CORES 1  /* CUDA-core kernels, fp32 h (any shape within the limits) */
+#define MAPLE_FFN_TENSOR 2 /* grouped tensor-core kernels (H % 128 == 0, I % 64 == 0,
+                              both in [128, 2080]); MAPLE_ERR_UNSUPPORTED_SHAPE otherwise */
+
+/* Bytes of workspace maple_moe_ffn_ex needs on `path` (0 when the call would be
+ * rejected: invalid arguments, an unknown path, a tensor path the shape does not allow). */
+MAPLE_API size_t maple_moe_ffn_workspace_size_ex(int32_t T, int32_t k, const maple_experts* ex,
+                                                 int32_t path);
+
+/*
+ * maple_moe_ffn with the internal path named by the caller instead of chosen from the
+ * load: the same arguments, limits and result bound, plus `path` (MAPLE_FFN_AUTO,
+ * MAPLE_FFN_CORES or MAPLE_FFN_TENSOR; anything else is MAPLE_ERR_INVALID_ARG).  The
+ * two paths differ only in rounding (the tensor path rounds h to bf16), so a caller
+ * that needs the same bits across batch sizes can pin one of them.  The workspace
+ * must hold maple_moe_ffn_workspace_size_ex(T, k, ex, path) bytes.
+ * ("Maple-Preview ...", section "The shipped code does no quantization".)
+ */
+MAPLE_API int maple_moe_ffn_ex(const maple_experts* ex, const uint16_t* x, const int32_t* idx,
+                               const float* w, int32_t T, int32_t k, float* y, int32_t path,
+                               void* ws, size_t ws_bytes, void* stream);
+
 /* Bytes of workspace maple_moe_layer needs (256 bytes of counters + the FFN's). */
 MAPLE_API size_t maple_moe_layer_workspace_size(int32_t T, int32_t k, const maple_experts* ex);
 
@@ -203,23 +249,46 @@ MAPLE_API size_t maple_moe_layer_workspace_size(int32_t T, int32_t k, const mapl
  * One MoE layer step: maple_route_topk followed by maple_moe_ffn, with the same
  * arguments, outputs and results (logits, idx, w and y are all written).
  * ("Maple-Preview ...", sections "The claim, verified from the bytes" and "The shipped
- * code does no quantization".)  For a single token (T = 1) at Maple-like sizes the
- * whole step runs as one cooperative launch of one CTA per SM: every CTA computes a
- * share of the logits, all of them select the same top-k, fetch and decode their
- * share of the gate/up rows and then of the down rows, with two grid-wide barriers in
- * between (bounded waits: MAPLE_ERR_TIMEOUT via maple_check_device_status).  Other
- * sizes run the two calls in sequence.
+ * code does no quantization".)  For a single token (T = 1) at Maple-like sizes (E <=
+ * 256, k <= 16, I a multiple of 256 up to 640, H a multiple of 128 up to 4096) the
+ * whole step is one launch of one 16-CTA thread-block cluster per routed slot: each
+ * cluster computes all E logits (a share per CTA, exchanged in distributed shared
+ * memory), every CTA selects the same top-k, cluster i then computes slot i's expert
+ * (h exchanged inside the cluster), and the k slots are added into y in the order
+ * i = 0..k-1 by whichever CTA finishes a row block last.  No CTA waits for another
+ * cluster; waits on copies are bounded (MAPLE_ERR_TIMEOUT via
+ * maple_check_device_status).  The results are those of the two calls: the same
+ * logits, idx and w bits, y within the FFN bound.  Other sizes run the two calls in
+ * sequence.
  *   Wr : [E][H] bf16 router (E = ex->E), bias : [E] fp32 or NULL
  *   ws : device workspace of at least maple_moe_layer_workspace_size(T, k, ex) bytes,
  *        16-byte aligned; its first 256 bytes must be zero before the first call (for
- *        example cudaMemsetAsync once after allocating it).  Every call leaves them
- *        zero again; after a MAPLE_ERR_TIMEOUT report, zero them again.
+ *        example cudaMemsetAsync once after allocating it).  Every call, including one
+ *        whose bounded wait gave up, leaves them zero again.
  * Limits: those of maple_route_topk and maple_moe_ffn (k <= 32).
  */
 MAPLE_API int maple_moe_layer(const uint16_t* x, const uint16_t* Wr, const float* bias,
                               const maple_experts* ex, int32_t T, int32_t k, float* logits,
                               int32_t* idx, float* w, float* y, void* ws, size_t ws_bytes,
                               void* stream);
+
+/*
+ * maple_moe_layer for callers whose activations live in host memory: enqueues on
+ * `stream` the copy of the T tokens x_host -> x_dev, the layer step on x_dev (exactly
+ * maple_moe_layer, same arguments and results) and the copy y -> y_host, then returns.
+ * y_host holds the result once the stream has synchronised.  Host buffers should be
+ * pinned (cudaHostAlloc / cudaHostRegister) for the copies to be asynchronous.
+ * ("Maple-Preview ...", sections "The claim, verified from the bytes" and "The shipped
+ * code does no quantization".)
+ *   x_host : [T][H] bf16, host     x_dev : [T][H] bf16 device staging, 16-byte aligned
+ *   y      : [T][H] fp32 device    y_host : [T][H] fp32, host
+ * Errors: those of maple_moe_layer (checked before anything is enqueued), an invalid
+ * argument for a null host buffer, MAPLE_ERR_CUDA if a copy cannot be enqueued.
+ */
+MAPLE_API int maple_moe_layer_host(const uint16_t* x_host, uint16_t* x_dev, const uint16_t* Wr,
+                                   const float* bias, const maple_experts* ex, int32_t T, int32_t k,
+                                   float* logits, int32_t* idx, float* w, float* y, float* y_host,
+                                   void* ws, size_t ws_bytes, void* stream);
 
 /*
  * maple_moe_ffn without a workspace argument, for callers that cannot allocate device

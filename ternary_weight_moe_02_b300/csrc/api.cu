@@ -2,6 +2,8 @@
 // validation, status codes and per-thread error text, then the kernel launches.
 #include <math.h>
 #include <stdarg.h>
+
+#include <atomic>
 #include <stdio.h>
 #include <string.h>
 
@@ -36,7 +38,14 @@ int cuda_fail(cudaError_t err, const char* what) {
 
 bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 
+// One-shot injected launch failure (maple_test_inject): consumed by the next call that
+// would launch kernels, which then reports MAPLE_ERR_CUDA and launches nothing.
+std::atomic<int> g_inject_launch_error{0};
+
+// Every entry point that launches kernels calls this once its arguments are checked.
 int get_device(maple::DeviceInfo* dev, const char* what) {
+    if (g_inject_launch_error.exchange(0) != 0)
+        return fail(MAPLE_ERR_CUDA, "%s: injected launch failure (maple_test_inject)", what);
     cudaError_t err = maple::device_info(dev);
     if (err != cudaSuccess) return cuda_fail(err, what);
     return MAPLE_OK;
@@ -103,6 +112,24 @@ const char* maple_status_string(int status) {
 }
 
 const char* maple_last_error(void) { return g_last_error; }
+
+int maple_test_inject(int32_t kind, int32_t value) {
+    switch (kind) {
+        case MAPLE_INJECT_NONE:
+            g_inject_launch_error.store(0);
+            maple::layer_b1_inject_stall(-1);
+            return ok();
+        case MAPLE_INJECT_COPY_STALL:
+            if (value < 1 || value > 100000) return fail(MAPLE_ERR_INVALID_ARG, "test_inject: polls=%d (1..100000)", value);
+            maple::layer_b1_inject_stall(value);
+            return ok();
+        case MAPLE_INJECT_LAUNCH_ERROR:
+            g_inject_launch_error.store(1);
+            return ok();
+        default:
+            return fail(MAPLE_ERR_INVALID_ARG, "test_inject: kind=%d", kind);
+    }
+}
 
 int maple_check_device_status(void* stream) {
     maple::DeviceInfo dev;
@@ -193,25 +220,50 @@ int maple_group_tokens(const int32_t* idx, int32_t T, int32_t k, int32_t E, int3
 }
 
 size_t maple_moe_ffn_workspace_size(int32_t T, int32_t k, const maple_experts* ex) {
-    return maple::moe_ffn_workspace_bytes(T, k, ex, true);
+    return maple::moe_ffn_workspace_bytes(T, k, ex, MAPLE_FFN_AUTO);
+}
+
+size_t maple_moe_ffn_workspace_size_ex(int32_t T, int32_t k, const maple_experts* ex, int32_t path) {
+    return maple::moe_ffn_workspace_bytes(T, k, ex, path);
 }
 
 int maple_moe_ffn(const maple_experts* ex, const uint16_t* x, const int32_t* idx,
                   const float* w, int32_t T, int32_t k, float* y, void* ws, size_t ws_bytes,
                   void* stream) {
-    return maple::moe_ffn_entry(ex, x, idx, w, T, k, y, ws, ws_bytes, stream, true);
+    return maple::moe_ffn_entry(ex, x, idx, w, T, k, y, ws, ws_bytes, stream, MAPLE_FFN_AUTO);
+}
+
+int maple_moe_ffn_ex(const maple_experts* ex, const uint16_t* x, const int32_t* idx, const float* w,
+                     int32_t T, int32_t k, float* y, int32_t path, void* ws, size_t ws_bytes, void* stream) {
+    return maple::moe_ffn_entry(ex, x, idx, w, T, k, y, ws, ws_bytes, stream, path);
 }
 
 }  // extern "C"
 
-size_t maple::moe_ffn_workspace_bytes(int T, int k, const maple_experts* ex, bool allow_tensor) {
+namespace {
+
+// The path a call takes: *tensor is set, and false is returned when `path` is not one
+// of the three values or names the tensor path for a call its kernels cannot take.
+bool resolve_ffn_path(int path, int T, int k, int E, int H, int I, bool* tensor) {
+    switch (path) {
+        case MAPLE_FFN_AUTO: *tensor = maple::ffn_use_tensor(T, k, E, H, I); return true;
+        case MAPLE_FFN_CORES: *tensor = false; return true;
+        case MAPLE_FFN_TENSOR: *tensor = true; return maple::ffn_tensor_allowed(T, k, E, H, I);
+        default: return false;
+    }
+}
+
+}  // namespace
+
+size_t maple::moe_ffn_workspace_bytes(int T, int k, const maple_experts* ex, int path) {
     if (!ex || T < 0 || k < 1 || ex->E < 1 || ex->H < 1 || ex->I < 1) return 0;
-    const bool tensor = allow_tensor && maple::ffn_use_tensor(T, k, ex->E, ex->H, ex->I);
+    bool tensor = false;
+    if (!resolve_ffn_path(path, T, k, ex->E, ex->H, ex->I, &tensor)) return 0;
     return maple::ffn_workspace_layout(T, k, ex->E, ex->H, ex->I, tensor).total;
 }
 
 int maple::moe_ffn_entry(const maple_experts* ex, const uint16_t* x, const int32_t* idx, const float* w, int T,
-                         int k, float* y, void* ws, size_t ws_bytes, void* stream, bool allow_tensor) {
+                         int k, float* y, void* ws, size_t ws_bytes, void* stream, int path) {
     if (!ex) return fail(MAPLE_ERR_INVALID_ARG, "moe_ffn: null experts");
     const int E = ex->E, H = ex->H, I = ex->I;
     if (T < 0 || k < 1 || E < 1 || H < 1 || I < 1) return fail(MAPLE_ERR_INVALID_ARG, "moe_ffn: T=%d k=%d E=%d H=%d I=%d", T, k, E, H, I);
@@ -225,7 +277,13 @@ int maple::moe_ffn_entry(const maple_experts* ex, const uint16_t* x, const int32
         !aligned(ex->s_up, 16) || !aligned(ex->s_down, 16) || !aligned(x, 16) || !aligned(ws, 16))
         return fail(MAPLE_ERR_MISALIGNED, "moe_ffn: packed weights, scales, x and ws need 16-byte alignment");
     if (!aligned(idx, 4) || !aligned(w, 4) || !aligned(y, 4)) return fail(MAPLE_ERR_MISALIGNED, "moe_ffn: idx, w, y need 4-byte alignment");
-    const bool tensor = allow_tensor && maple::ffn_use_tensor(T, k, E, H, I);
+    if (path != MAPLE_FFN_AUTO && path != MAPLE_FFN_CORES && path != MAPLE_FFN_TENSOR)
+        return fail(MAPLE_ERR_INVALID_ARG, "moe_ffn: path=%d (MAPLE_FFN_AUTO, _CORES or _TENSOR)", path);
+    bool tensor = false;
+    if (!resolve_ffn_path(path, T, k, E, H, I, &tensor))
+        return fail(MAPLE_ERR_UNSUPPORTED_SHAPE,
+                    "moe_ffn: the tensor-core path takes H a multiple of 128 and I of 64, both in [128, 2080] "
+                    "(H=%d I=%d), and at most 65535 token tiles", H, I);
     const maple::FfnWorkspaceLayout L = maple::ffn_workspace_layout(T, k, E, H, I, tensor);
     if (!ws || ws_bytes < L.total) return fail(MAPLE_ERR_WORKSPACE, "moe_ffn: workspace %zu bytes < %zu needed", ws_bytes, L.total);
     maple::DeviceInfo dev;
@@ -270,22 +328,29 @@ int maple::moe_ffn_entry(const maple_experts* ex, const uint16_t* x, const int32
 
 extern "C" {
 
-// Workspace of maple_moe_layer: 256 bytes of barrier counters, then the FFN workspace.
+// Workspace of maple_moe_layer: 256 bytes of counters, then either the FFN workspace
+// (two-call path) or, at T = 1, the fused kernel's per-slot outputs [k][H] fp32.
 size_t maple_moe_layer_workspace_size(int32_t T, int32_t k, const maple_experts* ex) {
     const size_t ffn = maple_moe_ffn_workspace_size(T, k, ex);
-    return ffn == 0 ? 0 : 256 + ffn;
+    if (ffn == 0) return 0;
+    const size_t part = T == 1 ? (maple::layer_b1_part_bytes(k, ex->H) + 255) / 256 * 256 : 0;
+    return 256 + (ffn > part ? ffn : part);
 }
 
-int maple_moe_layer(const uint16_t* x, const uint16_t* Wr, const float* bias,
-                    const maple_experts* ex, int32_t T, int32_t k, float* logits, int32_t* idx,
-                    float* w, float* y, void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Argument checks of maple_moe_layer (MAPLE_OK, or the status it reports).
+int check_layer_args(const uint16_t* x, const uint16_t* Wr, const float* bias, const maple_experts* ex, int32_t T,
+                     int32_t k, float* logits, int32_t* idx, float* w, float* y, void* ws, size_t ws_bytes) {
     if (!ex) return fail(MAPLE_ERR_INVALID_ARG, "moe_layer: null experts");
     const int E = ex->E, H = ex->H, I = ex->I;
     if (T < 0 || H < 1 || E < 1 || I < 1 || k < 1 || k > E) return fail(MAPLE_ERR_INVALID_ARG, "moe_layer: T=%d H=%d E=%d I=%d k=%d", T, H, E, I, k);
     if (!(ex->clamp > 0.f)) return fail(MAPLE_ERR_INVALID_ARG, "moe_layer: clamp must be > 0 (INFINITY for none)");
     if (E > 1024 || k > 32 || H > 2080 || I > 2080 || (int64_t)T * k > (int64_t(1) << 24))
         return fail(MAPLE_ERR_UNSUPPORTED_SHAPE, "moe_layer: E=%d (<=1024) k=%d (<=32) H=%d (<=2080) I=%d (<=2080) T*k=%lld", E, k, H, I, (long long)T * k);
-    if (T == 0) return ok();
+    if (T == 0) return MAPLE_OK;  // nothing to do: the pointers are not looked at
     if (!x || !Wr || !logits || !idx || !w || !y || !ex->gate || !ex->up || !ex->down || !ex->s_gate || !ex->s_up || !ex->s_down)
         return fail(MAPLE_ERR_INVALID_ARG, "moe_layer: null pointer");
     if (!aligned(x, 16) || !aligned(Wr, 16) || !aligned(ws, 16) || !aligned(ex->gate, 16) || !aligned(ex->up, 16) ||
@@ -295,11 +360,23 @@ int maple_moe_layer(const uint16_t* x, const uint16_t* Wr, const float* bias,
         return fail(MAPLE_ERR_MISALIGNED, "moe_layer: fp32/int32 arrays need 4-byte alignment");
     const size_t need = maple_moe_layer_workspace_size(T, k, ex);
     if (!ws || ws_bytes < need) return fail(MAPLE_ERR_WORKSPACE, "moe_layer: workspace %zu bytes < %zu needed", ws_bytes, need);
+    return MAPLE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int maple_moe_layer(const uint16_t* x, const uint16_t* Wr, const float* bias,
+                    const maple_experts* ex, int32_t T, int32_t k, float* logits, int32_t* idx,
+                    float* w, float* y, void* ws, size_t ws_bytes, void* stream) {
+    if (int st = check_layer_args(x, Wr, bias, ex, T, k, logits, idx, w, y, ws, ws_bytes)) return st;
+    if (T == 0) return ok();
+    const int E = ex->E, H = ex->H, I = ex->I;
     maple::DeviceInfo dev;
     if (int st = get_device(&dev, "moe_layer")) return st;
     char* base = static_cast<char*>(ws);
     if (T == 1 && maple::layer_b1_supported(H, I, E, k, dev)) {
-        const maple::FfnWorkspaceLayout L = maple::ffn_workspace_layout(T, k, E, H, I, false);
         maple::LayerLaunch p;
         p.x = x;
         p.Wr = Wr;
@@ -319,7 +396,7 @@ int maple_moe_layer(const uint16_t* x, const uint16_t* Wr, const float* bias,
         p.idx = idx;
         p.w = w;
         p.y = y;
-        p.h = reinterpret_cast<float*>(base + 256 + L.h);
+        p.part = reinterpret_cast<float*>(base + 256);
         p.sync = reinterpret_cast<unsigned*>(base);
         cudaError_t err = maple::launch_moe_layer_b1(p, (cudaStream_t)stream, dev);
         if (err != cudaSuccess) return cuda_fail(err, "moe_layer launch");
@@ -329,6 +406,24 @@ int maple_moe_layer(const uint16_t* x, const uint16_t* Wr, const float* bias,
     int st = maple_route_topk(x, Wr, bias, T, H, E, k, logits, idx, w, stream);
     if (st != MAPLE_OK) return st;
     return maple_moe_ffn(ex, x, idx, w, T, k, y, base + 256, ws_bytes - 256, stream);
+}
+
+int maple_moe_layer_host(const uint16_t* x_host, uint16_t* x_dev, const uint16_t* Wr, const float* bias,
+                         const maple_experts* ex, int32_t T, int32_t k, float* logits, int32_t* idx, float* w,
+                         float* y, float* y_host, void* ws, size_t ws_bytes, void* stream) {
+    // every check of the layer call first, so that a rejected call enqueues nothing
+    if (int st = check_layer_args(x_dev, Wr, bias, ex, T, k, logits, idx, w, y, ws, ws_bytes)) return st;
+    if (T == 0) return ok();
+    if (!x_host || !y_host) return fail(MAPLE_ERR_INVALID_ARG, "moe_layer_host: null host buffer");
+    const size_t x_bytes = (size_t)T * (size_t)ex->H * 2, y_bytes = (size_t)T * (size_t)ex->H * 4;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t err = cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, s);
+    if (err != cudaSuccess) return cuda_fail(err, "moe_layer_host: copy x in");
+    const int st = maple_moe_layer(x_dev, Wr, bias, ex, T, k, logits, idx, w, y, ws, ws_bytes, stream);
+    if (st != MAPLE_OK) return st;
+    err = cudaMemcpyAsync(y_host, y, y_bytes, cudaMemcpyDeviceToHost, s);
+    if (err != cudaSuccess) return cuda_fail(err, "moe_layer_host: copy y out");
+    return ok();
 }
 
 }  // extern "C"

@@ -144,6 +144,41 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// mbarrier.init without the fences: initialise several barriers this way, then make
+// them visible (to the async proxy and the cluster) with one mbar_init_fence().
+__device__ __forceinline__ void mbar_init_nofence(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Sums v[0..R) of every lane over the warp's 32 lanes, R a power of two <= 16, with
+// R - 1 + 5 - log2(R) shuffles instead of R full butterflies: at each of the first
+// log2(R) levels a lane keeps half of its values (the half its lane bit selects) and
+// adds its partner's copy of that half; the last levels are a plain butterfly.  Lane l
+// ends with the total of value (l >> (5 - log2 R)); v[0] holds it.
+template <int R>
+__device__ __forceinline__ float warp_transpose_sum(float (&v)[R], int lane) {
+    static_assert(R == 1 || R == 2 || R == 4 || R == 8 || R == 16, "R");
+#pragma unroll
+    for (int half = R / 2, o = 16; half >= 1; half /= 2, o /= 2) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float keep = upper ? v[i + half] : v[i];
+            const float send = upper ? v[i] : v[i + half];
+            v[i] = keep + __shfl_xor_sync(kFullMask, send, o);
+        }
+    }
+    constexpr int kDone = R == 1 ? 0 : (R == 2 ? 1 : (R == 4 ? 2 : (R == 8 ? 3 : 4)));
+#pragma unroll
+    for (int o = 16 >> kDone; o > 0; o >>= 1) v[0] += __shfl_xor_sync(kFullMask, v[0], o);
+    return v[0];
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                  "r"(bytes)

@@ -45,8 +45,8 @@ extern "C" MAPLE_API int maple_moe_ffn_static_scratch(const maple_experts* ex, c
     // Argument checks are maple_moe_ffn's own; a call it rejects (or an empty one,
     // T == 0) is forwarded without scratch, so it reports exactly as it would.
     if (!ex || T <= 0 || k < 1 || ex->E < 1 || ex->I < 1)
-        return maple::moe_ffn_entry(ex, x, idx, w, T, k, y, nullptr, 0, stream, false);
-    const size_t need = maple::moe_ffn_workspace_bytes(T, k, ex, false);
+        return maple::moe_ffn_entry(ex, x, idx, w, T, k, y, nullptr, 0, stream, MAPLE_FFN_CORES);
+    const size_t need = maple::moe_ffn_workspace_bytes(T, k, ex, MAPLE_FFN_CORES);
     if (need > kStaticScratchBytes)
         return maple::report_error(MAPLE_ERR_WORKSPACE,
                                    "moe_ffn_static_scratch: T=%d k=%d I=%d needs %zu bytes of "
@@ -76,5 +76,5 @@ extern "C" MAPLE_API int maple_moe_ffn_static_scratch(const maple_experts* ex, c
         }
         scratch = g_scratch_addr[dev];
     }
-    return maple::moe_ffn_entry(ex, x, idx, w, T, k, y, scratch, kStaticScratchBytes, stream, false);
+    return maple::moe_ffn_entry(ex, x, idx, w, T, k, y, scratch, kStaticScratchBytes, stream, MAPLE_FFN_CORES);
 }

@@ -40,8 +40,6 @@
 // are bounded.
 #include <cuda_bf16.h>
 #include <math.h>
-#include <stdlib.h>
-#include <string.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -995,18 +993,18 @@ int ffn_tensor_max_tiles(int S, int E) {
     return (S + nt - 1) / nt + (E < S ? E : S);
 }
 
-// MAPLE_FFN_PATH=tensor or =cores forces a path (for parity tests of both on the same
-// inputs); otherwise the tensor path runs once there are at least half as many slots
-// as experts (on the Maple layer, 16 tokens and up).
-bool ffn_use_tensor(int T, int k, int E, int H, int I) {
+// Whether the grouped kernels can take a call: a shape they support, and at most
+// 65535 tiles (the tiles sit in gridDim.y; beyond that, more than about 8.3 million
+// slots, only the CUDA-core kernels run).
+bool ffn_tensor_allowed(int T, int k, int E, int H, int I) {
     if (!ffn_tensor_shape_ok(H, I) || T < 1) return false;
-    // the grouped kernels put the tiles in gridDim.y (at most 65535); beyond that (more
-    // than about 8.3 million slots) the CUDA-core kernels run
-    if (ffn_tensor_max_tiles(T * k, E) > 65535) return false;
-    const char* env = getenv("MAPLE_FFN_PATH");
-    if (env != nullptr && strcmp(env, "tensor") == 0) return true;
-    if (env != nullptr && strcmp(env, "cores") == 0) return false;
-    return 2 * (int64_t)T * k >= (int64_t)E;
+    return ffn_tensor_max_tiles(T * k, E) <= 65535;
+}
+
+// The automatic choice: the tensor path once there are at least half as many slots as
+// experts (on the Maple layer, 16 tokens and up).
+bool ffn_use_tensor(int T, int k, int E, int H, int I) {
+    return ffn_tensor_allowed(T, k, E, H, I) && 2 * (int64_t)T * k >= (int64_t)E;
 }
 
 // H a multiple of the 128 down rows of a CTA, I of the 64 gate (and up) rows; both at

@@ -99,6 +99,7 @@ cudaError_t launch_moe_ffn(const FfnArgs& a, cudaStream_t stream, const DeviceIn
 // Grouped tensor-core FFN (tcgen05): shapes it takes, the path choice for a call, and
 // the launch (group, tile prefix, split x, gate/up, split h, down, combine).
 bool ffn_tensor_shape_ok(int H, int I);
+bool ffn_tensor_allowed(int T, int k, int E, int H, int I);
 bool ffn_use_tensor(int T, int k, int E, int H, int I);
 int ffn_tensor_tile_tokens(int S, int E);
 int ffn_tensor_max_tiles(int S, int E);
@@ -107,14 +108,16 @@ size_t ffn_tensor_h_bytes(int S, int E, int I);
 size_t ffn_tensor_scale_bytes(int S, int E);
 cudaError_t launch_moe_ffn_tensor(const FfnArgs& a, cudaStream_t stream, const DeviceInfo& dev);
 
-// maple_moe_ffn with the path choice made by the caller: allow_tensor = false keeps the
-// call on the CUDA-core kernels (the allocation-free entry point, whose scratch is
-// small).  moe_ffn_workspace_bytes is the workspace such a call needs.
-size_t moe_ffn_workspace_bytes(int T, int k, const ::maple_experts* ex, bool allow_tensor);
+// maple_moe_ffn with the path named by the caller: MAPLE_FFN_AUTO (the choice of
+// ffn_use_tensor), MAPLE_FFN_CORES or MAPLE_FFN_TENSOR (an error when the grouped
+// kernels cannot take the call).  moe_ffn_workspace_bytes is the workspace such a call
+// needs (0 for arguments the call would reject).
+size_t moe_ffn_workspace_bytes(int T, int k, const ::maple_experts* ex, int path);
 int moe_ffn_entry(const ::maple_experts* ex, const uint16_t* x, const int32_t* idx, const float* w, int T, int k,
-                  float* y, void* ws, size_t ws_bytes, void* stream, bool allow_tensor);
+                  float* y, void* ws, size_t ws_bytes, void* stream, int path);
 
-// Fused single-token layer step (route + gate/up + down in one cooperative launch).
+// Fused single-token layer step (route + gate/up + down + combine in one launch of
+// 16-CTA clusters: slot c < C on cluster c, slots past C split over the clusters).
 struct LayerLaunch {
     const uint16_t* x;
     const uint16_t* Wr;
@@ -131,10 +134,19 @@ struct LayerLaunch {
     int32_t* idx;
     float* w;
     float* y;
-    float* h;        // [k][I] scratch
-    unsigned* sync;  // 2 counters, zero on entry and on exit
+    float* part;     // [k][H] scratch (layer_b1_part_bytes)
+    unsigned* sync;  // 16 combine counters, zero on entry and on exit
 };
+// How many 16-CTA clusters of the fused kernel for (H, I, E) the current device runs
+// at once (0 if it cannot tell).
+int layer_b1_clusters(int H, int I, int E);
 bool layer_b1_supported(int H, int I, int E, int k, const DeviceInfo& dev);
+size_t layer_b1_part_bytes(int k, int H);
 cudaError_t launch_moe_layer_b1(const LayerLaunch& p, cudaStream_t stream, const DeviceInfo& dev);
+// How many of the kernel's 16-CTA clusters can be resident at once on this device.
+cudaError_t layer_b1_max_clusters(int H, int I, int E, int* n);
+// Test hook: the next fused launch arms one copy barrier of its first CTA for 16 bytes
+// that no copy delivers and gives every bounded wait `polls` polls.
+void layer_b1_inject_stall(int polls);
 
 }  // namespace maple

@@ -30,11 +30,22 @@ MAPLE_ERR_TIMEOUT = -5
 MAPLE_ERR_BAD_CODE = -6
 MAPLE_ERR_WORKSPACE = -7
 
+MAPLE_INJECT_NONE = 0
+MAPLE_INJECT_COPY_STALL = 1
+MAPLE_INJECT_LAUNCH_ERROR = 2
+
+MAPLE_FFN_AUTO = 0
+MAPLE_FFN_CORES = 1
+MAPLE_FFN_TENSOR = 2
+_FFN_PATHS = {"auto": MAPLE_FFN_AUTO, "cores": MAPLE_FFN_CORES, "tensor": MAPLE_FFN_TENSOR}
+
 EXPORTED = ("maple_version", "maple_status_string", "maple_last_error",
             "maple_check_device_status", "maple_ternarize_pack", "maple_pack_ternary",
             "maple_unpack", "maple_route_topk", "maple_group_tokens",
-            "maple_moe_ffn_workspace_size", "maple_moe_ffn", "maple_moe_layer_workspace_size",
-            "maple_moe_layer", "maple_moe_ffn_static_scratch")
+            "maple_moe_ffn_workspace_size", "maple_moe_ffn", "maple_moe_ffn_workspace_size_ex",
+            "maple_moe_ffn_ex", "maple_moe_layer_workspace_size",
+            "maple_moe_layer", "maple_moe_layer_host", "maple_moe_ffn_static_scratch",
+            "maple_test_inject")
 
 
 class maple_experts(ctypes.Structure):
@@ -62,15 +73,24 @@ _lib.maple_moe_ffn_workspace_size.argtypes = [_I32, _I32, ctypes.POINTER(maple_e
 _lib.maple_moe_ffn_workspace_size.restype = ctypes.c_size_t
 _lib.maple_moe_ffn.argtypes = [ctypes.POINTER(maple_experts), _P, _P, _P, _I32, _I32, _P, _P,
                                ctypes.c_size_t, _P]
+_lib.maple_moe_ffn_workspace_size_ex.argtypes = [_I32, _I32, ctypes.POINTER(maple_experts), _I32]
+_lib.maple_moe_ffn_workspace_size_ex.restype = ctypes.c_size_t
+_lib.maple_moe_ffn_ex.argtypes = [ctypes.POINTER(maple_experts), _P, _P, _P, _I32, _I32, _P, _I32, _P,
+                                  ctypes.c_size_t, _P]
 _lib.maple_moe_layer_workspace_size.argtypes = [_I32, _I32, ctypes.POINTER(maple_experts)]
 _lib.maple_moe_layer_workspace_size.restype = ctypes.c_size_t
 _lib.maple_moe_layer.argtypes = [_P, _P, _P, ctypes.POINTER(maple_experts), _I32, _I32, _P, _P, _P,
                                  _P, _P, ctypes.c_size_t, _P]
 _lib.maple_moe_layer.restype = ctypes.c_int
+_lib.maple_moe_layer_host.argtypes = [_P, _P, _P, _P, ctypes.POINTER(maple_experts), _I32, _I32, _P, _P, _P,
+                                      _P, _P, _P, ctypes.c_size_t, _P]
+_lib.maple_moe_layer_host.restype = ctypes.c_int
 _lib.maple_moe_ffn_static_scratch.argtypes = [ctypes.POINTER(maple_experts), _P, _P, _P, _I32,
                                               _I32, _P, _P]
+_lib.maple_test_inject.argtypes = [_I32, _I32]
+_lib.maple_test_inject.restype = ctypes.c_int
 for _n in ("maple_ternarize_pack", "maple_unpack", "maple_route_topk", "maple_group_tokens",
-           "maple_moe_ffn", "maple_moe_ffn_static_scratch"):
+           "maple_moe_ffn", "maple_moe_ffn_ex", "maple_moe_ffn_static_scratch"):
     getattr(_lib, _n).restype = ctypes.c_int
 
 
@@ -135,6 +155,11 @@ def maple_last_error() -> str:
 def maple_check_device_status(stream=None):
     """Synchronise the stream and raise if a kernel recorded a device-side error."""
     _check(_lib.maple_check_device_status(_stream(stream)), "maple_check_device_status")
+
+
+def maple_test_inject(kind: int, value: int = 0):
+    """One-shot failure injection for tests (MAPLE_INJECT_*; see include/maple.h)."""
+    _check(_lib.maple_test_inject(kind, value), "maple_test_inject")
 
 
 def maple_ternarize_pack(W, packed, scales, stream=None):
@@ -237,6 +262,30 @@ def maple_moe_ffn(experts: Experts, x, idx, w, y, ws, stream=None):
                               _stream(stream)), "maple_moe_ffn")
 
 
+def _path(path) -> int:
+    return _FFN_PATHS[path] if isinstance(path, str) else int(path)
+
+
+def maple_moe_ffn_workspace_size_ex(T: int, k: int, experts: Experts, path) -> int:
+    """Workspace of maple_moe_ffn_ex on `path` ("auto", "cores", "tensor" or the
+    MAPLE_FFN_* value); 0 when the call would be rejected."""
+    return int(_lib.maple_moe_ffn_workspace_size_ex(T, k, ctypes.byref(experts.struct), _path(path)))
+
+
+def maple_moe_ffn_ex(experts: Experts, x, idx, w, y, path, ws, stream=None):
+    """maple_moe_ffn on the named path ("auto", "cores", "tensor" or MAPLE_FFN_*)."""
+    T, H = x.shape
+    k = idx.shape[1]
+    _expect(x, torch.bfloat16, (T, experts.H), "x")
+    _expect(idx, torch.int32, (T, k), "idx")
+    _expect(w, torch.float32, (T, k), "w")
+    _expect(y, torch.float32, (T, experts.H), "y")
+    _check(_lib.maple_moe_ffn_ex(ctypes.byref(experts.struct), _ptr(x), _ptr(idx), _ptr(w), T, k,
+                                 _ptr(y), _path(path), _ptr(ws),
+                                 0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+           "maple_moe_ffn_ex")
+
+
 def maple_moe_layer_workspace_size(T: int, k: int, experts: Experts) -> int:
     return int(_lib.maple_moe_layer_workspace_size(T, k, ctypes.byref(experts.struct)))
 
@@ -244,7 +293,16 @@ def maple_moe_layer_workspace_size(T: int, k: int, experts: Experts) -> int:
 def maple_moe_layer(x, Wr, bias, experts: Experts, k, logits, idx, w, y, ws, stream=None):
     """Route + FFN for one layer step.  ws: uint8 tensor of maple_moe_layer_workspace_size
     bytes whose first 256 bytes are zero before the first call (torch.zeros does it)."""
-    T, H = x.shape
+    _check_layer(x, Wr, bias, experts, k, logits, idx, w, y)
+    T = x.shape[0]
+    _check(_lib.maple_moe_layer(_ptr(x), _ptr(Wr), _ptr(bias), ctypes.byref(experts.struct), T, k,
+                                _ptr(logits), _ptr(idx), _ptr(w), _ptr(y), _ptr(ws),
+                                0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+           "maple_moe_layer")
+
+
+def _check_layer(x, Wr, bias, experts, k, logits, idx, w, y):
+    T = x.shape[0]
     E = Wr.shape[0]
     _expect(x, torch.bfloat16, (T, experts.H), "x")
     _expect(Wr, torch.bfloat16, (experts.E, experts.H), "Wr")
@@ -254,10 +312,50 @@ def maple_moe_layer(x, Wr, bias, experts: Experts, k, logits, idx, w, y, ws, str
     _expect(idx, torch.int32, (T, k), "idx")
     _expect(w, torch.float32, (T, k), "w")
     _expect(y, torch.float32, (T, experts.H), "y")
-    _check(_lib.maple_moe_layer(_ptr(x), _ptr(Wr), _ptr(bias), ctypes.byref(experts.struct), T, k,
-                                _ptr(logits), _ptr(idx), _ptr(w), _ptr(y), _ptr(ws),
-                                0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
-           "maple_moe_layer")
+
+
+def _layer_host_args(x_host, x_dev, Wr, bias, experts, k, logits, idx, w, y, y_host, ws, stream):
+    _check_layer(x_dev, Wr, bias, experts, k, logits, idx, w, y)
+    T = x_dev.shape[0]
+    _expect(x_host, torch.bfloat16, (T, experts.H), "x_host")
+    _expect(y_host, torch.float32, (T, experts.H), "y_host")
+    if x_host.is_cuda or y_host.is_cuda:
+        raise ValueError("x_host and y_host must be host tensors (pinned for asynchronous copies)")
+    return (_ptr(x_host), _ptr(x_dev), _ptr(Wr), _ptr(bias), ctypes.byref(experts.struct), T, k, _ptr(logits),
+            _ptr(idx), _ptr(w), _ptr(y), _ptr(y_host), _ptr(ws),
+            0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+
+
+def maple_moe_layer_host(x_host, x_dev, Wr, bias, experts: Experts, k, logits, idx, w, y, y_host, ws,
+                         stream=None):
+    """maple_moe_layer with the tokens in host memory: x_host (bf16 [T,H], pinned) is
+    copied into x_dev, the layer runs, and y is copied into y_host (fp32 [T,H], pinned),
+    all enqueued on the stream."""
+    _check(_lib.maple_moe_layer_host(*_layer_host_args(x_host, x_dev, Wr, bias, experts, k, logits, idx, w,
+                                                       y, y_host, ws, stream)), "maple_moe_layer_host")
+
+
+class BoundCall:
+    """One C call with its arguments checked and marshalled once: calling the object
+    makes the C call and nothing else (for decode loops, where per-call checks would
+    take longer than the microseconds-long step).  The tensors must stay alive and
+    unchanged in shape while the object is used."""
+
+    def __init__(self, fn, args, where, keep):
+        self._fn, self._args, self._where, self._keep = fn, args, where, keep
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != MAPLE_OK:
+            raise MapleError(st, self._where)
+
+
+def bind_moe_layer_host(x_host, x_dev, Wr, bias, experts: Experts, k, logits, idx, w, y, y_host, ws,
+                        stream=None) -> BoundCall:
+    """maple_moe_layer_host with its arguments bound (see BoundCall)."""
+    args = _layer_host_args(x_host, x_dev, Wr, bias, experts, k, logits, idx, w, y, y_host, ws, stream)
+    return BoundCall(_lib.maple_moe_layer_host, args, "maple_moe_layer_host",
+                     (x_host, x_dev, Wr, bias, experts, logits, idx, w, y, y_host, ws))
 
 
 def maple_moe_ffn_static_scratch(experts: Experts, x, idx, w, y, stream=None):

@@ -31,9 +31,19 @@ def gamma(n: int) -> float:
     return n * U32 / (1 - n * U32)
 
 
+# A row can have excluded trits only if some bf16 magnitude lies within the window
+# ||w|/s - 0.5| <= 0.5e-6, i.e. within 0.5e-6 s of s/2.  bf16 magnitudes near s/2 are
+# 2^(e-7) apart for s/2 in [2^e, 2^(e+1)), so the window (width 1e-6 s) holds one with
+# probability at most 1e-6 s / 2^(e-7) < 1e-6 * 512 = 5.12e-4 per row.
+ROW_EXCLUSION_RATE = 5.12e-4
+
+
 def pack_compare(w_bits: np.ndarray, gpu_packed: np.ndarray, gpu_scales: np.ndarray):
     """Compare GPU ternarize+pack with the oracle.  Returns (n_excluded_trits,
-    oracle_packed, oracle_scales); raises AssertionError on a real mismatch."""
+    oracle_packed, oracle_scales); raises AssertionError on a real mismatch.
+    Excluded trits are checked against their expected rate: within a row they all
+    share one magnitude (the bf16 value next to s/2), and the rows holding any stay
+    within a 4-sigma Poisson bound of ROW_EXCLUSION_RATE per row."""
     rows, K = w_bits.shape
     ref_q, ref_s = oracle.ternarize(w_bits)
     ref_p = oracle.pack(ref_q)
@@ -52,6 +62,12 @@ def pack_compare(w_bits: np.ndarray, gpu_packed: np.ndarray, gpu_scales: np.ndar
             f"{int((~near).sum())} trits differ away from the rounding boundary; first ratio "
             f"{ratio[~near][:4]}")
         excluded = len(r_idx)
+        mag = np.abs(wv[r_idx, c_idx])
+        for r in np.unique(r_idx):
+            assert np.unique(mag[r_idx == r]).size == 1, f"row {diff_rows[r]}: excluded trits of two magnitudes"
+        lam = ROW_EXCLUSION_RATE * rows
+        assert len(diff_rows) <= lam + 4 * np.sqrt(lam) + 2, (
+            f"{len(diff_rows)} of {rows} rows hold excluded trits (expected about {lam:.3f})")
     return excluded, ref_p, ref_s
 
 
@@ -85,15 +101,48 @@ def upload_experts(packed: dict, clamp: float = 7.0, device="cuda"):
                          clamp=clamp)
 
 
-def run_ffn(ex, x, idx, w):
+def run_ffn(ex, x, idx, w, path=None):
+    """maple_moe_ffn (path None) or maple_moe_ffn_ex on the named path."""
     from ternary_weight_moe_02_b300 import maple
     T = x.shape[0]
     k = idx.shape[1]
     y = torch.full((T, ex.H), float("nan"), device=x.device, dtype=torch.float32)
-    ws = torch.empty(max(1, maple.maple_moe_ffn_workspace_size(T, k, ex)), dtype=torch.uint8,
-                     device=x.device)
-    maple.maple_moe_ffn(ex, x, idx, w, y, ws)
+    if path is None:
+        ws = torch.empty(max(1, maple.maple_moe_ffn_workspace_size(T, k, ex)), dtype=torch.uint8,
+                         device=x.device)
+        maple.maple_moe_ffn(ex, x, idx, w, y, ws)
+    else:
+        need = maple.maple_moe_ffn_workspace_size_ex(T, k, ex, path)
+        assert need > 0, f"path {path} cannot take T={T} k={k} on this shape"
+        ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+        maple.maple_moe_ffn_ex(ex, x, idx, w, y, path, ws)
     return y
+
+
+def oracle_moe_ffn_rows(packed: dict, x_bits: np.ndarray, idx: np.ndarray, w: np.ndarray,
+                        rows, clamp: float = 7.0, workers: int | None = None) -> np.ndarray:
+    """oracle.moe_ffn on the given token rows, the rows split over a pool of host
+    threads.  Each oracle call is the plain single-threaded C routine on a chunk of
+    rows (ctypes releases the GIL during it); the threads only run several such calls
+    at once.  Returns y fp64 [len(rows), H] in the order of `rows`."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    rows = np.asarray(rows, dtype=np.int64)
+    n = len(rows)
+    if workers is None:
+        workers = max(1, min(16, os.cpu_count() or 1))
+    chunks = [c for c in np.array_split(np.arange(n), min(n, 4 * workers)) if len(c)]
+
+    def one(c):
+        r = rows[c]
+        return c, oracle.moe_ffn(packed["gate"], packed["up"], packed["down"], packed["s_gate"],
+                                 packed["s_up"], packed["s_down"], x_bits[r], idx[r],
+                                 np.asarray(w, np.float64)[r], clamp=clamp)
+    out = np.empty((n, packed["down"].shape[1]), np.float64)
+    with ThreadPoolExecutor(max_workers=workers) as pool:
+        for c, y in pool.map(one, chunks):
+            out[c] = y
+    return out
 
 
 def assert_ffn_close(y_gpu: np.ndarray, y_ref: np.ndarray, what: str = ""):

@@ -155,7 +155,12 @@ def test_moe_layer_validation(lib):
     ffn = lib.maple_moe_ffn_workspace_size
     ffn.argtypes = [I32, I32, ctypes.POINTER(maple_experts)]
     ffn.restype = ctypes.c_size_t
-    assert need == 256 + ffn(1, 8, ctypes.byref(ex))
+    # 256 bytes of counters, then the larger of the FFN workspace and the fused kernel's
+    # per-slot outputs: C (1 + k - C) rows of H fp32 for C clusters, bounded over C <= k
+    groups = max(C * (1 + 8 - C) for C in range(1, 9))
+    assert groups == 20
+    assert need == 256 + max(ffn(1, 8, ctypes.byref(ex)), groups * 2048 * 4)
+    assert wsz(64, 8, ctypes.byref(ex)) == 256 + ffn(64, 8, ctypes.byref(ex))
     good = (A16, A16, None, ctypes.byref(ex), 1, 8, A16, A16, A16, A16, A16, need, None)
     assert f(*good[:3], None, *good[4:]) == -1
     assert f(A16, A16, None, ctypes.byref(ex), 1, 0, A16, A16, A16, A16, A16, need, None) == -1
@@ -165,3 +170,51 @@ def test_moe_layer_validation(lib):
     assert f(A16, A16, None, ctypes.byref(ex), 1, 8, A16, A16, A16, A16, A16, need - 1, None) == -7
     assert f(A16, A16, None, ctypes.byref(ex), 1, 8, None, A16, A16, A16, A16, need, None) == -1
     assert f(None, None, None, ctypes.byref(ex), 0, 8, None, None, None, None, None, 0, None) == 0
+
+
+def test_moe_ffn_ex_path_validation(lib):
+    """maple_moe_ffn_ex: an unknown path is an invalid argument; the tensor path on a
+    shape its kernels do not take is an unsupported shape (both before any launch)."""
+    from ternary_weight_moe_02_b300.maple import maple_experts
+    wsz = lib.maple_moe_ffn_workspace_size_ex
+    wsz.argtypes = [I32, I32, ctypes.POINTER(maple_experts), I32]
+    wsz.restype = ctypes.c_size_t
+    f = lib.maple_moe_ffn_ex
+    f.argtypes = [ctypes.POINTER(maple_experts), P, P, P, I32, I32, P, I32, P, ctypes.c_size_t, P]
+    ex = _experts(lib)
+    need = max(wsz(64, 8, ctypes.byref(ex), p) for p in (0, 1, 2))
+    assert wsz(64, 8, ctypes.byref(ex), 1) < wsz(64, 8, ctypes.byref(ex), 2)
+    assert f(ctypes.byref(ex), A16, A16, A16, 64, 8, A16, 3, A16, need, None) == -1
+    assert f(ctypes.byref(ex), A16, A16, A16, 64, 8, A16, -1, A16, need, None) == -1
+    odd = _experts(lib, H=2000)
+    assert wsz(64, 8, ctypes.byref(odd), 2) == 0
+    assert f(ctypes.byref(odd), A16, A16, A16, 64, 8, A16, 2, A16, need, None) == -2
+    # the workspace check follows the named path
+    cores = wsz(64, 8, ctypes.byref(ex), 1)
+    assert f(ctypes.byref(ex), A16, A16, A16, 64, 8, A16, 2, A16, cores, None) == -7
+
+
+def test_test_inject_validation_and_launch_error(lib):
+    """maple_test_inject rejects unknown kinds and poll counts; an injected launch error
+    is reported by the next launching call (before any CUDA call) and only once."""
+    f = lib.maple_test_inject
+    f.argtypes = [I32, I32]
+    assert f(7, 0) == -1
+    assert f(1, 0) == -1 and f(1, 100001) == -1
+    assert f(0, 0) == 0
+    route = lib.maple_route_topk
+    route.argtypes = [P, P, P, I32, I32, I32, I32, P, P, P, P]
+    last = lib.maple_last_error
+    last.restype = ctypes.c_char_p
+    assert f(2, 0) == 0
+    assert route(A16, A16, None, 1, 64, 8, 2, A16, A16, A16, None) == -4
+    assert b"injected launch failure" in last()
+    # consumed: the next call gets past the hook (here it then fails on the missing GPU
+    # or launches, but not with the injected message)
+    route(A16, A16, None, 1, 64, 8, 2, A16, A16, A16, None)
+    assert b"injected" not in last()
+    # validation errors come first and leave a pending injection in place
+    assert f(2, 0) == 0
+    assert route(A16, A16, None, 1, 64, 0, 2, A16, A16, A16, None) == -1
+    assert route(A16, A16, None, 1, 64, 8, 2, A16, A16, A16, None) == -4
+    assert f(0, 0) == 0

@@ -118,22 +118,52 @@ def test_ffn_decode_batches_full_layer(layer256, router256, T):
     _compare(packed, ex, x, idx, w32, what=f"T={T}")
 
 
-def test_ffn_prefill_4096_sampled(layer256, router256):
-    """4096-token prefill, Zipf(1.1) router bias; the GPU runs all tokens in one call,
-    the oracle checks 24 tokens chosen across the expert-load range."""
+def test_ffn_prefill_4096_every_tile(layer256, router256):
+    """4096-token prefill, Zipf(1.1) router bias; the GPU runs all tokens in one call
+    (grouped tensor-core path, 128-token tiles).  The oracle checks, for every expert
+    with a non-zero load, the first and the last token of each of its 128-token tiles
+    (tiles follow the stable grouping of slots by expert, which the oracle's own
+    grouping gives), plus the first tokens of the busiest and the idlest expert, the
+    first and last token of the call and random picks: every tile record of the call,
+    including the experts spanning several tiles and the tiles past the first chunk of
+    the grouping, has at least one checked token."""
+    from support import oracle_moe_ffn_rows
     packed, ex = layer256
-    T = 4096
+    T, k, E, NT = 4096, 8, 256, 128
     x = synth.tokens(T, 2048, seed=42)
-    idx, w32 = _route_oracle(x, router256.cpu(), synth.bias_zipf(256, seed=0, gamma=1.0), 8)
-    loads = np.bincount(idx.reshape(-1), minlength=256)
-    assert loads.max() >= 200  # several hundred tokens on the busiest expert
+    idx, w32 = _route_oracle(x, router256.cpu(), synth.bias_zipf(E, seed=0, gamma=1.0), k)
+    counts, offsets, perm = oracle.group(idx, E)
+    assert counts.max() >= 200  # several hundred tokens on the busiest expert
+    rows, tiles = set(), 0
+    for e in np.nonzero(counts)[0]:
+        for j in range(0, int(counts[e]), NT):
+            last = min(j + NT, int(counts[e])) - 1
+            rows.add(int(perm[offsets[e] + j]) // k)
+            rows.add(int(perm[offsets[e] + last]) // k)
+            tiles += 1
     rng = np.random.default_rng(0)
-    busiest, idlest = np.argmax(loads), np.argmin(np.where(loads > 0, loads, 10**9))
-    rows = set(np.nonzero((idx == busiest).any(axis=1))[0][:6].tolist())
+    busiest, idlest = np.argmax(counts), np.argmin(np.where(counts > 0, counts, 10**9))
+    rows |= set(np.nonzero((idx == busiest).any(axis=1))[0][:6].tolist())
     rows |= set(np.nonzero((idx == idlest).any(axis=1))[0][:6].tolist())
     rows |= {0, T - 1}
-    rows |= set(rng.choice(T, size=24 - len(rows), replace=False).tolist())
-    _compare(packed, ex, x, idx, w32, rows=sorted(rows), what="prefill sample")
+    rows |= set(rng.choice(T, size=24, replace=False).tolist())
+    rows = sorted(rows)
+    print(f"prefill parity: {tiles} tiles of {int((counts > 0).sum())} loaded experts, "
+          f"{len(rows)} tokens checked")
+    y_gpu = run_ffn(ex, x.cuda(), torch.from_numpy(idx).cuda(), torch.from_numpy(w32).cuda())
+    torch.cuda.synchronize()
+    y_gpu = y_gpu.cpu().numpy()
+    y_ref = oracle_moe_ffn_rows(packed, synth.bf16_bits(x), idx, w32, rows)
+    # the tolerance is taken over the checked rows (max|y| of the whole output is not
+    # known without the oracle on every token; over a subset it can only be smaller)
+    assert_ffn_close(y_gpu[rows], y_ref, "prefill, every tile")
+    # every tile has a checked token
+    checked = np.zeros(T, bool)
+    checked[rows] = True
+    for e in np.nonzero(counts)[0]:
+        for j in range(0, int(counts[e]), NT):
+            toks = perm[offsets[e] + j: offsets[e] + min(j + NT, int(counts[e]))] // k
+            assert checked[toks].any()
 
 
 @pytest.mark.parametrize("E,H,I", [(6, 40, 24), (8, 2048, 512)])

@@ -153,3 +153,27 @@ def test_layer_small_shapes_single_token():
         logits, idx, w32, y, _ = _layer_call(ex, x, router, None, k)
         torch.cuda.synchronize()
         _check_against_oracle(packed, x, router, None, k, logits, idx, w32, y)
+
+
+def test_layer_host_buffers_match_the_device_call(layer256):
+    """maple_moe_layer_host (token copied in from pinned host memory, y copied out)
+    gives the device call's results bit for bit, twice in a row; the bound form too."""
+    from ternary_weight_moe_02_b300 import maple
+    packed, ex, router = layer256
+    ws = torch.zeros(maple.maple_moe_layer_workspace_size(1, 8, ex), dtype=torch.uint8, device="cuda")
+    for seed in (21, 22):
+        x = synth.tokens(1, 2048, seed=seed, device="cuda")
+        logits, idx, w, y, _ = _layer_call(ex, x, router, None, 8, ws)
+        x_host = x.cpu().pin_memory()
+        y_host = torch.full((1, 2048), float("nan")).pin_memory()
+        x_dev = torch.empty_like(x)
+        l2, i2, w2, y2 = (torch.empty_like(logits), torch.empty_like(idx), torch.empty_like(w),
+                          torch.empty_like(y))
+        maple.maple_moe_layer_host(x_host, x_dev, router, None, ex, 8, l2, i2, w2, y2, y_host, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(logits, l2) and torch.equal(idx, i2) and torch.equal(w, w2)
+        assert torch.equal(y.cpu(), y_host)
+        y_host.fill_(float("nan"))
+        maple.bind_moe_layer_host(x_host, x_dev, router, None, ex, 8, l2, i2, w2, y2, y_host, ws)()
+        torch.cuda.synchronize()
+        assert torch.equal(y.cpu(), y_host)

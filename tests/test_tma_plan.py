@@ -104,66 +104,176 @@ def test_maple_shapes_take_the_bulk_copy_path():
 
 
 # ---------------------------------------------------------------- fused layer kernel
-LD_ITEM_ROWS, LD_DOWN_ROWS, LD_MAX_ITEMS, LD_MAX_ROUTER_ROWS, LD_MAX_K, LD_WARPS = 8, 16, 8, 8, 12, 16
+# restates csrc/layer_decode.cu: C 16-CTA clusters (one CTA per SM, 16 warps); slot c < C
+# on cluster c, slots C..k-1 split over the clusters by ranges of 40 intermediate columns
+LC_CS, LC_WARPS, LC_CHUNKS, LC_MAX_E, LC_MAX_K, LC_MAX_SPLIT = 16, 16, 4, 256, 16, 2
+LC_MAX_DOWN_LANE_BYTES, LC_UNIT, LC_MAX_UNITS, LC_SPLIT_COPY_ROWS = 4, 40, 4, 24
+LUT16_BYTES = 243 * 16 * 8
 
 
-def layer_ok(H, I, E, k, G=148, smem_optin=232448):
+def _a16(v):
+    return (v + 15) // 16 * 16
+
+
+def split_range(I, C, c):
+    nu = (I + LC_UNIT - 1) // LC_UNIT
+    u0, u1 = c * nu // C, (c + 1) * nu // C
+    return u0 * LC_UNIT, min(u1 * LC_UNIT, I)
+
+
+def split_pairs(n, r):
+    per = (n + LC_CS - 1) // LC_CS
+    p0 = min(r * per, n)
+    p1 = min(p0 + per, n)
+    return p0, p1, p0 // 8 * 8
+
+
+def layer_smem(H, I, E):
+    """Offsets of the union region and inside it, and the total bytes."""
     Bh, Bi = nbytes(H), nbytes(I)
-    if H % LD_DOWN_ROWS or H // LD_DOWN_ROWS > G:
-        return False
-    if I % LD_ITEM_ROWS or I % 4 or Bh % 2 or (Bh + 31) // 32 > 13:
-        return False
-    nr = (E + G - 1) // G
-    nitems = (k * (I // LD_ITEM_ROWS) + G - 1) // G
-    if k > LD_MAX_K or E > 1024 or nr > LD_MAX_ROUTER_ROWS or nr > LD_WARPS or nitems > LD_MAX_ITEMS:
-        return False
-    if (Bi + 31) // 32 > 4:
-        return False
     MB = (Bh + 31) // 32
-    total = (31104 + nr * 2 * H + 2 * H + 4 * 32 * MB * 5 + nitems * (2 * LD_ITEM_ROWS * Bh + 8 * LD_ITEM_ROWS)
-             + k * (LD_DOWN_ROWS * Bi + 4 * LD_DOWN_ROWS) + k * 4 * I + 4 * ((E + 3) // 4 * 4))
-    return total <= smem_optin - 1024
+    nr = (E + LC_CS - 1) // LC_CS
+    rg, rd = I // LC_CS, H // LC_CS
+    o = (LUT16_BYTES + _a16(2 * H) + 4 * 32 * MB * 5 + 4 * 32 * LC_MAX_DOWN_LANE_BYTES * 5
+         + 4 * LC_MAX_SPLIT * _a16(I) + 4 * LC_MAX_E + 4 * (rg + LC_MAX_SPLIT * LC_CS))
+    un = _a16(o)
+    cr = rg // LC_CHUNKS
+    chunk = 2 * cr * Bh + 8 * cr
+    dn = LC_CHUNKS * chunk
+    dn_bytes = rd * Bi + 4 * rd
+    sp = dn + dn_bytes
+    sp_gu = 2 * LC_SPLIT_COPY_ROWS * Bh + 8 * LC_SPLIT_COPY_ROWS
+    sp_bytes = sp_gu + dn_bytes
+    total = un + max(nr * 2 * H, sp + LC_MAX_SPLIT * sp_bytes)
+    return dict(un=un, cr=cr, chunk=chunk, dn=dn, sp=sp, sp_gu=sp_gu, sp_bytes=sp_bytes, total=total)
 
 
-def layer_transfers(E, H, I, k, G=148):
-    """Every bulk copy of every CTA, for any top-k outcome (all experts e < E)."""
+def layer_ok(H, I, E, k, C, smem_optin=232448):
     Bh, Bi = nbytes(H), nbytes(I)
-    ngroups = I // LD_ITEM_ROWS
-    nr = (E + G - 1) // G
-    nitems = (k * ngroups + G - 1) // G
-    for c in range(G):
-        for j in range(nr):
-            if c + j * G < E:
-                yield (c + j * G) * H * 2, 2 * H, E * H * 2, "router row"
-        yield 0, 2 * H, H * 2, "x"
-        for n in range(nitems):
-            jj = c + n * G
-            if jj >= k * ngroups:
-                continue
-            r0 = (jj % ngroups) * LD_ITEM_ROWS
+    if H % 8 or H % (LC_CS * LC_WARPS) or H // LC_CS // LC_WARPS > 8:
+        return False
+    rd = H // LC_CS
+    if (rd * Bi) % 16 or (H * Bi) % 16 or (Bi + 31) // 32 > LC_MAX_DOWN_LANE_BYTES:
+        return False
+    if I % 8 or I % (LC_CS * LC_WARPS) or I // LC_CS // LC_WARPS > 4:
+        return False
+    cr = I // LC_CS // LC_CHUNKS
+    if (cr * Bh) % 16 or (I * Bh) % 16 or (8 * Bh) % 16 or (Bh + 31) // 32 > 13:
+        return False
+    if k < 1 or k > LC_MAX_K or k > E or E > LC_MAX_E or (E + LC_CS - 1) // LC_CS > LC_WARPS:
+        return False
+    C = min(k, C)
+    nsplit = k - C
+    if nsplit > LC_MAX_SPLIT:
+        return False
+    if nsplit:
+        nu = (I + LC_UNIT - 1) // LC_UNIT
+        if (nu + C - 1) // C > LC_MAX_UNITS:
+            return False
+        for c in range(C):
+            c0, c1 = split_range(I, C, c)
+            per = (c1 - c0 + LC_CS - 1) // LC_CS
+            if per > LC_WARPS or per + 7 > LC_SPLIT_COPY_ROWS:
+                return False
+    return layer_smem(H, I, E)["total"] + 1024 <= smem_optin
+
+
+def layer_transfers(E, H, I, k, C):
+    """Every bulk copy of every CTA (global offset, size, global buffer size, what,
+    shared destination, shared end), for any top-k outcome (experts 0 and E - 1 stand
+    for all)."""
+    Bh, Bi = nbytes(H), nbytes(I)
+    L = layer_smem(H, I, E)
+    un, total = L["un"], L["total"]
+    C = min(k, C)
+    nsplit = k - C
+    nr = (E + LC_CS - 1) // LC_CS
+    rg, rd = I // LC_CS, H // LC_CS
+    cr = L["cr"]
+    for c in range(C):
+        col0, col1 = split_range(I, C, c)
+        for r in range(LC_CS):
+            yield 0, LUT16_BYTES, LUT16_BYTES, "table", 0, total
+            e_lo = r * nr
+            n = max(0, min(nr, E - e_lo))
+            if n:
+                yield e_lo * H * 2, n * 2 * H, E * H * 2, "router rows", un, un + nr * 2 * H
+            yield 0, 2 * H, 2 * H, "x", LUT16_BYTES, LUT16_BYTES + _a16(2 * H)
             for e in (0, E - 1):
-                yield (e * I + r0) * Bh, LD_ITEM_ROWS * Bh, E * I * Bh, "gate item"
-                yield (e * I + r0) * 4, 4 * LD_ITEM_ROWS, E * I * 4, "gate scales"
-        if c < H // LD_DOWN_ROWS:
-            c0 = c * LD_DOWN_ROWS
-            for e in (0, E - 1):
-                yield (e * H + c0) * Bi, LD_DOWN_ROWS * Bi, E * H * Bi, "down group"
-                yield (e * H + c0) * 4, 4 * LD_DOWN_ROWS, E * H * 4, "down scales"
-            for i in range(k):
-                yield i * I * 4, 4 * I, k * I * 4, "h"
+                for q in range(LC_CHUNKS):
+                    r0 = e * I + r * rg + q * cr
+                    base = un + q * L["chunk"]
+                    yield r0 * Bh, cr * Bh, E * I * Bh, "gate chunk", base, total
+                    yield r0 * Bh, cr * Bh, E * I * Bh, "up chunk", base + cr * Bh, total
+                    yield r0 * 4, 4 * cr, E * I * 4, "gate scales", base + 2 * cr * Bh, total
+                    yield r0 * 4, 4 * cr, E * I * 4, "up scales", base + 2 * cr * Bh + 4 * cr, total
+                d0 = e * H + r * rd
+                yield d0 * Bi, rd * Bi, E * H * Bi, "down rows", un + L["dn"], total
+                yield d0 * 4, 4 * rd, E * H * 4, "down scales", un + L["dn"] + rd * Bi, total
+                p0, p1, g0 = split_pairs(col1 - col0, r)
+                for s in range(nsplit):
+                    sp = un + L["sp"] + s * L["sp_bytes"]
+                    if p1 > p0:
+                        nrows = min(LC_SPLIT_COPY_ROWS, I - col0 - g0)
+                        assert nrows % 8 == 0 and p1 - g0 <= nrows, (c, r, p0, p1, g0, nrows)
+                        r0 = e * I + col0 + g0
+                        yield r0 * Bh, nrows * Bh, E * I * Bh, "split gate rows", sp, sp + LC_SPLIT_COPY_ROWS * Bh
+                        yield (r0 * Bh, nrows * Bh, E * I * Bh, "split up rows", sp + LC_SPLIT_COPY_ROWS * Bh,
+                               sp + 2 * LC_SPLIT_COPY_ROWS * Bh)
+                        sc = sp + 2 * LC_SPLIT_COPY_ROWS * Bh
+                        yield r0 * 4, 4 * nrows, E * I * 4, "split gate scales", sc, sc + 4 * LC_SPLIT_COPY_ROWS
+                        yield (r0 * 4, 4 * nrows, E * I * 4, "split up scales", sc + 4 * LC_SPLIT_COPY_ROWS,
+                               sc + 8 * LC_SPLIT_COPY_ROWS)
+                    d0 = e * H + r * rd
+                    yield d0 * Bi, rd * Bi, E * H * Bi, "split down rows", sp + L["sp_gu"], total
+                    yield d0 * 4, 4 * rd, E * H * 4, "split down scales", sp + L["sp_gu"] + rd * Bi, total
 
 
 def test_fused_layer_plan_is_aligned_and_in_bounds():
+    """Source and shared-memory destination of every copy 16-byte aligned, sizes multiples
+    of 16, both inside their buffers, for cluster counts that take every slot whole
+    (C >= k) or split one or two slots; the router rows fit the union region; the copies
+    of one barrier stay below the 2^20 - 1 byte count."""
     checked = 0
-    for H, I in [(2048, 512), (160, 40), (512, 64), (2080, 520), (1024, 640), (96, 16)]:
-        for E, k in [(256, 8), (32, 8), (8, 8), (1024, 12), (300, 3)]:
-            if k > E or not layer_ok(H, I, E, k):
-                continue
-            for off, size, buf, what in layer_transfers(E, H, I, k):
-                _check(off, size, buf, f"layer H={H} I={I} E={E} k={k} {what}")
-                checked += 1
-    assert checked > 1000
-    assert layer_ok(2048, 512, 256, 8) and layer_ok(2048, 512, 32, 8)
+    for H, I in [(2048, 512), (1024, 512), (2048, 256), (4096, 512), (2048, 768)]:
+        for E, k in [(256, 8), (32, 8), (8, 8), (250, 3), (16, 9), (256, 1), (256, 16)]:
+            for C in (7, 8, 6, 5, 16):
+                if k > E or not layer_ok(H, I, E, k, C):
+                    continue
+                nr = (E + LC_CS - 1) // LC_CS
+                assert LUT16_BYTES + nr * 2 * H < 1 << 20
+                for off, size, buf, what, dst, dst_end in layer_transfers(E, H, I, k, C):
+                    _check(off, size, buf, f"layer H={H} I={I} E={E} k={k} C={C} {what}")
+                    assert dst % 16 == 0 and dst + size <= dst_end, f"{what}: smem [{dst}, {dst + size})"
+                    checked += 1
+    assert checked > 5000
+    assert layer_ok(2048, 512, 256, 8, 7) and layer_ok(2048, 512, 32, 8, 7) and layer_ok(2048, 512, 256, 8, 8)
+
+
+def test_fused_layer_split_ranges_cover_every_column_once():
+    """Split slot: the clusters' column ranges tile [0, I) in order, each range starts on
+    a 40-column unit (8 whole gate/up row groups, 8 whole down-row bytes), and the CTAs'
+    pair ranges tile each cluster's range."""
+    for I in (512, 256):
+        for C in (5, 6, 7, 8):
+            cols = []
+            for c in range(C):
+                c0, c1 = split_range(I, C, c)
+                assert c0 % LC_UNIT == 0 and c0 < c1 or c0 == c1
+                pairs = []
+                for r in range(LC_CS):
+                    p0, p1, g0 = split_pairs(c1 - c0, r)
+                    pairs += list(range(c0 + p0, c0 + p1))
+                assert pairs == list(range(c0, c1))
+                cols += list(range(c0, c1))
+            assert cols == list(range(I))
+
+
+def test_fused_layer_is_one_cta_per_sm_at_the_maple_shape():
+    """The Maple layer's CTA (shared memory plus the SM's 1 KB reserve per CTA) does not
+    fit twice into an SM's 228 KB, so the clusters never share SMs."""
+    total = layer_smem(2048, 512, 256)["total"]
+    assert 228 * 1024 < 2 * (total + 3440 + 1024) and total + 3440 + 1024 <= 227 * 1024
 
 
 PK_MAX_WARPS = 8

@@ -2,10 +2,10 @@
 for follows the FFN path the call will take.  The CUDA-core layout is counts, offsets,
 the slot permutation, the active-expert list and h fp32 [T*k][I], each region 256-byte
 aligned; the grouped tensor-core path adds its own regions.  That path is taken for
-2*T*k >= E on shapes it accepts (MAPLE_FFN_PATH = tensor or cores forces one), and never
-when its tile count would pass the 65535 limit of a grid's y dimension."""
+2*T*k >= E on shapes it accepts (maple_moe_ffn_workspace_size_ex names a path), and
+never when its tile count would pass the 65535 limit of a grid's y dimension; asking
+for the tensor path where it cannot run sizes nothing (0: the call would be rejected)."""
 import ctypes
-import os
 
 import pytest
 
@@ -27,19 +27,10 @@ def cores_bytes(T, k, E, I):
 
 
 def ws(T, k, E, H, I, path=None):
-    old = os.environ.get("MAPLE_FFN_PATH")
-    try:
-        if path is None:
-            os.environ.pop("MAPLE_FFN_PATH", None)
-        else:
-            os.environ["MAPLE_FFN_PATH"] = path
-        ex = maple.maple_experts(None, None, None, None, None, None, E, H, I, 7.0)
+    ex = maple.maple_experts(None, None, None, None, None, None, E, H, I, 7.0)
+    if path is None:
         return maple._lib.maple_moe_ffn_workspace_size(T, k, ctypes.byref(ex))
-    finally:
-        if old is None:
-            os.environ.pop("MAPLE_FFN_PATH", None)
-        else:
-            os.environ["MAPLE_FFN_PATH"] = old
+    return maple._lib.maple_moe_ffn_workspace_size_ex(T, k, ctypes.byref(ex), maple._path(path))
 
 
 @pytest.mark.parametrize("T,k,E,H,I", [(1, 8, 256, 2048, 512), (64, 8, 256, 2048, 512),
@@ -58,11 +49,18 @@ def test_default_choice_follows_the_slot_count():
     assert ws(15, 8, 256, 2048, 512) == cores_bytes(15, 8, 256, 512)      # 120 slots
     assert ws(16, 8, 256, 2048, 512) > cores_bytes(16, 8, 256, 512)       # 128 slots: tensor path
     assert ws(16, 8, 256, 2048, 512) == ws(16, 8, 256, 2048, 512, "tensor")
+    assert ws(16, 8, 256, 2048, 512) == ws(16, 8, 256, 2048, 512, "auto")
+
+
+def test_unknown_path_sizes_nothing():
+    assert ws(16, 8, 256, 2048, 512, 3) == 0
+    assert ws(16, 8, 256, 2048, 512, -1) == 0
 
 
 def test_shapes_the_tensor_path_rejects_stay_on_cuda_cores():
     for H, I in ((2000, 512), (2048, 520), (2176, 512), (64, 128)):
-        assert ws(64, 8, 256, H, I, "tensor") == cores_bytes(64, 8, 256, I)
+        assert ws(64, 8, 256, H, I) == cores_bytes(64, 8, 256, I)
+        assert ws(64, 8, 256, H, I, "tensor") == 0
 
 
 def test_calls_beyond_the_grid_limit_take_cuda_cores():
@@ -72,4 +70,4 @@ def test_calls_beyond_the_grid_limit_take_cuda_cores():
     assert ws(1 << 19, k, E, H, I, "tensor") > cores_bytes(1 << 19, k, E, I)
     for T in (1 << 20, 1 << 21):
         assert ws(T, k, E, H, I) == cores_bytes(T, k, E, I)
-        assert ws(T, k, E, H, I, "tensor") == cores_bytes(T, k, E, I)
+        assert ws(T, k, E, H, I, "tensor") == 0
