@@ -385,8 +385,10 @@ def run_gpu(args, world, rank, local):
 
 # ------------------------------------------------------------- secondary workloads
 
-SECONDARY_LEGS = ("decode_b1", "decode_b8", "decode_b32", "decode_b64", "prefill_4096", "ternarize_pack",
-                  "pack_ternary")
+SECONDARY_LEGS = ("decode_b1", "decode_b8", "decode_b32", "decode_b64", "decode_b1_streamed", "prefill_4096",
+                  "ternarize_pack", "pack_ternary")
+STREAM_SLOTS = 64    # HBM expert slots of the streamed-decode leg
+STREAM_STEPS = 200   # timed tokens of the streamed-decode leg
 DECODE_BATCHES = (1, 8, 32, 64)
 
 
@@ -473,6 +475,9 @@ def run_secondary(maple, synth, layers, dev, stream, legs=SECONDARY_LEGS, flush=
             leg["cpu_baseline"] = oracle_decode_sample(T, min(T, 4), dev)
         out[f"decode_b{T}"] = leg
 
+    if "decode_b1_streamed" in legs:
+        out["decode_b1_streamed"] = streamed_leg(maple, layers[0], dev, stream, flush, cpu)
+
     if "prefill_4096" not in legs and "ternarize_pack" not in legs:
         return out
     T = 4096
@@ -554,6 +559,79 @@ def run_secondary(maple, synth, layers, dev, stream, legs=SECONDARY_LEGS, flush=
         out["pack_ternary"]["cpu_baseline"] = oracle_pack_sample(tern, 48, exact=True)
     del tern, pk2, sc2
     return out
+
+
+def streamed_leg(maple, layer, dev, stream, flush, cpu):
+    """Batch-1 decode with the layer's experts in pinned host memory and STREAM_SLOTS
+    expert slots in HBM: per token, route (device), maple_cache_fetch (copies the
+    missing experts across the host link) and the FFN on the cache, all in one CUDA
+    graph of STREAM_STEPS distinct tokens.  Reports tokens/s, the host-link rate of the
+    expert copies (the cache's own count of copied experts x their bytes, over the
+    timed region) and, for comparison, the measured rate of a pinned host-to-device
+    copy of 256 MB."""
+    from ternary_weight_moe_02_b300 import synth
+    ex, router = layer
+    pool = maple.Experts(*[t.cpu().pin_memory() for t in ex.tensors], clamp=ex.clamp)
+    cache = maple.ExpertCache(STREAM_SLOTS, E, H, I, clamp=ex.clamp, device=dev)
+    xs = synth.tokens(2 * STREAM_STEPS, H, seed=400, device=dev)
+    logits = torch.empty((1, E), device=dev)
+    idx = torch.empty((1, K_TOP), dtype=torch.int32, device=dev)
+    w = torch.empty((1, K_TOP), device=dev)
+    idx_slot = torch.empty((1, K_TOP), dtype=torch.int32, device=dev)
+    y = torch.empty((1, H), device=dev)
+    ws_c = torch.empty(maple.maple_cache_fetch_workspace_size(1, K_TOP), dtype=torch.uint8, device=dev)
+    ws_f = torch.empty(maple.maple_moe_ffn_workspace_size(1, K_TOP, cache.experts), dtype=torch.uint8, device=dev)
+
+    def step(i):
+        x = xs[i:i + 1]
+        maple.maple_route_topk(x, router, None, K_TOP, logits, idx, w, stream=stream)
+        maple.maple_cache_fetch(pool, cache, idx, idx_slot, ws_c, stream=stream)
+        maple.maple_moe_ffn(cache.experts, x, idx_slot, w, y, ws_f, stream=stream)
+
+    def graph(start):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(STREAM_STEPS):
+                    step(start + i)
+        return g
+    g_warm, g_time = graph(STREAM_STEPS), graph(0)
+    with torch.cuda.stream(stream):
+        g_warm.replay()  # fills the cache with other tokens' experts
+        flush()
+    stream.synchronize()
+    c0 = cache.counters()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        g_time.replay()
+        b.record(stream)
+    b.synchronize()
+    sec = a.elapsed_time(b) / 1e3
+    c1 = cache.counters()
+    copied = (c1["experts_copied"] - c0["experts_copied"]) * EXPERT_BYTES
+    hits, misses = c1["hits"] - c0["hits"], c1["misses"] - c0["misses"]
+    # the host link's plain copy rate, for comparison
+    src = torch.empty(256 << 20, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        dst.copy_(src, non_blocking=True)
+        a.record(stream)
+        dst.copy_(src, non_blocking=True)
+        b.record(stream)
+    b.synchronize()
+    link = (256 << 20) / (a.elapsed_time(b) / 1e3) / 1e9
+    del src, dst
+    leg = {"value": STREAM_STEPS / sec, "unit": "tokens/s", "ms_per_token": sec * 1e3 / STREAM_STEPS,
+           "cache_slots": STREAM_SLOTS, "hit_rate": hits / max(1, hits + misses),
+           "experts_copied_per_token": (c1["experts_copied"] - c0["experts_copied"]) / STREAM_STEPS,
+           "host_link_gbs": copied / sec / 1e9, "pinned_h2d_copy_gbs": link,
+           "link_frac": copied / sec / 1e9 / link,
+           "steps": "route_topk + cache_fetch + moe_ffn per token, one CUDA graph"}
+    if cpu:
+        leg["cpu_baseline"] = oracle_decode_sample(1, 1, dev)
+    del pool, cache
+    return leg
 
 
 # ------------------------------------------------------------------- CPU (oracle) arm

@@ -291,6 +291,52 @@ MAPLE_API int maple_moe_layer_host(const uint16_t* x_host, uint16_t* x_dev, cons
                                    void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Expert cache: the experts of a layer kept in host memory (a "pool") and streamed into
+ * C slots of device memory when a step routes to them, in the manner of the Mference
+ * port that keeps MoE experts off the accelerator and reads them on demand
+ * ("Maple Preview 接入 Mference：M4 MacBook 上 500MB 内存跑 20B MoE", opening paragraph
+ * and section "接入 Mference 后的实测结果").
+ *   slots     : a layer of C experts in device memory (slots.E = C, same H and I as the
+ *               pool, 16-byte aligned arrays); its clamp is the FFN's
+ *   slot_of   : [E] device int32, the slot holding expert e or -1; all -1 initially
+ *   expert_of : [C] device int32, the expert in slot s or -1; all -1 initially
+ *   last_use  : [C] device uint32, step of the slot's last use; all 0 initially
+ *   stats     : [4] device uint32, zero initially: steps, hits, misses, experts copied
+ * The tables belong to the cache; only maple_cache_fetch changes them.
+ */
+typedef struct maple_expert_cache {
+    maple_experts slots;
+    int32_t* slot_of;
+    int32_t* expert_of;
+    uint32_t* last_use;
+    uint32_t* stats;
+} maple_expert_cache;
+
+/* Bytes of workspace maple_cache_fetch needs. */
+MAPLE_API size_t maple_cache_fetch_workspace_size(int32_t T, int32_t k);
+
+/*
+ * Makes every expert that idx routes to resident in the cache and renames idx to slots:
+ * a routed expert already in a slot is a hit (its last use is updated); each miss takes
+ * the least recently used slot that no expert of this step holds (empty slots first,
+ * ties to the lower slot), misses taken in increasing expert order, and is copied from
+ * the pool (16-byte loads across the host link).  Then
+ *   maple_moe_ffn(&cache->slots, x, idx_slot, w, ...)
+ * computes the step's FFN exactly as on the pool's experts.  Everything runs on the
+ * device, ordered on `stream` (no host synchronisation).
+ *   pool     : E experts whose arrays the device can read (pinned host memory on a
+ *              system with unified addressing, or device memory), 16-byte aligned
+ *   idx      : [T][k] int32 device; ids outside [0, E) become -1 in idx_slot
+ *   idx_slot : [T][k] int32 device, written
+ *   ws       : device workspace of maple_cache_fetch_workspace_size(T, k) bytes
+ * Limits: E <= 1024, C <= 1024, T*k <= C (every routed expert fits), each expert array
+ * a whole number of 16-byte chunks.
+ */
+MAPLE_API int maple_cache_fetch(const maple_experts* pool, const maple_expert_cache* cache, const int32_t* idx,
+                                int32_t T, int32_t k, int32_t* idx_slot, void* ws, size_t ws_bytes,
+                                void* stream);
+
+/*
  * maple_moe_ffn without a workspace argument, for callers that cannot allocate device
  * memory: a plugin whose host process owns every device allocation, code running
  * while a stream is captured into a CUDA graph (cudaMalloc is not allowed there), or

@@ -426,4 +426,46 @@ int maple_moe_layer_host(const uint16_t* x_host, uint16_t* x_dev, const uint16_t
     return ok();
 }
 
+size_t maple_cache_fetch_workspace_size(int32_t T, int32_t k) {
+    if (T < 0 || k < 1) return 0;
+    return 4 * (1 + 2 * (size_t)T * (size_t)k);
+}
+
+int maple_cache_fetch(const maple_experts* pool, const maple_expert_cache* cache, const int32_t* idx, int32_t T,
+                      int32_t k, int32_t* idx_slot, void* ws, size_t ws_bytes, void* stream) {
+    if (!pool || !cache) return fail(MAPLE_ERR_INVALID_ARG, "cache_fetch: null pool or cache");
+    const maple_experts& sl = cache->slots;
+    const int E = pool->E, C = sl.E, H = pool->H, I = pool->I;
+    if (T < 0 || k < 1 || E < 1 || C < 1 || H < 1 || I < 1)
+        return fail(MAPLE_ERR_INVALID_ARG, "cache_fetch: T=%d k=%d E=%d C=%d H=%d I=%d", T, k, E, C, H, I);
+    if (sl.H != H || sl.I != I) return fail(MAPLE_ERR_INVALID_ARG, "cache_fetch: pool and slots differ in H or I");
+    if (E > 1024 || C > 1024 || (int64_t)T * k > C)
+        return fail(MAPLE_ERR_UNSUPPORTED_SHAPE, "cache_fetch: E=%d, C=%d (both <= 1024) and T*k=%lld <= C needed", E, C,
+                    (long long)T * k);
+    if (!maple::cache_shape_ok(H, I))
+        return fail(MAPLE_ERR_UNSUPPORTED_SHAPE, "cache_fetch: an expert's arrays must be whole 16-byte chunks (H=%d I=%d)", H, I);
+    if (T == 0) return ok();
+    const maple_experts* both[2] = {pool, &sl};
+    for (const maple_experts* ex : both) {
+        if (!ex->gate || !ex->up || !ex->down || !ex->s_gate || !ex->s_up || !ex->s_down)
+            return fail(MAPLE_ERR_INVALID_ARG, "cache_fetch: null expert array");
+        if (!aligned(ex->gate, 16) || !aligned(ex->up, 16) || !aligned(ex->down, 16) || !aligned(ex->s_gate, 16) ||
+            !aligned(ex->s_up, 16) || !aligned(ex->s_down, 16))
+            return fail(MAPLE_ERR_MISALIGNED, "cache_fetch: expert arrays need 16-byte alignment");
+    }
+    if (!cache->slot_of || !cache->expert_of || !cache->last_use || !cache->stats || !idx || !idx_slot)
+        return fail(MAPLE_ERR_INVALID_ARG, "cache_fetch: null pointer");
+    if (!aligned(cache->slot_of, 4) || !aligned(cache->expert_of, 4) || !aligned(cache->last_use, 4) ||
+        !aligned(cache->stats, 4) || !aligned(idx, 4) || !aligned(idx_slot, 4) || !aligned(ws, 4))
+        return fail(MAPLE_ERR_MISALIGNED, "cache_fetch: int arrays need 4-byte alignment");
+    const size_t need = maple_cache_fetch_workspace_size(T, k);
+    if (!ws || ws_bytes < need) return fail(MAPLE_ERR_WORKSPACE, "cache_fetch: workspace %zu bytes < %zu needed", ws_bytes, need);
+    maple::DeviceInfo dev;
+    if (int st = get_device(&dev, "cache_fetch")) return st;
+    cudaError_t err = maple::launch_cache_fetch(*pool, sl, cache->slot_of, cache->expert_of, cache->last_use, cache->stats,
+                                                idx, T * k, idx_slot, static_cast<int32_t*>(ws), (cudaStream_t)stream, dev);
+    if (err != cudaSuccess) return cuda_fail(err, "cache_fetch launch");
+    return ok();
+}
+
 }  // extern "C"

@@ -149,4 +149,10 @@ cudaError_t layer_b1_max_clusters(int H, int I, int E, int* n);
 // that no copy delivers and gives every bounded wait `polls` polls.
 void layer_b1_inject_stall(int polls);
 
+// Expert cache: host-resident pool -> HBM slots (plan + copy kernels).
+bool cache_shape_ok(int H, int I);
+cudaError_t launch_cache_fetch(const ::maple_experts& pool, const ::maple_experts& slots, int32_t* slot_of,
+                               int32_t* expert_of, uint32_t* last_use, uint32_t* stats, const int32_t* idx,
+                               int S, int32_t* idx_slot, int32_t* jobs, cudaStream_t stream, const DeviceInfo& dev);
+
 }  // namespace maple

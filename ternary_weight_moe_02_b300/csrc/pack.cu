@@ -166,29 +166,56 @@ __device__ __forceinline__ float group_row_abs_sum(const uint4* r4, int n4, int 
     return v;
 }
 
+// Per-half unsigned max / min of two packed 16-bit pairs.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Folds one word (two bf16) into the running packed maxima of the magnitudes and minima
+// of (magnitude - 1) mod 2^16, which sends a zero magnitude to 0xffff, above every
+// other.  Setting bit 15 of each half first keeps the subtraction from borrowing across
+// halves: (|w| | 0x8000) - 1 lies in [0x7fff, 0xfffe], and the xor with 0x8000 maps it
+// to |w| - 1 for |w| >= 1 and to 0xffff for |w| = 0.
+__device__ __forceinline__ void fold_mag_word(uint32_t w, uint32_t& hi2, uint32_t& lo2) {
+    hi2 = max_u16x2(hi2, w & 0x7fff7fffu);
+    lo2 = min_u16x2(lo2, ((w | 0x80008000u) - 0x00010001u) ^ 0x80008000u);
+}
+
 // Largest and smallest nonzero magnitude (bf16 bits; 0x7fff when there is none) over
 // a row slot, as every lane of the row's G-lane group sees them (j: the lane's index
-// in the group).  Non-negative finite bf16 values order like their bit patterns.
+// in the group).  Non-negative finite bf16 values order like their bit patterns, so
+// both halves of every word are compared at once as unsigned 16-bit values.
 template <int G>
 __device__ __forceinline__ void group_row_mag_range(const uint4* r4, int n4, int j, uint32_t& mx, uint32_t& mn) {
-    uint32_t hi = 0u, lo = 0x7fffu;
-    for (int c = j; c < n4; c += G) {
-        const uint4 v = r4[c];
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t a = w4[i] & 0x7fffu, b = (w4[i] >> 16) & 0x7fffu;
-            hi = max(hi, max(a, b));
-            lo = min(lo, min(a != 0u ? a : 0x7fffu, b != 0u ? b : 0x7fffu));
-        }
+    uint32_t hi2 = 0u, lo2 = 0xffffffffu;
+    for (int c = j; c < n4; c += 2 * G) {
+        const uint4 v0 = r4[c];
+        const uint4 v1 = c + G < n4 ? r4[c + G] : make_uint4(0u, 0u, 0u, 0u);
+        fold_mag_word(v0.x, hi2, lo2);
+        fold_mag_word(v0.y, hi2, lo2);
+        fold_mag_word(v0.z, hi2, lo2);
+        fold_mag_word(v0.w, hi2, lo2);
+        fold_mag_word(v1.x, hi2, lo2);
+        fold_mag_word(v1.y, hi2, lo2);
+        fold_mag_word(v1.z, hi2, lo2);
+        fold_mag_word(v1.w, hi2, lo2);
     }
+    uint32_t hi = max(hi2 & 0xffffu, hi2 >> 16);
+    uint32_t lo = min(lo2 & 0xffffu, lo2 >> 16);  // (smallest nonzero magnitude - 1), or 0xffff
 #pragma unroll
     for (int o = G / 2; o >= 1; o >>= 1) {
         hi = max(hi, __shfl_xor_sync(kFullMask, hi, o));
         lo = min(lo, __shfl_xor_sync(kFullMask, lo, o));
     }
     mx = hi;
-    mn = lo;
+    mn = lo == 0xffffu ? 0x7fffu : lo + 1u;
 }
 
 // Packs the units j, j + G, ... of one row slot (two per loop trip).

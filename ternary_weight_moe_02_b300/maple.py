@@ -45,7 +45,7 @@ EXPORTED = ("maple_version", "maple_status_string", "maple_last_error",
             "maple_moe_ffn_workspace_size", "maple_moe_ffn", "maple_moe_ffn_workspace_size_ex",
             "maple_moe_ffn_ex", "maple_moe_layer_workspace_size",
             "maple_moe_layer", "maple_moe_layer_host", "maple_moe_ffn_static_scratch",
-            "maple_test_inject")
+            "maple_test_inject", "maple_cache_fetch_workspace_size", "maple_cache_fetch")
 
 
 class maple_experts(ctypes.Structure):
@@ -53,6 +53,11 @@ class maple_experts(ctypes.Structure):
                 ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
                 ("E", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
                 ("clamp", ctypes.c_float)]
+
+
+class maple_expert_cache(ctypes.Structure):
+    _fields_ = [("slots", maple_experts), ("slot_of", ctypes.c_void_p), ("expert_of", ctypes.c_void_p),
+                ("last_use", ctypes.c_void_p), ("stats", ctypes.c_void_p)]
 
 
 _P = ctypes.c_void_p
@@ -87,6 +92,11 @@ _lib.maple_moe_layer_host.argtypes = [_P, _P, _P, _P, ctypes.POINTER(maple_exper
 _lib.maple_moe_layer_host.restype = ctypes.c_int
 _lib.maple_moe_ffn_static_scratch.argtypes = [ctypes.POINTER(maple_experts), _P, _P, _P, _I32,
                                               _I32, _P, _P]
+_lib.maple_cache_fetch_workspace_size.argtypes = [_I32, _I32]
+_lib.maple_cache_fetch_workspace_size.restype = ctypes.c_size_t
+_lib.maple_cache_fetch.argtypes = [ctypes.POINTER(maple_experts), ctypes.POINTER(maple_expert_cache), _P, _I32,
+                                   _I32, _P, _P, ctypes.c_size_t, _P]
+_lib.maple_cache_fetch.restype = ctypes.c_int
 _lib.maple_test_inject.argtypes = [_I32, _I32]
 _lib.maple_test_inject.restype = ctypes.c_int
 for _n in ("maple_ternarize_pack", "maple_unpack", "maple_route_topk", "maple_group_tokens",
@@ -243,6 +253,54 @@ class Experts:
     @property
     def packed_bytes(self) -> int:
         return sum(t.numel() * t.element_size() for t in self.tensors)
+
+
+class ExpertCache:
+    """C expert slots in device memory plus the cache's tables (caller-owned tensors,
+    initialised as include/maple.h asks: slot_of and expert_of -1, last_use and stats
+    0).  `experts` is the slots seen as a layer of C experts, for maple_moe_ffn."""
+
+    def __init__(self, C: int, E: int, H: int, I: int, clamp: float = 7.0, device="cuda"):
+        bh, bi = packed_row_bytes(H), packed_row_bytes(I)
+        self.C, self.E, self.H, self.I = C, E, H, I
+        self.gate = torch.empty((C, I, bh), dtype=torch.uint8, device=device)
+        self.up = torch.empty((C, I, bh), dtype=torch.uint8, device=device)
+        self.down = torch.empty((C, H, bi), dtype=torch.uint8, device=device)
+        self.s_gate = torch.empty((C, I), dtype=torch.float32, device=device)
+        self.s_up = torch.empty((C, I), dtype=torch.float32, device=device)
+        self.s_down = torch.empty((C, H), dtype=torch.float32, device=device)
+        self.experts = Experts(self.gate, self.up, self.down, self.s_gate, self.s_up, self.s_down, clamp=clamp)
+        self.slot_of = torch.full((E,), -1, dtype=torch.int32, device=device)
+        self.expert_of = torch.full((C,), -1, dtype=torch.int32, device=device)
+        self.last_use = torch.zeros((C,), dtype=torch.int32, device=device)  # uint32 bits
+        self.stats = torch.zeros((4,), dtype=torch.int32, device=device)     # uint32 bits
+        self.struct = maple_expert_cache(self.experts.struct, self.slot_of.data_ptr(), self.expert_of.data_ptr(),
+                                         self.last_use.data_ptr(), self.stats.data_ptr())
+
+    def counters(self) -> dict:
+        st = self.stats.cpu().tolist()
+        return {"steps": st[0], "hits": st[1], "misses": st[2], "experts_copied": st[3]}
+
+
+def maple_cache_fetch_workspace_size(T: int, k: int) -> int:
+    return int(_lib.maple_cache_fetch_workspace_size(T, k))
+
+
+def maple_cache_fetch(pool: Experts, cache: ExpertCache, idx, idx_slot, ws, stream=None):
+    """Make the experts idx routes to resident in the cache; idx_slot (int32 [T, k]) gets
+    their slots.  pool: Experts whose tensors the device can read (pinned host memory or
+    device memory)."""
+    T, k = idx.shape
+    _expect(idx, torch.int32, (T, k), "idx")
+    _expect(idx_slot, torch.int32, (T, k), "idx_slot")
+    if pool.H != cache.H or pool.I != cache.I or pool.E != cache.E:
+        raise ValueError("pool and cache differ in E, H or I")
+    for t in pool.tensors:
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError("a host pool must be pinned memory")
+    _check(_lib.maple_cache_fetch(ctypes.byref(pool.struct), ctypes.byref(cache.struct), _ptr(idx), T, k,
+                                  _ptr(idx_slot), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                                  _stream(stream)), "maple_cache_fetch")
 
 
 def maple_moe_ffn_workspace_size(T: int, k: int, experts: Experts) -> int:

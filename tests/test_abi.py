@@ -218,3 +218,32 @@ def test_test_inject_validation_and_launch_error(lib):
     assert route(A16, A16, None, 1, 64, 0, 2, A16, A16, A16, None) == -1
     assert route(A16, A16, None, 1, 64, 8, 2, A16, A16, A16, None) == -4
     assert f(0, 0) == 0
+
+
+def test_cache_fetch_validation(lib):
+    """maple_cache_fetch rejects, before any launch: a null pool or cache, pool and slots
+    of different H or I, more routed slots than cache slots, arrays that are not whole
+    16-byte chunks, misaligned arrays and a short workspace."""
+    from ternary_weight_moe_02_b300.maple import maple_expert_cache, maple_experts
+    wsz = lib.maple_cache_fetch_workspace_size
+    wsz.argtypes = [I32, I32]
+    wsz.restype = ctypes.c_size_t
+    assert wsz(1, 8) == 4 * (1 + 16) and wsz(0, 8) == 4
+    f = lib.maple_cache_fetch
+    f.argtypes = [ctypes.POINTER(maple_experts), ctypes.POINTER(maple_expert_cache), P, I32, I32, P, P,
+                  ctypes.c_size_t, P]
+
+    def cache(C=12, H=2048, I=512, gate=A16):
+        return maple_expert_cache(maple_experts(gate, A16, A16, A16, A16, A16, C, H, I, 7.0), A16, A16, A16, A16)
+    pool = _experts(lib, E=32)
+    good = (ctypes.byref(pool), ctypes.byref(cache()), A16, 1, 8, A16, A16, wsz(1, 8), None)
+    assert f(None, *good[1:]) == -1
+    assert f(good[0], None, *good[2:]) == -1
+    assert f(good[0], ctypes.byref(cache(H=1024)), *good[2:]) == -1
+    assert f(good[0], ctypes.byref(cache(C=7)), *good[2:]) == -2       # T*k = 8 > C
+    assert f(ctypes.byref(_experts(lib, E=2000)), *good[1:]) == -2
+    odd = _experts(lib, E=32, H=13, I=7)
+    assert f(ctypes.byref(odd), ctypes.byref(cache(H=13, I=7)), *good[2:]) == -2
+    assert f(good[0], ctypes.byref(cache(gate=A16 + 8)), *good[2:]) == -3
+    assert f(*good[:7], wsz(1, 8) - 4, None) == -7
+    assert f(good[0], good[1], A16, 0, 8, A16, A16, 0, None) == 0

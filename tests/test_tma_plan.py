@@ -623,3 +623,20 @@ def test_multi_block_down_plan_fits_and_is_aligned():
                         off = (e * H + (blk0 + b) * TC_ROWS) * rb
                         _check(off, TC_ROWS * rb, (e + 1) * H * rb, f"multi down H={H} I={I}")
 
+
+
+def test_packed_magnitude_fold_has_no_cross_half_borrow():
+    """The already-ternary pack folds a word of two bf16 into packed 16-bit minima of
+    (|w| - 1) mod 2^16 as ((w | 0x80008000) - 0x00010001) ^ 0x80008000: every magnitude
+    in either half (any sign bit, any value in the other half) maps to |w| - 1, and 0 to
+    0xffff, above every other."""
+    m = np.arange(0x8000, dtype=np.uint64)
+    for sign in (0, 1):
+        for other in (0x0000, 0x0001, 0x7fff, 0x8000, 0xffff):
+            for low_half in (True, False):
+                h = (m | (sign << 15)).astype(np.uint64)
+                w = (h | (other << 16)) if low_half else ((h << 16) | other)
+                f = (((w | 0x80008000) - 0x00010001) ^ 0x80008000) & 0xffffffff
+                got = (f & 0xffff) if low_half else (f >> 16)
+                want = np.where(m == 0, 0xffff, m - 1)
+                assert np.array_equal(got, want), (sign, other, low_half)
