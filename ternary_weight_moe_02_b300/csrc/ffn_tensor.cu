@@ -33,11 +33,15 @@
 // stage at (k / 16) * (2NT * 16) + n * 16 + k % 16.  The split kernels store each
 // tile's rows in global memory in that order ([K / 16][2NT][16] bytes), so a K tile's
 // B stage is one contiguous block loaded by one 1-D bulk copy.  K tiles hold 160 values
-// (32 packed bytes per row).  Eight producer warps fill a ring of stages (three for
-// 128-token tiles, four for 16-token tiles); one thread issues five
+// (32 packed bytes per row).  128-token tiles: a CTA per (tile, 128-row block); eight
+// producer warps fill a ring of three stages; one thread issues five
 // tcgen05.mma.kind::f8f6f4 (K = 32 each) per stage and commits them to the stage's
-// "empty" mbarrier, which the producers wait for before refilling the stage.  All waits
-// are bounded.
+// "empty" mbarrier, which the producers wait for before refilling the stage.
+// 16-token tiles: the streaming kernels further down (persistent CTAs, items overlapped).
+// One MMA of M = 128, K = 32 occupies the tensor pipe about as long for N = 32 as for
+// N = 128 (about 100 cycles; 170 at N = 256, measured on B300), so the 16-token path is
+// bound by the MMA count, 64 per gate/up item and 16 per down item, not by N.  All
+// waits are bounded.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -62,7 +66,7 @@ template <int NT>
 struct TileCfg {
     static constexpr int kN = 2 * NT;                                    // MMA N: hi and lo rows
     static constexpr int kStageB = kChunks * kN * 16;                    // bytes of a B stage
-    static constexpr int kStages = NT >= 128 ? 3 : 4;                    // ring depth (shared memory)
+    static constexpr int kStages = 3;                                    // ring depth (shared memory)
     static constexpr int kABase = kN < 32 ? 32 : kN;                     // first A column
     static constexpr int kUsedCols = kABase + kStages * kAStride;
     static constexpr int kTmemCols = kUsedCols <= 256 ? 256 : 512;       // power of two
@@ -124,14 +128,7 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t* w) {
                  : "memory");
 }
 
-// 8 or 16 consecutive 32-bit columns of this thread's TMEM lane; complete after
-// tmem_wait_ld
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                 : "r"(taddr)
-                 : "memory");
-}
+// 16 consecutive 32-bit columns of this thread's TMEM lane; complete after tmem_wait_ld
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -497,17 +494,12 @@ __device__ __forceinline__ void tc_release(uint32_t tmem, uint32_t tmem_cols) {
 // the hi and lo accumulators of CB tokens, summed (all loads issued, then one wait).
 template <int NT, int CB>
 __device__ __forceinline__ void tmem_ld_sum(uint32_t lane_addr, int c0, float* v) {
-    constexpr int W = CB % 16 == 0 ? 16 : 8;
+    static_assert(CB % 16 == 0, "blocks of 16 columns");
     uint32_t hi[CB], lo[CB];
 #pragma unroll
-    for (int i = 0; i < CB; i += W) {
-        if constexpr (W == 16) {
-            tmem_ld16(lane_addr + (uint32_t)(c0 + i), hi + i);
-            tmem_ld16(lane_addr + (uint32_t)(NT + c0 + i), lo + i);
-        } else {
-            tmem_ld8(lane_addr + (uint32_t)(c0 + i), hi + i);
-            tmem_ld8(lane_addr + (uint32_t)(NT + c0 + i), lo + i);
-        }
+    for (int i = 0; i < CB; i += 16) {
+        tmem_ld16(lane_addr + (uint32_t)(c0 + i), hi + i);
+        tmem_ld16(lane_addr + (uint32_t)(NT + c0 + i), lo + i);
     }
     tmem_wait_ld();
 #pragma unroll
@@ -661,145 +653,400 @@ __global__ void __launch_bounds__(kThreads, 1) tc_down_kernel(TcArgs a) {
 }
 
 // Down for 16-token tiles whose whole h operand fits the B stages (K tiles <= stages):
-// grid (ceil(H / 128 / kDownBlocks), max tiles); the CTA computes kDownBlocks
-// consecutive 128-row blocks of down rows in turn.  The decode table, TMEM and the
-// barriers are set up once, the tile's h operand is loaded once and stays in shared
-// memory, and each block's packed rows (two buffers) are copied while the blocks
-// before it compute.  The A ring keeps counting across blocks.
-constexpr int kDownBlocks = 4;
+// ----------------------------------------------------------------- streaming kernels
+//
+// Decode batches (16-token tiles) through one persistent CTA per SM per stage, with the
+// work of consecutive items overlapped instead of a CTA per item run start to finish.
+// An item is one 128-row block of one tile: for gate/up the 64 gate and the same 64 up
+// rows of block b of the tile's expert, for down 128 down rows.  CTA c takes items
+// c, c + grid, c + 2 grid, ... .  The K dimension moves through a ring of kPsStages
+// stages of kPsSuper K tiles each (A in tensor memory, B in shared memory), one "full"
+// barrier per stage for both operands, so that the MMA thread waits once and issues
+// 5 kPsSuper MMAs per stage.  Roles (warps):
+//   0-15  producers: decode A into the ring, stage after stage across item boundaries:
+//         thread (w, lane) owns row 32 (w & 3) + lane and packed bytes
+//         [16 (w >> 2), +16) of the stage's 64 bytes of that row;
+//   16    lane 0 issues the MMAs into one of kPsAccs accumulators (item it into it % kPsAccs), commits
+//         each stage back to its producers, and each item to the epilogue; the warp
+//         owns the tensor memory;
+//   17    lane 0 copies the items' packed rows into npk buffers, as far ahead as the
+//         producers free them (weights: issued before the PDL wait);
+//   18    lane 0 copies the tiles' B operands (split x or h) into the ring;
+//   19-22 epilogue: drain the item's accumulator (TMEM lane quarter warp % 4), free it
+//         for a later item, and finish the item as the per-item kernels do.
+// Every wait is bounded; a wait that gives up records MAPLE_ERR_TIMEOUT and raises a
+// CTA-wide abort flag that ends the other roles' waits, after which copies and MMAs
+// still in flight are waited for before the CTA frees its tensor memory and exits.
+constexpr int kPsNT = 16;                    // tile tokens of the streaming kernels
+constexpr int kPsN = 2 * kPsNT;              // MMA N
+constexpr int kPsSuper = 2;                  // K tiles per ring stage
+constexpr int kPsKS = kPsSuper * kKTile;     // K values per stage
+constexpr int kPsRowBytesS = kPsKS / 5;      // packed bytes of a row per stage
+constexpr int kPsChunksS = kPsKS / 16;       // B chunks per stage
+constexpr int kPsStageB = kPsChunksS * kPsN * 16;
+constexpr int kPsStageCols = kPsKS / 4;      // A columns per stage (four e4m3 a column)
+// Tensor-memory plan (512 columns): the A stages in columns [0, 256), the accumulators
+// (one per item in flight) in [256, 512).  A operands above column 256 measured slower.
+constexpr int kPsStages = 3;
+constexpr int kPsAccs = 4;                   // accumulators: items in flight to the epilogue
+constexpr int kPsTmemCols = 512;
+constexpr int kPsAccCol = 256;
+__host__ __device__ constexpr int ps_stage_col(int s) { return s * kPsStageCols; }
+static_assert(kPsStages * kPsStageCols <= kPsAccCol && kPsAccCol + kPsAccs * kPsN <= kPsTmemCols,
+              "tensor-memory plan");
+constexpr int kPsProducers = 16;             // producer warps
+constexpr int kPsMmaWarp = 16, kPsPackWarp = 17, kPsBWarp = 18, kPsEpiWarp0 = 19;
+constexpr int kPsThreads = (kPsEpiWarp0 + 4) * 32;
+constexpr int kPsMaxPacked = 4;              // packed-row buffers (at least 2)
+// instruction descriptor as in TileCfg: D fp32, A and B e4m3, both K-major, N, M = 128
+constexpr uint32_t kPsIdesc = (1u << 4) | ((uint32_t)(kPsN >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
 
-__host__ __device__ constexpr size_t tc_multi_packed_bytes(int row_bytes) {
-    return ((size_t)kRows * row_bytes + 127) / 128 * 128;
+struct PsBars {
+    uint64_t pk_full[kPsMaxPacked], pk_empty[kPsMaxPacked];
+    uint64_t full[kPsStages], empty[kPsStages];
+    uint64_t acc_full[kPsAccs], acc_empty[kPsAccs];
+    uint64_t lut, fin;
+    int abort;
+};
+
+// Shared-memory plan: decode table, npk packed-row buffers of pk_stride bytes, the B
+// ring, and (gate/up) the epilogue's gate/up exchange, two buffers of [NT][128] floats.
+__host__ __device__ constexpr size_t ps_pk_stride(int row_bytes) { return ((size_t)kRows * row_bytes + 127) / 128 * 128; }
+__host__ __device__ constexpr size_t ps_b_offset(int row_bytes, int npk) {
+    return (size_t)kLutBytes + (size_t)npk * ps_pk_stride(row_bytes);
 }
-template <int NT>
-__host__ __device__ constexpr size_t tc_multi_smem_bytes(int row_bytes) {
-    return (size_t)kLutBytes + 2 * tc_multi_packed_bytes(row_bytes) + (size_t)TileCfg<NT>::kStages * TileCfg<NT>::kStageB;
+__host__ __device__ constexpr size_t ps_x_offset(int row_bytes, int npk) {
+    return ps_b_offset(row_bytes, npk) + (size_t)kPsStages * kPsStageB;
+}
+__host__ __device__ constexpr size_t ps_smem_bytes(int row_bytes, int npk, bool down) {
+    return ps_x_offset(row_bytes, npk) + (down ? 0 : 2 * (size_t)kPsNT * kRows * sizeof(float));
 }
 
-template <int NT>
-__global__ void __launch_bounds__(kThreads, 2) tc_down_multi_kernel(TcArgs a) {
-    using Cfg = TileCfg<NT>;
-    constexpr int CW = NT / 2;
-    constexpr int CB = CW < 32 ? CW : 32;
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded waits that also end when another role has raised the abort flag.  The spin
+// form (single-thread roles whose waits are short) polls without suspending, up to
+// about 4e9 cycles; the other tests once, then suspends between polls.
+__device__ __noinline__ bool ps_give_up(int* status, volatile int* abort) {
+    *abort = 1;
+    if (status != nullptr) atomicExch(status, kStatusTimeout);
+    return false;
+}
+__device__ __forceinline__ bool ps_wait_spin(uint64_t* bar, uint32_t parity, int* status, volatile int* abort) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (clock64() - t0 < 4000000000ll) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if (*abort) return false;
+    }
+    return ps_give_up(status, abort);
+}
+__device__ __forceinline__ bool ps_wait(uint64_t* bar, uint32_t parity, int* status, volatile int* abort) {
+    if (mbar_test_wait(bar, parity)) return true;
+    for (uint32_t i = 0; i < kWaitPolls; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+    }
+    return ps_give_up(status, abort);
+}
+
+// Whether any of the 128 epilogue threads (named barrier 1) passes pred = true; all of
+// them must call it.
+__device__ __forceinline__ bool bar_any_128(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\n"
+        "setp.ne.u32 q, %1, 0;\n"
+        "bar.red.or.pred p, 1, 128, q;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+// Item `item` of a stage with nblk row blocks per tile: its tile record.
+__device__ __forceinline__ int4 ps_item_tile(const TcArgs& a, int item, int nblk) {
+    return __ldcg(a.tile_info + item / nblk);
+}
+
+// Bytes [b0, b0 + 16) of a row (zeros at and past rb) as 20 words of e4m3.
+__device__ __forceinline__ void ps_decode16(uint32_t packed_s, uint32_t row_off, int rb, int b0, uint32_t lut_s,
+                                            uint32_t* words) {
+    if (b0 + 16 <= rb)
+        decode_half_tile_impl<false>(packed_s, row_off, rb, b0, lut_s, words);
+    else
+        decode_half_tile_impl<true>(packed_s, row_off, rb, b0, lut_s, words);
+}
+
+template <bool kDown>
+__global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int npk) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ TcBars bars;
-    __shared__ uint64_t pk[2];  // packed-row buffers
+    __shared__ PsBars bars;
     __shared__ uint32_t tmem_slot;
-    __shared__ int s_slot[NT];
-    __shared__ float s_w[NT];   // routing weight of the slot, times its h split scale
-    int e, n0, nv, pos0;
-    if (!tc_tile<NT>(a, blockIdx.y, e, n0, nv, pos0)) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int H = a.H, I = a.I, Bi = (I + 4) / 5;
-    const int tile = blockIdx.y;
-    const int KT = (I + kKTile - 1) / kKTile;  // at most Cfg::kStages (host check)
-    const int blk0 = blockIdx.x * kDownBlocks;
-    const int nblk = H / kRows - blk0 < kDownBlocks ? H / kRows - blk0 : kDownBlocks;
-    const uint32_t pbytes = (uint32_t)(kRows * Bi);
-    unsigned char* pkbuf[2] = {smem + kLutBytes, smem + kLutBytes + tc_multi_packed_bytes(Bi)};
-    unsigned char* stages = smem + kLutBytes + 2 * tc_multi_packed_bytes(Bi);
-    const uint8_t* dsrc = a.down + ((int64_t)e * H + (int64_t)blk0 * kRows) * Bi;  // block b at + b * pbytes
-    // loads whose first use is the epilogue
-    int slot = 0;
-    float w_slot = 0.f;
-    if (tid < nv) {
-        slot = __ldcg(a.perm + pos0 + tid);
-        w_slot = __ldcg(a.w + slot);
-    }
-    // prologue: decode table and the first two blocks' packed rows, barriers, the
-    // never-copied K tail of the last B stage zeroed, TMEM
-    int pk_last[2] = {-1, -1};  // (thread 0) last block copied into each buffer
-    if (tid == 0) {
-        mbar_init(&bars.packed, 1);
-        mbar_arrive_expect_tx(&bars.packed, (uint32_t)kLutBytes);
-        bulk_copy_g2s(smem, &g_f8_lut_image, (uint32_t)kLutBytes, &bars.packed);
-        mbar_init(&pk[0], 1);
-        mbar_init(&pk[1], 1);
-        for (int b = 0; b < 2 && b < nblk; ++b) {
-            mbar_arrive_expect_tx(&pk[b], pbytes);
-            bulk_copy_g2s(pkbuf[b], dsrc + (size_t)b * pbytes, pbytes, &pk[b]);
-            pk_last[b] = b;
+    const int H = a.H, I = a.I;
+    const int Kdim = kDown ? I : H;
+    const int rb = (Kdim + 4) / 5;                     // packed bytes per row
+    const int nblk = kDown ? H / kRows : I / (kRows / 2);
+    const int NS = (Kdim + kPsKS - 1) / kPsKS;         // ring stages per item
+    // the tile table is complete before this grid starts (see tc_tile)
+    const int n_items = __ldcg(a.tile_off + a.E) * nblk;
+    if ((int)blockIdx.x >= n_items) return;
+    const int stride = gridDim.x;
+    const size_t pk_stride = ps_pk_stride(rb);
+    unsigned char* pk0 = smem + kLutBytes;
+    unsigned char* bring = smem + ps_b_offset(rb, npk);
+    volatile int* abort = &bars.abort;
+    if (warp == kPsMmaWarp) {
+        if (lane == 0) {
+            for (int i = 0; i < kPsMaxPacked; ++i) {
+                mbar_init(&bars.pk_full[i], 1);
+                mbar_init(&bars.pk_empty[i], kPsProducers * 32);
+            }
+            for (int i = 0; i < kPsStages; ++i) {
+                mbar_init(&bars.full[i], kPsProducers * 32 + 1);  // producers + the B copy
+                mbar_init(&bars.empty[i], 1);
+            }
+            for (int i = 0; i < kPsAccs; ++i) {
+                mbar_init(&bars.acc_full[i], 1);
+                mbar_init(&bars.acc_empty[i], 128);
+            }
+            mbar_init(&bars.lut, 1);
+            mbar_init(&bars.fin, 1);
+            bars.abort = 0;
         }
-        for (int i = 0; i < kMaxStages; ++i) {
-            mbar_init(&bars.full[i], kProducerWarps * 32);
-            mbar_init(&bars.bfull[i], 1);
-            mbar_init(&bars.empty[i], 1);
-        }
-        mbar_init(&bars.done, 1);
+        __syncwarp();
+        tmem_alloc(&tmem_slot, kPsTmemCols);
     }
-    const int left = I / 16 - (KT - 1) * kChunks;  // chunks of the last K tile
-    if (left < kChunks) {
-        uint4* z = reinterpret_cast<uint4*>(stages + (size_t)(KT - 1) * Cfg::kStageB + (size_t)left * Cfg::kN * 16);
-        for (int i = tid; i < (kChunks - left) * Cfg::kN; i += blockDim.x) z[i] = make_uint4(0u, 0u, 0u, 0u);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    if (warp == kProducerWarps) tmem_alloc(&tmem_slot, Cfg::kTmemCols);
+    pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    bool ok = !__syncthreads_or(!mbar_wait_bounded(&bars.packed, 0, a.status));
     const uint32_t tmem = tmem_slot;
-    pdl_wait();  // the split h of the previous kernel
-    pdl_launch_dependents();
-    // the tile's whole h operand, one bulk copy per K tile
-    const uint8_t* bsrc = a.hs + (size_t)tile * I * Cfg::kN;
-    if (tid == 0) {
-        for (int kt = 0; kt < KT; ++kt) {
-            const int l = I / 16 - kt * kChunks;
-            const uint32_t bytes = (uint32_t)((l < kChunks ? l : kChunks) * Cfg::kN * 16);
-            mbar_arrive_expect_tx(&bars.bfull[kt], bytes);
-            bulk_copy_g2s(stages + (size_t)kt * Cfg::kStageB, bsrc + (size_t)kt * Cfg::kStageB, bytes, &bars.bfull[kt]);
-        }
-    }
-    const float h_scale = tid < NT ? a.hscale[(size_t)tile * NT + tid] : 0.f;
-    if (tid < NT) {
-        s_slot[tid] = slot;
-        s_w[tid] = w_slot * h_scale;
-    }
-    __syncthreads();
-    int b = 0;
-    for (; b < nblk && ok; ++b) {
-        const int m0 = (blk0 + b) * kRows;
-        const float row_scale =
-            warp < kProducerWarps ? a.s_down[(int64_t)e * H + m0 + 32 * (warp & 3) + lane] : 0.f;
-        ok = !__syncthreads_or(!mbar_wait_bounded(&pk[b & 1], (uint32_t)((b >> 1) & 1), a.status));
-        if (ok)
-            ok = tc_mainloop<NT, true>(smem, pkbuf[b & 1], stages, Bi, I, bsrc, tmem, bars, a.status, b * KT,
-                                       (uint32_t)(b & 1));
-        if (!ok) break;
-        // block b's packed rows are consumed (its last MMA is done): refill the buffer
-        if (tid == 0 && b + 2 < nblk) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive_expect_tx(&pk[b & 1], pbytes);
-            bulk_copy_g2s(pkbuf[b & 1], dsrc + (size_t)(b + 2) * pbytes, pbytes, &pk[b & 1]);
-            pk_last[b & 1] = b + 2;
-        }
-        // epilogue as in tc_down_kernel
-        if (warp < kProducerWarps) {
-            const int q = warp & 3, r = 32 * q + lane;
-            const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-            float* yr = a.ys + m0 + r;
-            float v[CW];
+
+    if (warp < kPsProducers) {
+        // ---- producers.  Waits are taken by every lane and voted on, so that the warp
+        // stays converged for the .sync.aligned tensor-memory stores.
+        const int q = warp & 3, part = warp >> 2, r = 32 * q + lane;
+        const uint32_t row_off = (uint32_t)(r * rb);
+        const uint32_t lut_s = smem_addr(smem) + 8u * (uint32_t)(lane & (kLutReps - 1));
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+            return __all_sync(kFullMask, ps_wait(bar, parity, a.status, abort));
+        };
+        auto pk_s = [&](int it) { return smem_addr(pk0 + (size_t)(it % npk) * pk_stride); };
+        bool ok = wait_all(&bars.lut, 0) && wait_all(&bars.pk_full[0], 0);
+        int it = 0, st = 0;
+        uint32_t g = 0;
+        uint32_t cur[20], nxt[20];
+        if (ok) ps_decode16(pk_s(0), row_off, rb, 16 * part, lut_s, cur);
+        while (ok) {
+            const int s = (int)(g % kPsStages);
+            if (g >= (uint32_t)kPsStages && !wait_all(&bars.empty[s], ((g / kPsStages) - 1) & 1)) break;
+            const uint32_t col = (uint32_t)(ps_stage_col(s) + 20 * part);
+            tmem_st16(lane_base + col, cur);
+            tmem_st4(lane_base + col + 16, cur + 16);
+            bool more = true;
+            if (st + 1 < NS) {
+                ++st;
+                ps_decode16(pk_s(it), row_off, rb, kPsRowBytesS * st + 16 * part, lut_s, nxt);
+            } else {
+                mbar_arrive(&bars.pk_empty[it % npk]);  // this item's packed rows are read
+                ++it;
+                st = 0;
+                more = (int)blockIdx.x + it * stride < n_items;
+                if (more && !wait_all(&bars.pk_full[it % npk], (uint32_t)((it / npk) & 1))) more = false;
+                if (more) ps_decode16(pk_s(it), row_off, rb, 16 * part, lut_s, nxt);
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            mbar_arrive(&bars.full[s]);
+            ++g;
+            if (!more) break;
 #pragma unroll
-            for (int cb = 0; cb < CW; cb += CB) tmem_ld_sum<NT, CB>(lane_addr, CW * (warp >> 2) + cb, v + cb);
+            for (int i = 0; i < 20; ++i) cur[i] = nxt[i];
+        }
+    } else if (warp == kPsMmaWarp) {
+        // ---- MMA issue
+        if (lane == 0) {
+            uint32_t g = 0;
+            bool ok = true;
+            for (int it = 0; ok && (int)blockIdx.x + it * stride < n_items; ++it) {
+                const int acc = it % kPsAccs;
+                if (it >= kPsAccs &&
+                    !ps_wait_spin(&bars.acc_empty[acc], (uint32_t)((it / kPsAccs - 1) & 1), a.status, abort))
+                    break;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(kPsAccCol + acc * kPsN);
+                for (int st = 0; st < NS; ++st, ++g) {
+                    const int s = (int)(g % kPsStages);
+                    if (!ps_wait_spin(&bars.full[s], (g / kPsStages) & 1, a.status, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = tmem + (uint32_t)ps_stage_col(s);
+                    const uint32_t b0 = smem_addr(bring + (size_t)s * kPsStageB);
+                    // only the K range the stage's copy filled (Kdim is a multiple of 32):
+                    // the rest of a B stage may hold another tile's rows, whose padding
+                    // rows are not guaranteed finite
+                    const int left = Kdim - st * kPsKS;
+                    const int nq = (left < kPsKS ? left : kPsKS) / 32;
 #pragma unroll
-            for (int i = 0; i < CW; ++i) {
-                const int tok = CW * (warp >> 2) + i;
-                if (tok < nv) yr[(int64_t)s_slot[tok] * H] = s_w[tok] * (row_scale * v[i]);
+                    for (int qk = 0; qk < kPsKS / 32; ++qk) {
+                        if (qk < nq) {
+                            const uint64_t bd = smem_desc(b0 + qk * 2 * (kPsN * 16), kPsN * 16, 128);
+                            mma_f8_tmem_a(d, a0 + 8 * qk, bd, kPsIdesc, (st | qk) != 0 ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(&bars.empty[s]);
+                }
+                if (ok) mma_commit(&bars.acc_full[acc]);
+            }
+            // every MMA issued has completed before the tensor memory is freed
+            mma_commit(&bars.fin);
+            mbar_wait_bounded(&bars.fin, 0, a.status);
+        }
+        __syncwarp();
+    } else if (warp == kPsPackWarp) {
+        // ---- packed rows (weights: no dependence on the previous kernel)
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars.lut, (uint32_t)kLutBytes);
+            bulk_copy_g2s(smem, &g_f8_lut_image, (uint32_t)kLutBytes, &bars.lut);
+            int it = 0;
+            for (; (int)blockIdx.x + it * stride < n_items; ++it) {
+                const int p = it % npk;
+                if (it >= npk && !ps_wait_spin(&bars.pk_empty[p], (uint32_t)((it / npk - 1) & 1), a.status, abort)) break;
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // reads done -> refill
+                const int item = (int)blockIdx.x + it * stride;
+                const int4 info = ps_item_tile(a, item, nblk);
+                const int blk = item % nblk;
+                unsigned char* dst = pk0 + (size_t)p * pk_stride;
+                if (kDown) {
+                    const uint32_t bytes = (uint32_t)(kRows * rb);
+                    mbar_arrive_expect_tx(&bars.pk_full[p], bytes);
+                    bulk_copy_g2s(dst, a.down + ((int64_t)info.x * H + (int64_t)blk * kRows) * rb, bytes,
+                                  &bars.pk_full[p]);
+                } else {
+                    const uint32_t bytes = (uint32_t)((kRows / 2) * rb);
+                    const int64_t r0 = (int64_t)info.x * I + (int64_t)blk * (kRows / 2);
+                    mbar_arrive_expect_tx(&bars.pk_full[p], 2 * bytes);
+                    bulk_copy_g2s(dst, a.gate + r0 * rb, bytes, &bars.pk_full[p]);
+                    bulk_copy_g2s(dst + bytes, a.up + r0 * rb, bytes, &bars.pk_full[p]);
+                }
+            }
+            // copies still in flight land before the CTA leaves
+            mbar_wait_bounded(&bars.lut, 0, nullptr);
+            for (int j = it - npk > 0 ? it - npk : 0; j < it; ++j)
+                mbar_wait_bounded(&bars.pk_full[j % npk], (uint32_t)((j / npk) & 1), nullptr);
+        }
+        __syncwarp();
+    } else if (warp == kPsBWarp) {
+        // ---- B operands (written by the previous kernel)
+        pdl_wait();
+        if (lane == 0) {
+            const uint8_t* bbase = kDown ? a.hs : a.xs;
+            uint32_t g = 0;
+            bool ok = true;
+            for (int it = 0; ok && (int)blockIdx.x + it * stride < n_items; ++it) {
+                const int tile = ((int)blockIdx.x + it * stride) / nblk;
+                const uint8_t* bsrc = bbase + (size_t)tile * Kdim * kPsN;
+                for (int st = 0; st < NS; ++st, ++g) {
+                    const int s = (int)(g % kPsStages);
+                    if (g >= (uint32_t)kPsStages &&
+                        !ps_wait_spin(&bars.empty[s], ((g / kPsStages) - 1) & 1, a.status, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const int left = Kdim / 16 - st * kPsChunksS;
+                    const uint32_t bytes = (uint32_t)((left < kPsChunksS ? left : kPsChunksS) * kPsN * 16);
+                    mbar_arrive_expect_tx(&bars.full[s], bytes);
+                    bulk_copy_g2s(bring + (size_t)s * kPsStageB, bsrc + (size_t)st * kPsStageB, bytes, &bars.full[s]);
+                }
+            }
+            // the last copy into each stage lands before the CTA leaves
+            for (uint32_t j = g > (uint32_t)kPsStages ? g - kPsStages : 0u; j < g; ++j)
+                mbar_wait_bounded(&bars.full[j % kPsStages], (j / kPsStages) & 1, nullptr);
+        }
+        __syncwarp();
+    } else {
+        // ---- epilogue: TMEM lane quarter warp % 4, row r of the item's 128
+        pdl_wait();
+        const int q = warp & 3, r = 32 * q + lane;
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
+        float* X = reinterpret_cast<float*>(smem + ps_x_offset(rb, npk));  // [2][NT][128]
+        for (int it = 0; (int)blockIdx.x + it * stride < n_items; ++it) {
+            const int item = (int)blockIdx.x + it * stride;
+            const int tile = item / nblk, blk = item % nblk, acc = it % kPsAccs;
+            const int4 info = ps_item_tile(a, item, nblk);
+            const int e = info.x, nv = info.z, pos0 = info.w;
+            // per-item scalars, loaded while the accumulator fills
+            float row_scale, tok_scale;
+            int slot = 0;
+            if (kDown) {
+                row_scale = a.s_down[(int64_t)e * H + blk * kRows + r];
+                float ws = 0.f;
+                if (lane < nv && lane < kPsNT) {
+                    slot = __ldcg(a.perm + pos0 + lane);
+                    ws = __ldcg(a.w + slot) * a.hscale[(size_t)tile * kPsNT + lane];
+                }
+                tok_scale = ws;
+            } else {
+                const int m = blk * (kRows / 2);
+                row_scale = r < kRows / 2 ? a.s_gate[(int64_t)e * I + m + r] : a.s_up[(int64_t)e * I + m + r - kRows / 2];
+                tok_scale = lane < kPsNT ? a.xscale[(size_t)tile * kPsNT + lane] : 0.f;
+            }
+            // one decision for all 128 epilogue threads (they meet at named barriers)
+            const bool got = ps_wait(&bars.acc_full[acc], (uint32_t)((it / kPsAccs) & 1), a.status, abort);
+            if (bar_any_128(!got)) break;
+            tc_fence_after();
+            float v[kPsNT];
+            tmem_ld_sum<kPsNT, kPsNT>(lane_addr + (uint32_t)(kPsAccCol + acc * kPsN), 0, v);
+            tc_fence_before();
+            mbar_arrive(&bars.acc_empty[acc]);  // drained into registers
+            if (kDown) {
+                float* yr = a.ys + blk * kRows + r;
+#pragma unroll
+                for (int i = 0; i < kPsNT; ++i) {
+                    const int si = __shfl_sync(kFullMask, slot, i);
+                    const float wi = __shfl_sync(kFullMask, tok_scale, i);
+                    if (i < nv) yr[(int64_t)si * H] = wi * (row_scale * v[i]);
+                }
+            } else {
+                float* Xb = X + (size_t)(it & 1) * kPsNT * kRows;
+                const bool up_side = r >= kRows / 2;
+#pragma unroll
+                for (int i = 0; i < kPsNT; ++i) {
+                    const float t = row_scale * __shfl_sync(kFullMask, tok_scale, i) * v[i];
+                    Xb[i * kRows + r] = fminf(up_side ? fmaxf(t, -a.clamp) : t, a.clamp);
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                // thread (q, lane): row pair j, tokens [8 (q >> 1), +8)
+                const int j = 32 * (q & 1) + lane, t0 = 8 * (q >> 1);
+                const int m = blk * (kRows / 2);
+#pragma unroll
+                for (int i = t0; i < t0 + 8; ++i) {
+                    const float gg = Xb[i * kRows + j], u = Xb[i * kRows + kRows / 2 + j];
+                    const __nv_bfloat16 hb = __float2bfloat16_rn(__fdividef(gg, 1.f + __expf(-gg)) * u);
+                    if (i < nv) a.hrow[(int64_t)(pos0 + i) * I + m + j] = __bfloat16_as_ushort(hb);
+                }
             }
         }
-        // the accumulator is drained before the next block's MMAs
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
     }
-    if (!ok && tid == 0) {
-        // copies that may still be in flight land before the CTA leaves
-        for (int kt = 0; kt < KT; ++kt) mbar_wait_bounded(&bars.bfull[kt], 0, nullptr);
-        for (int x = 0; x < 2; ++x)
-            if (pk_last[x] >= b) mbar_wait_bounded(&pk[x], (uint32_t)((pk_last[x] >> 1) & 1), nullptr);
-    }
-    tc_release(tmem, Cfg::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kPsMmaWarp) tmem_dealloc(tmem, kPsTmemCols);
 }
 
 __device__ __forceinline__ void bf16x8_to_f32(uint4 p, float* v) {
@@ -1030,18 +1277,43 @@ size_t ffn_tensor_scale_bytes(int S, int E) {
 
 namespace {
 
+// 16-token tiles: the streaming kernels, one CTA per SM (fewer when there are fewer
+// items), the down stage with as many packed-row buffers as shared memory holds.
+cudaError_t launch_tc_ffn_stream(const TcArgs& a, int S, cudaStream_t stream, int sm_count) {
+    constexpr int NT = kPsNT;
+    const int tiles = ffn_tensor_max_tiles(S, a.E);
+    const int Bh = (a.H + 4) / 5, Bi = (a.I + 4) / 5;
+    constexpr size_t kSmemLimit = 227 * 1024;
+    int npk_dn = kPsMaxPacked;
+    while (npk_dn > 2 && ps_smem_bytes(Bi, npk_dn, true) > kSmemLimit) --npk_dn;
+    const size_t smem_gu = ps_smem_bytes(Bh, 2, false), smem_dn = ps_smem_bytes(Bi, npk_dn, true);
+    auto gu = tc_stream_kernel<false>;
+    auto dn = tc_stream_kernel<true>;
+    cudaError_t err = ensure_dynamic_smem(gu, smem_gu);
+    if (err != cudaSuccess) return err;
+    err = ensure_dynamic_smem(dn, smem_dn);
+    if (err != cudaSuccess) return err;
+    const int64_t items_gu = (int64_t)tiles * (a.I / (kRows / 2)), items_dn = (int64_t)tiles * (a.H / kRows);
+    const int grid_gu = (int)(items_gu < sm_count ? items_gu : sm_count);
+    const int grid_dn = (int)(items_dn < sm_count ? items_dn : sm_count);
+    err = launch_pdl(tc_gather_kernel<NT>, dim3(tiles, NT / kSplitRows), dim3(256), 0, stream, a);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(gu, dim3(grid_gu), dim3(kPsThreads), smem_gu, stream, a, 2);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(tc_split_h_kernel<NT>, dim3(tiles, NT / kSplitRows), dim3(256), 0, stream, a);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(dn, dim3(grid_dn), dim3(kPsThreads), smem_dn, stream, a, npk_dn);
+}
+
 template <int NT>
 cudaError_t launch_tc_ffn(const TcArgs& a, int S, cudaStream_t stream) {
     const int tiles = ffn_tensor_max_tiles(S, a.E);
     const int Bh = (a.H + 4) / 5, Bi = (a.I + 4) / 5;
-    // 16-token tiles whose whole h operand fits the B stages take the multi-block down
-    constexpr bool kSmallTile = NT == 16;
-    const bool multi = kSmallTile && (a.I + kKTile - 1) / kKTile <= TileCfg<NT>::kStages;
     const size_t smem_gu = tc_smem_bytes<NT>(Bh);
-    const size_t smem_dn = multi ? tc_multi_smem_bytes<NT>(Bi) : tc_smem_bytes<NT>(Bi);
+    const size_t smem_dn = tc_smem_bytes<NT>(Bi);
     auto gu = tc_gateup_kernel<NT>;
-    auto dn = multi ? tc_down_multi_kernel<16> : tc_down_kernel<NT>;
-    const dim3 dn_grid(multi ? (a.H / kRows + kDownBlocks - 1) / kDownBlocks : a.H / kRows, tiles);
+    auto dn = tc_down_kernel<NT>;
+    const dim3 dn_grid(a.H / kRows, tiles);
     cudaError_t err = ensure_dynamic_smem(gu, smem_gu);
     if (err != cudaSuccess) return err;
     err = ensure_dynamic_smem(dn, smem_dn);
@@ -1099,7 +1371,7 @@ cudaError_t launch_moe_ffn_tensor(const FfnArgs& f, cudaStream_t stream, const D
     a.y = f.y;
     a.T = f.T;
     a.status = f.status;
-    err = nt == 128 ? launch_tc_ffn<128>(a, S, stream) : launch_tc_ffn<16>(a, S, stream);
+    err = nt == 128 ? launch_tc_ffn<128>(a, S, stream) : launch_tc_ffn_stream(a, S, stream, dev.sm_count);
     if (err != cudaSuccess) return err;
     const int64_t work = (int64_t)f.T * (f.H / 4);
     const int64_t want = (work + 255) / 256;
