@@ -65,18 +65,19 @@ def test_route_parity(name):
     assert np.all(np.abs(g_w.sum(axis=1) - 1) < 1e-5)
 
 
-@pytest.mark.parametrize("T,H,E", [(96, 2048, 256), (37, 2048, 250), (64, 520, 33)])
-def test_route_tiled_logits_equal_the_per_row_kernel(T, H, E):
-    """From 32 tokens on, the logits come from the register-tiled kernel; it performs
-    every logit's FMA chain and butterfly in the same order as the per-row kernel used
-    below 32 tokens, so the logits of one call equal, bit for bit, those of the same
-    tokens routed 8 at a time."""
+@pytest.mark.parametrize("T,H,E", [(300, 2048, 256), (290, 520, 33), (270, 4096, 250)])
+def test_route_logit_kernels_agree_bitwise(T, H, E):
+    """The register-tiled logits kernel (more than 256 tokens) and the staged one (at
+    most 256) run the same FMA chain per logit in the same column order and the same
+    butterfly, so the logits of one call equal, bit for bit, those of the same tokens
+    routed in smaller groups."""
     x = synth.tokens(T, H, seed=T + E, device="cuda")
     wr = synth.router_weights(E, H, seed=T + E, device="cuda")
     bias = synth.bias_normal(E, seed=T).cuda()
     whole, _, _ = _route_gpu(x, wr, bias, 8)
-    parts = [_route_gpu(x[t:t + 8].contiguous(), wr, bias, 8)[0] for t in range(0, T, 8)]
-    np.testing.assert_array_equal(whole, np.concatenate(parts))
+    for step in (8, 100):
+        parts = [_route_gpu(x[t:t + step].contiguous(), wr, bias, 8)[0] for t in range(0, T, step)]
+        np.testing.assert_array_equal(whole, np.concatenate(parts))
 
 
 def test_route_exact_ties_go_to_lower_index():
