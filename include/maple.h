@@ -200,11 +200,12 @@ MAPLE_API size_t maple_moe_ffn_workspace_size(int32_t T, int32_t k, const maple_
  * ("Maple-Preview ...", section "The shipped code does no quantization": the
  * MapleMLP forward with its clamps; "IA de 20B ...", section "Pesos ternarios":
  * skip / add / subtract.)
- * Two internal paths give results within the same bound: with at least half as many
- * slots as experts (2*T*k >= E) and H a multiple of 128, I of 64, both in [128, 2080],
- * the sums run on the tensor cores (fp8 MMAs on trits and on exact two-part splits of
- * the bf16 activations; h is rounded to bf16 between the two projections); otherwise
- * on CUDA cores with fp32 h.  maple_moe_ffn_ex below names the path explicitly.
+ * Two internal paths give results within the same bound: with at least 32 slots and an
+ * eighth as many slots as experts (T*k >= 32, 8*T*k >= E) and H a multiple of 128, I of
+ * 64, both in [128, 2080], the sums run on the tensor cores (fp8 MMAs on trits and on
+ * exact two-part splits of the bf16 activations; h is rounded to bf16 between the two
+ * projections); otherwise on CUDA cores with fp32 h.  maple_moe_ffn_ex below names the
+ * path explicitly.
  *   ex  : expert weights (see maple_experts)
  *   x   : [T][H] bf16, 16-byte aligned
  *   idx : [T][k] int32 (ids outside [0, E) contribute 0)   w : [T][k] fp32
@@ -219,7 +220,7 @@ MAPLE_API int maple_moe_ffn(const maple_experts* ex, const uint16_t* x, const in
                   void* stream);
 
 /* FFN paths of maple_moe_ffn_ex (maple_moe_ffn always takes MAPLE_FFN_AUTO). */
-#define MAPLE_FFN_AUTO 0   /* tensor cores when 2*T*k >= E and the shape allows it */
+#define MAPLE_FFN_AUTO 0   /* tensor cores when T*k >= 32, 8*T*k >= E and the shape allows it */
 #define MAPLE_FFN_CORES 1  /* CUDA-core kernels, fp32 h (any shape within the limits) */
 #define MAPLE_FFN_TENSOR 2 /* grouped tensor-core kernels (H % 128 == 0, I % 64 == 0,
                               both in [128, 2080]); MAPLE_ERR_UNSUPPORTED_SHAPE otherwise */

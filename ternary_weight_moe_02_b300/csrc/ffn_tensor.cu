@@ -1248,10 +1248,14 @@ bool ffn_tensor_allowed(int T, int k, int E, int H, int I) {
     return ffn_tensor_max_tiles(T * k, E) <= 65535;
 }
 
-// The automatic choice: the tensor path once there are at least half as many slots as
-// experts (on the Maple layer, 16 tokens and up).
+// The automatic choice: the tensor path from 32 slots on, and once there are at least
+// an eighth as many slots as experts (on the Maple layer, 4 tokens and up: measured on
+// B300 through the FFN call alone, CUDA cores / tensor cores 20.7 / 26.6 us at 2
+// tokens, 34.7 / 34.4 at 4, 59.0 / 48.1 at 8, 108.6 / 63.2 at 16).  The grouped path's
+// fixed kernels (tile table, x and h splits, combine) outweigh its MMAs below that.
 bool ffn_use_tensor(int T, int k, int E, int H, int I) {
-    return ffn_tensor_allowed(T, k, E, H, I) && 2 * (int64_t)T * k >= (int64_t)E;
+    const int64_t S = (int64_t)T * k;
+    return ffn_tensor_allowed(T, k, E, H, I) && S >= 32 && 8 * S >= (int64_t)E;
 }
 
 // H a multiple of the 128 down rows of a CTA, I of the 64 gate (and up) rows; both at

@@ -2,7 +2,7 @@
 for follows the FFN path the call will take.  The CUDA-core layout is counts, offsets,
 the slot permutation, the active-expert list and h fp32 [T*k][I], each region 256-byte
 aligned; the grouped tensor-core path adds its own regions.  That path is taken for
-2*T*k >= E on shapes it accepts (maple_moe_ffn_workspace_size_ex names a path), and
+T*k >= 32 and 8*T*k >= E on shapes it accepts (maple_moe_ffn_workspace_size_ex names a path), and
 never when its tile count would pass the 65535 limit of a grid's y dimension; asking
 for the tensor path where it cannot run sizes nothing (0: the call would be rejected)."""
 import ctypes
@@ -45,11 +45,11 @@ def test_static_scratch_limit_is_127_tokens_at_the_maple_shape():
 
 
 def test_default_choice_follows_the_slot_count():
-    assert ws(1, 8, 256, 2048, 512) == cores_bytes(1, 8, 256, 512)        # 8 slots < 256 / 2
-    assert ws(15, 8, 256, 2048, 512) == cores_bytes(15, 8, 256, 512)      # 120 slots
-    assert ws(16, 8, 256, 2048, 512) > cores_bytes(16, 8, 256, 512)       # 128 slots: tensor path
-    assert ws(16, 8, 256, 2048, 512) == ws(16, 8, 256, 2048, 512, "tensor")
-    assert ws(16, 8, 256, 2048, 512) == ws(16, 8, 256, 2048, 512, "auto")
+    assert ws(1, 8, 256, 2048, 512) == cores_bytes(1, 8, 256, 512)        # 8 slots < 256 / 8
+    assert ws(3, 8, 256, 2048, 512) == cores_bytes(3, 8, 256, 512)        # 24 slots
+    assert ws(4, 8, 256, 2048, 512) > cores_bytes(4, 8, 256, 512)         # 32 slots: tensor path
+    assert ws(4, 8, 256, 2048, 512) == ws(4, 8, 256, 2048, 512, "tensor")
+    assert ws(4, 8, 256, 2048, 512) == ws(4, 8, 256, 2048, 512, "auto")
 
 
 def test_unknown_path_sizes_nothing():
