@@ -36,6 +36,11 @@ cudaError_t launch_unpack(const uint8_t* packed, const float* scales, int64_t ro
                           float* W_out, int32_t* bad_codes, cudaStream_t stream,
                           const DeviceInfo& dev);
 
+// Router logits on the tensor cores (route_tc.cu); cudaErrorNotSupported when the
+// driver offers no tensor-map encoder.
+bool route_tc_shape_ok(const void* x, const void* Wr, int H);
+cudaError_t launch_route_logits_tc(const uint16_t* x, const uint16_t* Wr, const float* bias, int T, int H, int E,
+                                   float* logits, cudaStream_t stream, int* status);
 cudaError_t launch_route_topk(const uint16_t* x, const uint16_t* Wr, const float* bias, int T,
                               int H, int E, int k, float* logits, int32_t* idx, float* w,
                               cudaStream_t stream, const DeviceInfo& dev);

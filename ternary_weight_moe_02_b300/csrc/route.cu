@@ -223,6 +223,9 @@ cudaError_t launch_route_chunk(const uint16_t* x, const uint16_t* Wr, const floa
                 err = launch_pdl(route_logits_staged_kernel<16>, gs, dim3(kStExp * 32), smem, stream, x, Wr, bias,
                                  T, H, E, logits, status);
         }
+    } else if (vec && route_tc_shape_ok(x, Wr, H) &&
+               (err = launch_route_logits_tc(x, Wr, bias, T, H, E, logits, stream, status)) != cudaErrorNotSupported) {
+        // tensor cores (more than kStagedMaxT tokens)
     } else if (vec) {
         dim3 gt((E + kTileWarpsE * kTileExp - 1) / (kTileWarpsE * kTileExp),
                 (T + kTileWarpsT * kTileTok - 1) / (kTileWarpsT * kTileTok));

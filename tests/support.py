@@ -153,14 +153,23 @@ def assert_ffn_close(y_gpu: np.ndarray, y_ref: np.ndarray, what: str = ""):
     return err.max() / max(np.abs(y_ref).max(), 1e-30)
 
 
-def logit_bounds(x_bits, wr_bits, bias):
-    """Rigorous bound on |l_gpu - l_exact| for every (t, e)."""
+def logit_bounds(x_bits, wr_bits, bias, tensor=False):
+    """Bound on |l_gpu - l_exact| for every (t, e).  CUDA-core kernels: a lane's FMA
+    chain of H/32 terms, a 5-level butterfly and the bias add, rounded to nearest
+    (rigorous).  Tensor-core kernel (tensor=True): H/16 MMA accumulations, each adding
+    16 exact products, taken as 16 more rounding steps, plus the bias add, with the
+    unit doubled (2^-23) so that truncating additions are covered too; the hardware's
+    internal order is not published, so this one is a model, checked here."""
     H = x_bits.shape[1]
-    n = (H + 31) // 32 + 7
     mag = np.abs(synth.bits_to_float(x_bits).astype(np.float64)) @ \
         np.abs(synth.bits_to_float(wr_bits).astype(np.float64)).T
     if bias is not None:
         mag = mag + np.abs(np.asarray(bias, np.float64))[None, :]
+    if tensor:
+        n = (H + 15) // 16 + 16 + 8
+        u = 2.0 ** -23
+        return n * u / (1 - n * u) * mag + 1e-30
+    n = (H + 31) // 32 + 7
     return gamma(n) * mag + 1e-30
 
 
