@@ -16,32 +16,24 @@
 //     one product, and the epilogue adds the two accumulators and applies s.
 //
 // Per expert e with n_e routed tokens (slots grouped by expert, tiles of NT tokens;
-// NT = 128 for prefill-sized calls, 16 for decode batches):
+// NT = 64 for prefill-sized calls, 16 for decode batches):
 //   split x: each tile's token rows of x into hi/lo rows and scales;
-//   gate/up CTA: D[128 x 2NT] = A . B^T, A = 64 gate rows and the same 64 up rows of e,
-//     B = the tile's hi rows then its lo rows; epilogue
+//   gate/up item: D[128 x 2NT] = A . B^T, A = 64 gate rows and the same 64 up rows of e
+//     (interleaved), B = the tile's hi rows then its lo rows; epilogue
 //     h = silu(min(s_g g, clamp)) * clamp(s_u u, -clamp, clamp), rounded to bf16 and
 //     stored by grouped position;
 //   split h: each tile's h rows into hi/lo rows and scales, as for x;
-//   down CTA: D[128 x 2NT] = A_down . B^T over I; epilogue w_slot * s_d * s_h * D per
+//   down item: D[128 x 2NT] = A_down . B^T over I; epilogue w_slot * s_d * s_h * D per
 //     slot (fp32); a combine kernel adds each token's k slots in order 0..k-1.
 //
-// A is decoded from the packed bytes straight into tensor memory: thread r of lane
-// quarter r / 32 owns weight row r (TMEM lane r) and writes its K values as e4m3, four
-// per 32-bit column (K order from the low byte), with tcgen05.st; the MMA reads A from
+// A is decoded from the packed bytes straight into tensor memory: the thread of TMEM
+// lane r decodes that lane's weight row and writes its K values as e4m3, four per
+// 32-bit column (K order from the low byte), with tcgen05.st; the MMA reads A from
 // tensor memory.  B sits in shared memory K-major without swizzle: byte (n, k) of a
 // stage at (k / 16) * (2NT * 16) + n * 16 + k % 16.  The split kernels store each
-// tile's rows in global memory in that order ([K / 16][2NT][16] bytes), so a K tile's
-// B stage is one contiguous block loaded by one 1-D bulk copy.  K tiles hold 160 values
-// (32 packed bytes per row).  128-token tiles: a CTA per (tile, 128-row block); eight
-// producer warps fill a ring of three stages; one thread issues five
-// tcgen05.mma.kind::f8f6f4 (K = 32 each) per stage and commits them to the stage's
-// "empty" mbarrier, which the producers wait for before refilling the stage.
-// 16-token tiles: the streaming kernels further down (persistent CTAs, items overlapped).
-// One MMA of M = 128, K = 32 occupies the tensor pipe about as long for N = 32 as for
-// N = 128 (about 100 cycles; 170 at N = 256, measured on B300), so the 16-token path is
-// bound by the MMA count, 64 per gate/up item and 16 per down item, not by N.  All
-// waits are bounded.
+// tile's rows in global memory in that order ([K / 16][2NT][16] bytes), so a stage of B
+// is one contiguous block loaded by one 1-D bulk copy.  The gate/up and down items run
+// in the persistent streaming kernels below.  All waits are bounded.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -53,27 +45,10 @@ namespace maple {
 
 namespace {
 
-constexpr int kRows = 128;                 // MMA M: weight rows per CTA
-constexpr int kKTile = 160;                // K values per stage (32 packed bytes)
-constexpr int kChunks = kKTile / 16;       // 16-byte core-matrix columns per B stage
-constexpr int kMaxStages = 4;
-constexpr int kAStride = 48;               // TMEM column stride between A stages (40 used)
+constexpr int kRows = 128;                 // MMA M: weight rows of an item
+constexpr int kKTile = 160;                // K values of 32 packed bytes
 constexpr int kLutReps = 16;               // copies of the decode table, by lane & 15
 constexpr int kLutBytes = 256 * kLutReps * 8;  // 32 KB
-constexpr int kProducerWarps = 8;          // decode A, load B; warp 8 issues the MMAs
-constexpr int kThreads = (kProducerWarps + 1) * 32;
-
-template <int NT>
-struct TileCfg {
-    static constexpr int kN = 2 * NT;                                    // MMA N: hi and lo rows
-    static constexpr int kStageB = kChunks * kN * 16;                    // bytes of a B stage
-    static constexpr int kStages = 3;                                    // ring depth (shared memory)
-    static constexpr int kABase = kN < 32 ? 32 : kN;                     // first A column
-    static constexpr int kUsedCols = kABase + kStages * kAStride;
-    static constexpr int kTmemCols = kUsedCols <= 256 ? 256 : 512;       // power of two
-    // instruction descriptor: D fp32, A and B e4m3 (format 0), both K-major, N, M = 128
-    static constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
-};
 
 // ----------------------------------------------------------------- tcgen05 helpers
 // (allocation, fences, descriptors, commits and loads: tcgen05.cuh)
@@ -235,16 +210,6 @@ __device__ __forceinline__ void decode_half_tile_impl(uint32_t packed_s, uint32_
     }
 }
 
-// Bytes [32 kt + 16 h, +16) of a row: the masked variant only for the row's last tile.
-__device__ __forceinline__ void decode_half_tile(uint32_t packed_s, uint32_t row_off, int rb, int kt, int h,
-                                                 uint32_t lut_s, uint32_t* words) {
-    const int b0 = 32 * kt + 16 * h;
-    if (b0 + 16 <= rb)
-        decode_half_tile_impl<false>(packed_s, row_off, rb, b0, lut_s, words);
-    else
-        decode_half_tile_impl<true>(packed_s, row_off, rb, b0, lut_s, words);
-}
-
 struct TcArgs {
     const uint8_t* gate;
     const uint8_t* up;
@@ -273,17 +238,6 @@ struct TcArgs {
     int* status;
 };
 
-// Shared-memory plan of a grouped CTA: the decode table, the CTA's packed rows, the B
-// stages.  The epilogue reuses the packed rows and the stages.
-__host__ __device__ constexpr size_t tc_packed_offset() { return (size_t)kLutBytes; }
-__host__ __device__ constexpr size_t tc_stage_offset(int row_bytes) {
-    return (tc_packed_offset() + (size_t)kRows * row_bytes + 127) / 128 * 128;
-}
-template <int NT>
-__host__ __device__ constexpr size_t tc_smem_bytes(int row_bytes) {
-    return tc_stage_offset(row_bytes) + (size_t)TileCfg<NT>::kStages * TileCfg<NT>::kStageB;
-}
-
 // Finds the expert and token range of grid row `tile`; false when past the last tile.
 // The tile table comes from a kernel that completed before the previous one started,
 // so it is read (through L2) before this grid's PDL wait; both loads are in flight at
@@ -298,159 +252,6 @@ __device__ __forceinline__ bool tc_tile(const TcArgs& a, int tile, int& e, int& 
     nv = info.z;
     pos0 = info.w;
     return nv > 0;
-}
-
-// Barriers of a grouped CTA: full[s] (one arrival per producer thread once its A words
-// are in tensor memory), bfull[s] (the B stage's bulk-copy bytes), empty[s] (MMA
-// commit), done (commit after the last MMA), packed (bulk copy of the packed rows).
-struct TcBars {
-    uint64_t full[kMaxStages];
-    uint64_t bfull[kMaxStages];
-    uint64_t empty[kMaxStages];
-    uint64_t done;
-    uint64_t packed;
-};
-
-// Warp-specialised main loop over the K tiles of one accumulator.  Warp w < 8
-// produces: its thread owns row 32 (w & 3) + lane (the warp's TMEM lane quarter) and
-// decodes half w >> 2 of that row's 32 bytes of each K tile into A stage s (tensor
-// memory), decoding the next K tile while the current one's stores complete, then
-// arrives on full[s].  Warp 8 lane 0 waits for A and B, issues the tile's five MMAs and
-// commits empty[s], and after the last tile also done.  The ring position of K tile kt
-// is j0 + kt (a CTA that runs several accumulators in turn keeps counting); done is
-// waited for with parity done_parity.
-// B: either streamed through the ring (thread 0 copies K tile kt's chunks of the
-// operand block bsrc, fewer at the K tail, into the tile's ring stage with one bulk
-// copy, the first S up front), or, with kResidentB, already loaded whole: stage kt
-// holds K tile kt and has completed bfull[kt] once.
-// Returns false if a bounded wait gave up.
-template <int NT, bool kResidentB>
-__device__ bool tc_mainloop(const unsigned char* lut_smem, const uint8_t* packed, unsigned char* stages, int rb,
-                            int Kdim, const uint8_t* bsrc, uint32_t tmem, TcBars& bars, int* status, int j0,
-                            uint32_t done_parity) {
-    using Cfg = TileCfg<NT>;
-    constexpr int S = Cfg::kStages;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t lut_s = smem_addr(lut_smem) + 8u * (uint32_t)(lane & (kLutReps - 1));
-    const uint32_t packed_s = smem_addr(packed);
-    const int KT = (Kdim + kKTile - 1) / kKTile;
-    bool ok = true;
-    int issued = 0;  // K tiles whose B thread 0 has loaded
-    auto load_b = [&](int kt) {
-        const int s = (j0 + kt) % S;
-        const int left = Kdim / 16 - kt * kChunks;
-        const uint32_t bytes = (uint32_t)((left < kChunks ? left : kChunks) * Cfg::kN * 16);
-        mbar_arrive_expect_tx(&bars.bfull[s], bytes);
-        bulk_copy_g2s(stages + s * Cfg::kStageB, bsrc + (size_t)kt * Cfg::kStageB, bytes, &bars.bfull[s]);
-        issued = kt + 1;
-    };
-    if (warp < kProducerWarps) {
-        const int q = warp & 3, h = warp >> 2, r = 32 * q + lane;
-        const uint32_t row_off = (uint32_t)(r * rb);
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
-        if (!kResidentB && tid == 0)
-            for (int kt = 0; kt < S && kt < KT; ++kt) load_b(kt);  // every stage starts free
-        uint32_t cur[20], nxt[20];
-        decode_half_tile(packed_s, row_off, rb, 0, h, lut_s, cur);
-        for (int kt = 0; kt < KT && ok; ++kt) {
-            const int j = j0 + kt, s = j % S;
-            if (j >= S && !mbar_wait_bounded(&bars.empty[s], (uint32_t)(((j - S) / S) & 1), status)) {
-                ok = false;
-                break;
-            }
-            if (!kResidentB && kt >= S && tid == 0) load_b(kt);
-            const uint32_t col = (uint32_t)(Cfg::kABase + s * kAStride + 20 * h);
-            tmem_st16(lane_base + col, cur);
-            tmem_st4(lane_base + col + 16, cur + 16);
-            if (kt + 1 < KT) decode_half_tile(packed_s, row_off, rb, kt + 1, h, lut_s, nxt);
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-            tc_fence_before();
-            mbar_arrive(&bars.full[s]);
-#pragma unroll
-            for (int i = 0; i < 20; ++i) cur[i] = nxt[i];
-        }
-    } else if (tid == kProducerWarps * 32) {
-        for (int kt = 0; kt < KT; ++kt) {
-            const int j = j0 + kt, s = j % S;
-            const int sb = kResidentB ? kt : s;
-            const uint32_t bpar = kResidentB ? 0u : (uint32_t)((j / S) & 1);
-            if (!mbar_wait_bounded(&bars.full[s], (uint32_t)((j / S) & 1), status) ||
-                !mbar_wait_bounded(&bars.bfull[sb], bpar, status)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t a0 = tmem + (uint32_t)(Cfg::kABase + s * kAStride);
-            const uint32_t b0 = smem_addr(stages + sb * Cfg::kStageB);
-#pragma unroll
-            for (int qk = 0; qk < kKTile / 32; ++qk) {
-                const uint64_t bd = smem_desc(b0 + qk * 2 * (Cfg::kN * 16), Cfg::kN * 16, 128);
-                mma_f8_tmem_a(tmem, a0 + 8 * qk, bd, Cfg::kIdesc, (kt | qk) != 0 ? 1u : 0u);
-            }
-            mma_commit(&bars.empty[s]);
-            if (kt == KT - 1) mma_commit(&bars.done);
-        }
-    }
-    __syncwarp();
-    // every thread waits for the last MMA (the epilogue reads TMEM and reuses shared memory)
-    if (ok && !mbar_wait_bounded(&bars.done, done_parity, status)) ok = false;
-    if (!kResidentB && !ok && tid == 0) {
-        // the last B load of each stage may still be in flight: let it land first
-        for (int t = issued - S > 0 ? issued - S : 0; t < issued; ++t)
-            mbar_wait_bounded(&bars.bfull[(j0 + t) % S], (uint32_t)(((j0 + t) / S) & 1), nullptr);
-    }
-    tc_fence_after();
-    return !__syncthreads_or(!ok);
-}
-
-// CTA prologue shared by both stages: one mbarrier for the bulk copies of the decode
-// table and of the CTA's packed rows (nrows_copy rows of rb bytes from src0 and, when
-// src1 is set, as many from src1), issued first; then, while they land, the other
-// barriers, TMEM (warp 8), and zeros for the B chunks that no copy fills before the
-// MMA reads them: the K tail of the last K tile when that tile is its stage's first
-// use (a stage used before holds finite values of the same token rows, which meet zero
-// A values there).
-template <int NT>
-__device__ bool tc_prologue(unsigned char* smem, TcBars& bars, uint32_t* tmem_slot, const uint8_t* src0,
-                            const uint8_t* src1, int nrows_copy, int rb, int Kdim, int* status) {
-    using Cfg = TileCfg<NT>;
-    const int tid = threadIdx.x;
-    if (tid == 0) {
-        mbar_init(&bars.packed, 1);
-        const uint32_t bytes = (uint32_t)(nrows_copy * rb);
-        mbar_arrive_expect_tx(&bars.packed, (src1 ? 2 * bytes : bytes) + (uint32_t)kLutBytes);
-        bulk_copy_g2s(smem + tc_packed_offset(), src0, bytes, &bars.packed);
-        if (src1) bulk_copy_g2s(smem + tc_packed_offset() + bytes, src1, bytes, &bars.packed);
-        bulk_copy_g2s(smem, &g_f8_lut_image, (uint32_t)kLutBytes, &bars.packed);
-    }
-    const int KT = (Kdim + kKTile - 1) / kKTile;
-    const int left = Kdim / 16 - (KT - 1) * kChunks;  // chunks of the last K tile
-    if (KT - 1 < Cfg::kStages && left < kChunks) {
-        uint4* z = reinterpret_cast<uint4*>(smem + tc_stage_offset(rb) + (size_t)(KT - 1) * Cfg::kStageB +
-                                            (size_t)left * Cfg::kN * 16);
-        for (int i = tid; i < (kChunks - left) * Cfg::kN; i += blockDim.x) z[i] = make_uint4(0u, 0u, 0u, 0u);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    if (tid == 0) {
-        for (int i = 0; i < kMaxStages; ++i) {
-            mbar_init(&bars.full[i], kProducerWarps * 32);
-            mbar_init(&bars.bfull[i], 1);
-            mbar_init(&bars.empty[i], 1);
-        }
-        mbar_init(&bars.done, 1);
-    }
-    if ((tid >> 5) == kProducerWarps) tmem_alloc(tmem_slot, Cfg::kTmemCols);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const bool ok = mbar_wait_bounded(&bars.packed, 0, status);
-    return !__syncthreads_or(!ok);
-}
-
-__device__ __forceinline__ void tc_release(uint32_t tmem, uint32_t tmem_cols) {
-    tc_fence_before();
-    __syncthreads();
-    if ((threadIdx.x >> 5) == kProducerWarps) tmem_dealloc(tmem, tmem_cols);
 }
 
 // Columns [c0, c0 + CB) of this thread's lane plus columns [NT + c0, NT + c0 + CB):
@@ -469,220 +270,80 @@ __device__ __forceinline__ void tmem_ld_sum(uint32_t lane_addr, int c0, float* v
     for (int i = 0; i < CB; ++i) v[i] = __uint_as_float(hi[i]) + __uint_as_float(lo[i]);
 }
 
-// gate/up: grid (I / 64, max tiles); rows 0..63 of the CTA are gate rows m0..m0+63 of
-// the expert, rows 64..127 the same up rows.
-template <int NT>
-__global__ void __launch_bounds__(kThreads, 1) tc_gateup_kernel(TcArgs a) {
-    using Cfg = TileCfg<NT>;
-    constexpr int CW = NT / 2;             // token columns per epilogue warp
-    constexpr int CB = CW < 32 ? CW : 32;  // columns per tensor-memory read block
-    extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ TcBars bars;
-    __shared__ uint32_t tmem_slot;
-    __shared__ float s_xs[NT];        // split scales of the tile's x rows
-    int e, n0, nv, pos0;
-    if (!tc_tile<NT>(a, blockIdx.y, e, n0, nv, pos0)) return;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int H = a.H, I = a.I, Bh = (H + 4) / 5;
-    const int m0 = blockIdx.x * (kRows / 2);
-    const int tile = blockIdx.y;
-    // loads whose first use is the epilogue: in flight through the main loop
-    float row_scale = 0.f;  // s of the epilogue row 32 (w & 3) + lane (gate rows, then up rows)
-    if (warp < kProducerWarps) {
-        const int r = 32 * (warp & 3) + lane;
-        row_scale = r < kRows / 2 ? a.s_gate[(int64_t)e * I + m0 + r] : a.s_up[(int64_t)e * I + m0 + r - kRows / 2];
-    }
-    const uint8_t* gsrc = a.gate + ((int64_t)e * I + m0) * Bh;
-    const uint8_t* usrc = a.up + ((int64_t)e * I + m0) * Bh;
-    // everything up to here reads data no kernel of this call writes
-    bool ok = tc_prologue<NT>(smem, bars, &tmem_slot, gsrc, usrc, kRows / 2, Bh, H, a.status);
-    const uint32_t tmem = tmem_slot;
-    pdl_wait();  // the split x of the previous kernel
-    pdl_launch_dependents();
-    const float x_scale = tid < NT ? a.xscale[(size_t)tile * NT + tid] : 0.f;
-    if (ok)
-        ok = tc_mainloop<NT, false>(smem, smem + tc_packed_offset(), smem + tc_stage_offset(Bh), Bh, H,
-                                    a.xs + (size_t)tile * H * Cfg::kN, tmem, bars, a.status, 0, 0u);
-    if (tid < NT) s_xs[tid] = x_scale;
-    __syncthreads();
-    // Epilogue.  Warp w < 8 reads TMEM lanes 32 (w & 3) .. +31: rows j = 32 (w & 1) + lane
-    // of the gate side (w & 2 clear) or of the up side, tokens [CW (w >> 2), +CW) in
-    // blocks of CB, as min(s_g s_x g, clamp) or clamp(s_u s_x u, -clamp, clamp).  Of each
-    // block the gate warp keeps the first half of the tokens and the up warp (the other
-    // side of the same rows and tokens) the second half; each hands the other half to
-    // its partner through shared memory.  Each then forms h = silu(g) u for its own
-    // tokens, rounds it to bf16 and stores it by grouped position.
-    constexpr int NB = CW / CB, HB = CB / 2;
-    float* X = reinterpret_cast<float*>(smem + tc_packed_offset());  // [NT][64] exchange
-    float own[NB][HB];
-    const int q = warp & 3, j = 32 * (q & 1) + lane;
-    const bool up_side = (q & 2) != 0;
-    if (ok && warp < kProducerWarps) {
-        const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            const int c0 = CW * (warp >> 2) + b * CB;
-            float v[CB];
-            tmem_ld_sum<NT, CB>(lane_addr, c0, v);
-#pragma unroll
-            for (int i = 0; i < CB; ++i) {
-                const float t = row_scale * s_xs[c0 + i] * v[i];
-                v[i] = fminf(up_side ? fmaxf(t, -a.clamp) : t, a.clamp);
-            }
-#pragma unroll
-            for (int i = 0; i < HB; ++i) {
-                own[b][i] = up_side ? v[HB + i] : v[i];
-                X[(c0 + (up_side ? i : HB + i)) * 64 + j] = up_side ? v[i] : v[HB + i];
-            }
-        }
-    }
-    __syncthreads();
-    if (ok && warp < kProducerWarps) {
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-#pragma unroll
-            for (int i = 0; i < HB; ++i) {
-                const int tok = CW * (warp >> 2) + b * CB + (up_side ? HB + i : i);
-                const float other = X[tok * 64 + j];
-                const float g = up_side ? other : own[b][i];
-                const float u = up_side ? own[b][i] : other;
-                // silu with the fast exponential and division (a quotient of 0 once
-                // exp(-g) overflows): h is rounded to bf16 next
-                const __nv_bfloat16 hb = __float2bfloat16_rn(__fdividef(g, 1.f + __expf(-g)) * u);
-                if (tok < nv) a.hrow[(int64_t)(pos0 + tok) * I + m0 + j] = __bfloat16_as_ushort(hb);
-            }
-        }
-    }
-    tc_release(tmem, Cfg::kTmemCols);
-}
-
-// down: grid (H / 128, max tiles); the CTA's 128 rows are down rows m0..m0+127.
-template <int NT>
-__global__ void __launch_bounds__(kThreads, 1) tc_down_kernel(TcArgs a) {
-    using Cfg = TileCfg<NT>;
-    constexpr int CW = NT / 2;
-    constexpr int CB = CW < 32 ? CW : 32;
-    extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ TcBars bars;
-    __shared__ uint32_t tmem_slot;
-    __shared__ int s_slot[NT];
-    __shared__ float s_w[NT];   // routing weight of the slot, times its h split scale
-    int e, n0, nv, pos0;
-    if (!tc_tile<NT>(a, blockIdx.y, e, n0, nv, pos0)) return;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int H = a.H, I = a.I, Bi = (I + 4) / 5;
-    const int m0 = blockIdx.x * kRows;
-    const int tile = blockIdx.y;
-    // loads whose first use is the epilogue: in flight through the main loop
-    int slot = 0;
-    float w_slot = 0.f;
-    if (tid < nv) {
-        slot = __ldcg(a.perm + pos0 + tid);
-        w_slot = __ldcg(a.w + slot);
-    }
-    const float row_scale = warp < kProducerWarps ? a.s_down[(int64_t)e * H + m0 + 32 * (warp & 3) + lane] : 0.f;
-    const uint8_t* dsrc = a.down + ((int64_t)e * H + m0) * Bi;
-    // everything up to here reads data no kernel of this call writes after the grouping
-    bool ok = tc_prologue<NT>(smem, bars, &tmem_slot, dsrc, nullptr, kRows, Bi, I, a.status);
-    const uint32_t tmem = tmem_slot;
-    pdl_wait();  // the split h of the previous kernel
-    pdl_launch_dependents();
-    const float h_scale = tid < NT ? a.hscale[(size_t)tile * NT + tid] : 0.f;
-    if (ok)
-        ok = tc_mainloop<NT, false>(smem, smem + tc_packed_offset(), smem + tc_stage_offset(Bi), Bi, I,
-                                    a.hs + (size_t)tile * I * Cfg::kN, tmem, bars, a.status, 0, 0u);
-    if (tid < NT) {
-        s_slot[tid] = slot;
-        s_w[tid] = w_slot * h_scale;
-    }
-    __syncthreads();
-    // epilogue: warp w < 8 reads rows 32 (w & 3) + lane and tokens [CW (w >> 2), +CW)
-    // and stores w_slot s_h s_d D straight to the slots' rows (a warp's 32 rows of one
-    // token are 128 contiguous bytes)
-    if (ok && warp < kProducerWarps) {
-        const int q = warp & 3, r = 32 * q + lane;
-        const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-        float* yr = a.ys + m0 + r;
-        float v[CW];
-#pragma unroll
-        for (int cb = 0; cb < CW; cb += CB) tmem_ld_sum<NT, CB>(lane_addr, CW * (warp >> 2) + cb, v + cb);
-#pragma unroll
-        for (int i = 0; i < CW; ++i) {
-            const int tok = CW * (warp >> 2) + i;
-            if (tok < nv) yr[(int64_t)s_slot[tok] * H] = s_w[tok] * (row_scale * v[i]);
-        }
-    }
-    tc_release(tmem, Cfg::kTmemCols);
-}
-
-// Down for 16-token tiles whose whole h operand fits the B stages (K tiles <= stages):
 // ----------------------------------------------------------------- streaming kernels
 //
-// Decode batches (16-token tiles) through one persistent CTA per SM per stage, with the
-// work of consecutive items overlapped instead of a CTA per item run start to finish.
-// An item is one 128-row block of one tile: for gate/up the 64 gate and the same 64 up
-// rows of block b of the tile's expert, for down 128 down rows.  CTA c takes items
-// c, c + grid, c + 2 grid, ... .  The K dimension moves through a ring of kPsStages
-// stages of kPsSuper K tiles each (A in tensor memory, B in shared memory), one "full"
-// barrier per stage for both operands, so that the MMA thread waits once and issues
-// 5 kPsSuper MMAs per stage.  Roles (warps):
+// Grouped tiles of NT = 16 (decode batches) or 64 (prefill) tokens, through one
+// persistent CTA per SM per stage, with the work of consecutive items overlapped
+// instead of a CTA per item run start to finish.  An item is one 128-row block of one
+// tile: for gate/up the 64 gate and the same 64 up rows of block b of the tile's
+// expert, for down 128 down rows.  CTA c takes items c, c + grid, c + 2 grid, ... .
+// The K dimension moves through a ring of stages of kSuper K tiles each (A in tensor
+// memory, B in shared memory), one "full" barrier per stage for both operands, so that
+// the MMA thread waits once and issues 5 kSuper MMAs per stage.  Roles (warps):
 //   0-15  producers: decode A into the ring, stage after stage across item boundaries:
-//         thread (w, lane) owns row 32 (w & 3) + lane and packed bytes
-//         [16 (w >> 2), +16) of the stage's 64 bytes of that row;
-//   16    lane 0 issues the MMAs into one of kPsAccs accumulators (item it into it % kPsAccs), commits
-//         each stage back to its producers, and each item to the epilogue; the warp
-//         owns the tensor memory;
+//         thread (w, lane) owns TMEM lane 32 (w & 3) + lane and packed bytes
+//         [16 (w >> 2), +16) of each 64-byte stage of that lane's row;
+//   16    lane 0 issues the MMAs into one of kAccs accumulators (item it into
+//         it % kAccs), commits each stage back to its producers and each item to the
+//         epilogue; the warp owns the tensor memory;
 //   17    lane 0 copies the items' packed rows into npk buffers, as far ahead as the
 //         producers free them (weights: issued before the PDL wait);
 //   18    lane 0 copies the tiles' B operands (split x or h) into the ring;
-//   19-22 epilogue: drain the item's accumulator (TMEM lane quarter warp % 4), free it
-//         for a later item, and finish the item as the per-item kernels do.
+//   19-22 epilogue: drain the item's accumulator (TMEM lane quarter warp % 4) 16 tokens
+//         at a time, free it, and finish the item as the per-item kernels do.
+// Gate/up items interleave their rows in tensor memory: lane 2j holds gate row j and
+// lane 2j + 1 the same up row, so that the two values h needs meet in one warp (a
+// shuffle) instead of in shared memory.
+// One MMA of M = 128, K = 32 occupies the tensor pipe about as long at N = 32 as at
+// N = 128 (about 100 cycles, measured), so 64-token tiles (N = 128) cost about as much
+// per MMA as 16-token ones and do four times the work.
 // Every wait is bounded; a wait that gives up records MAPLE_ERR_TIMEOUT and raises a
 // CTA-wide abort flag that ends the other roles' waits, after which copies and MMAs
 // still in flight are waited for before the CTA frees its tensor memory and exits.
-constexpr int kPsNT = 16;                    // tile tokens of the streaming kernels
-constexpr int kPsN = 2 * kPsNT;              // MMA N
-constexpr int kPsSuper = 2;                  // K tiles per ring stage
-constexpr int kPsKS = kPsSuper * kKTile;     // K values per stage
-constexpr int kPsRowBytesS = kPsKS / 5;      // packed bytes of a row per stage
-constexpr int kPsChunksS = kPsKS / 16;       // B chunks per stage
-constexpr int kPsStageB = kPsChunksS * kPsN * 16;
-constexpr int kPsStageCols = kPsKS / 4;      // A columns per stage (four e4m3 a column)
-// Tensor-memory plan (512 columns): the A stages in columns [0, 256), the accumulators
-// (one per item in flight) in [256, 512).  A operands above column 256 measured slower.
-constexpr int kPsStages = 3;
-constexpr int kPsAccs = 4;                   // accumulators: items in flight to the epilogue
-constexpr int kPsTmemCols = 512;
-constexpr int kPsAccCol = 256;
-__host__ __device__ constexpr int ps_stage_col(int s) { return s * kPsStageCols; }
-static_assert(kPsStages * kPsStageCols <= kPsAccCol && kPsAccCol + kPsAccs * kPsN <= kPsTmemCols,
-              "tensor-memory plan");
 constexpr int kPsProducers = 16;             // producer warps
 constexpr int kPsMmaWarp = 16, kPsPackWarp = 17, kPsBWarp = 18, kPsEpiWarp0 = 19;
 constexpr int kPsThreads = (kPsEpiWarp0 + 4) * 32;
 constexpr int kPsMaxPacked = 4;              // packed-row buffers (at least 2)
-// instruction descriptor as in TileCfg: D fp32, A and B e4m3, both K-major, N, M = 128
-constexpr uint32_t kPsIdesc = (1u << 4) | ((uint32_t)(kPsN >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+constexpr int kPsMaxStages = 4;
+constexpr int kPsMaxAccs = 4;
+constexpr int kPsTmemCols = 512;
+constexpr int kPsAccCol = 256;               // accumulators in [256, 512), A stages below:
+                                             // A operands above column 256 measured slower
+
+template <int NT>
+struct PsCfg {
+    static constexpr int kN = 2 * NT;                         // MMA N: hi and lo rows
+    static constexpr int kSuper = 2;                          // K tiles per ring stage
+    static constexpr int kKS = kSuper * kKTile;               // K values per stage
+    static constexpr int kRowBytesS = kKS / 5;                // packed bytes of a row per stage
+    static constexpr int kChunksS = kKS / 16;                 // B chunks per stage
+    static constexpr int kStageB = kChunksS * kN * 16;        // bytes of a B stage
+    static constexpr int kStageCols = kKS / 4;                // A columns per stage
+    static constexpr int kStages = NT <= 16 ? 3 : 2;          // ring depth (shared memory)
+    static constexpr int kAccs = 256 / kN < kPsMaxAccs ? 256 / kN : kPsMaxAccs;
+    // instruction descriptor as in TileCfg: D fp32, A and B e4m3, both K-major, N, M = 128
+    static constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+    static_assert(kRowBytesS == 4 * 16, "four producer parts of 16 bytes per stage row");
+    static_assert(kStages * kStageCols <= kPsAccCol && kAccs * kN <= kPsTmemCols - kPsAccCol, "tensor memory");
+    static_assert(kStages <= kPsMaxStages && kAccs >= 2 && NT % 16 == 0 && NT <= 64, "plan");
+};
 
 struct PsBars {
     uint64_t pk_full[kPsMaxPacked], pk_empty[kPsMaxPacked];
-    uint64_t full[kPsStages], empty[kPsStages];
-    uint64_t acc_full[kPsAccs], acc_empty[kPsAccs];
+    uint64_t full[kPsMaxStages], empty[kPsMaxStages];
+    uint64_t acc_full[kPsMaxAccs], acc_empty[kPsMaxAccs];
     uint64_t lut, fin;
     int abort;
 };
 
-// Shared-memory plan: decode table, npk packed-row buffers of pk_stride bytes, the B
-// ring, and (gate/up) the epilogue's gate/up exchange, two buffers of [NT][128] floats.
+// Shared-memory plan: decode table, npk packed-row buffers of pk_stride bytes, the B ring.
 __host__ __device__ constexpr size_t ps_pk_stride(int row_bytes) { return ((size_t)kRows * row_bytes + 127) / 128 * 128; }
 __host__ __device__ constexpr size_t ps_b_offset(int row_bytes, int npk) {
     return (size_t)kLutBytes + (size_t)npk * ps_pk_stride(row_bytes);
 }
-__host__ __device__ constexpr size_t ps_x_offset(int row_bytes, int npk) {
-    return ps_b_offset(row_bytes, npk) + (size_t)kPsStages * kPsStageB;
-}
-__host__ __device__ constexpr size_t ps_smem_bytes(int row_bytes, int npk, bool down) {
-    return ps_x_offset(row_bytes, npk) + (down ? 0 : 2 * (size_t)kPsNT * kRows * sizeof(float));
+template <int NT>
+__host__ __device__ constexpr size_t ps_smem_bytes(int row_bytes, int npk) {
+    return ps_b_offset(row_bytes, npk) + (size_t)PsCfg<NT>::kStages * PsCfg<NT>::kStageB;
 }
 
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
@@ -738,11 +399,6 @@ __device__ __forceinline__ bool bar_any_128(bool pred) {
     return r != 0;
 }
 
-// Item `item` of a stage with nblk row blocks per tile: its tile record.
-__device__ __forceinline__ int4 ps_item_tile(const TcArgs& a, int item, int nblk) {
-    return __ldcg(a.tile_info + item / nblk);
-}
-
 // Bytes [b0, b0 + 16) of a row (zeros at and past rb) as 20 words of e4m3.
 __device__ __forceinline__ void ps_decode16(uint32_t packed_s, uint32_t row_off, int rb, int b0, uint32_t lut_s,
                                             uint32_t* words) {
@@ -752,8 +408,10 @@ __device__ __forceinline__ void ps_decode16(uint32_t packed_s, uint32_t row_off,
         decode_half_tile_impl<true>(packed_s, row_off, rb, b0, lut_s, words);
 }
 
-template <bool kDown>
+template <int NT, bool kDown>
 __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int npk) {
+    using Cfg = PsCfg<NT>;
+    constexpr int S = Cfg::kStages, NACC = Cfg::kAccs;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ PsBars bars;
     __shared__ uint32_t tmem_slot;
@@ -762,7 +420,7 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
     const int Kdim = kDown ? I : H;
     const int rb = (Kdim + 4) / 5;                     // packed bytes per row
     const int nblk = kDown ? H / kRows : I / (kRows / 2);
-    const int NS = (Kdim + kPsKS - 1) / kPsKS;         // ring stages per item
+    const int NS = (Kdim + Cfg::kKS - 1) / Cfg::kKS;   // ring stages per item
     // the tile table is complete before this grid starts (see tc_tile)
     const int n_items = __ldcg(a.tile_off + a.E) * nblk;
     if ((int)blockIdx.x >= n_items) return;
@@ -777,11 +435,11 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
                 mbar_init(&bars.pk_full[i], 1);
                 mbar_init(&bars.pk_empty[i], kPsProducers * 32);
             }
-            for (int i = 0; i < kPsStages; ++i) {
+            for (int i = 0; i < S; ++i) {
                 mbar_init(&bars.full[i], kPsProducers * 32 + 1);  // producers + the B copy
                 mbar_init(&bars.empty[i], 1);
             }
-            for (int i = 0; i < kPsAccs; ++i) {
+            for (int i = 0; i < NACC; ++i) {
                 mbar_init(&bars.acc_full[i], 1);
                 mbar_init(&bars.acc_empty[i], 128);
             }
@@ -802,7 +460,9 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
         // ---- producers.  Waits are taken by every lane and voted on, so that the warp
         // stays converged for the .sync.aligned tensor-memory stores.
         const int q = warp & 3, part = warp >> 2, r = 32 * q + lane;
-        const uint32_t row_off = (uint32_t)(r * rb);
+        // packed row of TMEM lane r: gate/up rows interleaved (gate j at 2j, up j at 2j + 1)
+        const int prow = kDown ? r : ((r & 1) ? kRows / 2 + (r >> 1) : (r >> 1));
+        const uint32_t row_off = (uint32_t)(prow * rb);
         const uint32_t lut_s = smem_addr(smem) + 8u * (uint32_t)(lane & (kLutReps - 1));
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         auto wait_all = [&](uint64_t* bar, uint32_t parity) {
@@ -815,15 +475,15 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
         uint32_t cur[20], nxt[20];
         if (ok) ps_decode16(pk_s(0), row_off, rb, 16 * part, lut_s, cur);
         while (ok) {
-            const int s = (int)(g % kPsStages);
-            if (g >= (uint32_t)kPsStages && !wait_all(&bars.empty[s], ((g / kPsStages) - 1) & 1)) break;
-            const uint32_t col = (uint32_t)(ps_stage_col(s) + 20 * part);
+            const int s = (int)(g % S);
+            if (g >= (uint32_t)S && !wait_all(&bars.empty[s], ((g / S) - 1) & 1)) break;
+            const uint32_t col = (uint32_t)(s * Cfg::kStageCols + 20 * part);
             tmem_st16(lane_base + col, cur);
             tmem_st4(lane_base + col + 16, cur + 16);
             bool more = true;
             if (st + 1 < NS) {
                 ++st;
-                ps_decode16(pk_s(it), row_off, rb, kPsRowBytesS * st + 16 * part, lut_s, nxt);
+                ps_decode16(pk_s(it), row_off, rb, Cfg::kRowBytesS * st + 16 * part, lut_s, nxt);
             } else {
                 mbar_arrive(&bars.pk_empty[it % npk]);  // this item's packed rows are read
                 ++it;
@@ -846,31 +506,31 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
             uint32_t g = 0;
             bool ok = true;
             for (int it = 0; ok && (int)blockIdx.x + it * stride < n_items; ++it) {
-                const int acc = it % kPsAccs;
-                if (it >= kPsAccs &&
-                    !ps_wait_spin(&bars.acc_empty[acc], (uint32_t)((it / kPsAccs - 1) & 1), a.status, abort))
+                const int acc = it % NACC;
+                if (it >= NACC &&
+                    !ps_wait_spin(&bars.acc_empty[acc], (uint32_t)((it / NACC - 1) & 1), a.status, abort))
                     break;
                 tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(kPsAccCol + acc * kPsN);
+                const uint32_t d = tmem + (uint32_t)(kPsAccCol + acc * Cfg::kN);
                 for (int st = 0; st < NS; ++st, ++g) {
-                    const int s = (int)(g % kPsStages);
-                    if (!ps_wait_spin(&bars.full[s], (g / kPsStages) & 1, a.status, abort)) {
+                    const int s = (int)(g % S);
+                    if (!ps_wait_spin(&bars.full[s], (g / S) & 1, a.status, abort)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = tmem + (uint32_t)ps_stage_col(s);
-                    const uint32_t b0 = smem_addr(bring + (size_t)s * kPsStageB);
+                    const uint32_t a0 = tmem + (uint32_t)(s * Cfg::kStageCols);
+                    const uint32_t b0 = smem_addr(bring + (size_t)s * Cfg::kStageB);
                     // only the K range the stage's copy filled (Kdim is a multiple of 32):
                     // the rest of a B stage may hold another tile's rows, whose padding
                     // rows are not guaranteed finite
-                    const int left = Kdim - st * kPsKS;
-                    const int nq = (left < kPsKS ? left : kPsKS) / 32;
+                    const int left = Kdim - st * Cfg::kKS;
+                    const int nq = (left < Cfg::kKS ? left : Cfg::kKS) / 32;
 #pragma unroll
-                    for (int qk = 0; qk < kPsKS / 32; ++qk) {
+                    for (int qk = 0; qk < Cfg::kKS / 32; ++qk) {
                         if (qk < nq) {
-                            const uint64_t bd = smem_desc(b0 + qk * 2 * (kPsN * 16), kPsN * 16, 128);
-                            mma_f8_tmem_a(d, a0 + 8 * qk, bd, kPsIdesc, (st | qk) != 0 ? 1u : 0u);
+                            const uint64_t bd = smem_desc(b0 + qk * 2 * (Cfg::kN * 16), Cfg::kN * 16, 128);
+                            mma_f8_tmem_a(d, a0 + 8 * qk, bd, Cfg::kIdesc, (st | qk) != 0 ? 1u : 0u);
                         }
                     }
                     mma_commit(&bars.empty[s]);
@@ -890,10 +550,11 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
             int it = 0;
             for (; (int)blockIdx.x + it * stride < n_items; ++it) {
                 const int p = it % npk;
-                if (it >= npk && !ps_wait_spin(&bars.pk_empty[p], (uint32_t)((it / npk - 1) & 1), a.status, abort)) break;
+                if (it >= npk && !ps_wait_spin(&bars.pk_empty[p], (uint32_t)((it / npk - 1) & 1), a.status, abort))
+                    break;
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // reads done -> refill
                 const int item = (int)blockIdx.x + it * stride;
-                const int4 info = ps_item_tile(a, item, nblk);
+                const int4 info = __ldcg(a.tile_info + item / nblk);
                 const int blk = item % nblk;
                 unsigned char* dst = pk0 + (size_t)p * pk_stride;
                 if (kDown) {
@@ -924,87 +585,108 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
             bool ok = true;
             for (int it = 0; ok && (int)blockIdx.x + it * stride < n_items; ++it) {
                 const int tile = ((int)blockIdx.x + it * stride) / nblk;
-                const uint8_t* bsrc = bbase + (size_t)tile * Kdim * kPsN;
+                const uint8_t* bsrc = bbase + (size_t)tile * Kdim * Cfg::kN;
                 for (int st = 0; st < NS; ++st, ++g) {
-                    const int s = (int)(g % kPsStages);
-                    if (g >= (uint32_t)kPsStages &&
-                        !ps_wait_spin(&bars.empty[s], ((g / kPsStages) - 1) & 1, a.status, abort)) {
+                    const int s = (int)(g % S);
+                    if (g >= (uint32_t)S && !ps_wait_spin(&bars.empty[s], ((g / S) - 1) & 1, a.status, abort)) {
                         ok = false;
                         break;
                     }
-                    const int left = Kdim / 16 - st * kPsChunksS;
-                    const uint32_t bytes = (uint32_t)((left < kPsChunksS ? left : kPsChunksS) * kPsN * 16);
+                    const int left = Kdim / 16 - st * Cfg::kChunksS;
+                    const uint32_t bytes = (uint32_t)((left < Cfg::kChunksS ? left : Cfg::kChunksS) * Cfg::kN * 16);
                     mbar_arrive_expect_tx(&bars.full[s], bytes);
-                    bulk_copy_g2s(bring + (size_t)s * kPsStageB, bsrc + (size_t)st * kPsStageB, bytes, &bars.full[s]);
+                    bulk_copy_g2s(bring + (size_t)s * Cfg::kStageB, bsrc + (size_t)st * Cfg::kStageB, bytes,
+                                  &bars.full[s]);
                 }
             }
             // the last copy into each stage lands before the CTA leaves
-            for (uint32_t j = g > (uint32_t)kPsStages ? g - kPsStages : 0u; j < g; ++j)
-                mbar_wait_bounded(&bars.full[j % kPsStages], (j / kPsStages) & 1, nullptr);
+            for (uint32_t j = g > (uint32_t)S ? g - S : 0u; j < g; ++j)
+                mbar_wait_bounded(&bars.full[j % S], (j / S) & 1, nullptr);
         }
         __syncwarp();
     } else {
-        // ---- epilogue: TMEM lane quarter warp % 4, row r of the item's 128
+        // ---- epilogue: TMEM lane quarter warp % 4, lane r of the item's 128
         pdl_wait();
+        constexpr int TPL = NT / 32 > 0 ? NT / 32 : 1;  // tokens per lane in the scale preload
         const int q = warp & 3, r = 32 * q + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-        float* X = reinterpret_cast<float*>(smem + ps_x_offset(rb, npk));  // [2][NT][128]
+        const bool up_side = !kDown && (r & 1);
         for (int it = 0; (int)blockIdx.x + it * stride < n_items; ++it) {
             const int item = (int)blockIdx.x + it * stride;
-            const int tile = item / nblk, blk = item % nblk, acc = it % kPsAccs;
-            const int4 info = ps_item_tile(a, item, nblk);
+            const int tile = item / nblk, blk = item % nblk, acc = it % NACC;
+            const int4 info = __ldcg(a.tile_info + tile);
             const int e = info.x, nv = info.z, pos0 = info.w;
-            // per-item scalars, loaded while the accumulator fills
-            float row_scale, tok_scale;
-            int slot = 0;
-            if (kDown) {
-                row_scale = a.s_down[(int64_t)e * H + blk * kRows + r];
-                float ws = 0.f;
-                if (lane < nv && lane < kPsNT) {
-                    slot = __ldcg(a.perm + pos0 + lane);
-                    ws = __ldcg(a.w + slot) * a.hscale[(size_t)tile * kPsNT + lane];
+            // per-item scalars, loaded while the accumulator fills: the row's scale, and
+            // per token (token t held by lane t % 32, register t / 32) its x split scale
+            // (gate/up) or its slot and routing weight times its h split scale (down)
+            float row_scale;
+            float tsc[TPL];
+            int tslot[TPL];
+#pragma unroll
+            for (int u = 0; u < TPL; ++u) {
+                const int t = lane + 32 * u;
+                tsc[u] = 0.f;
+                tslot[u] = 0;
+                if (t < NT) {
+                    if (kDown) {
+                        if (t < nv) {
+                            tslot[u] = __ldcg(a.perm + pos0 + t);
+                            tsc[u] = __ldcg(a.w + tslot[u]) * a.hscale[(size_t)tile * NT + t];
+                        }
+                    } else {
+                        tsc[u] = a.xscale[(size_t)tile * NT + t];
+                    }
                 }
-                tok_scale = ws;
-            } else {
-                const int m = blk * (kRows / 2);
-                row_scale = r < kRows / 2 ? a.s_gate[(int64_t)e * I + m + r] : a.s_up[(int64_t)e * I + m + r - kRows / 2];
-                tok_scale = lane < kPsNT ? a.xscale[(size_t)tile * kPsNT + lane] : 0.f;
             }
-            // one decision for all 128 epilogue threads (they meet at named barriers)
-            const bool got = ps_wait(&bars.acc_full[acc], (uint32_t)((it / kPsAccs) & 1), a.status, abort);
+            const int m = kDown ? blk * kRows : blk * (kRows / 2);
+            const int j = kDown ? r : (r >> 1);  // down row, or gate/up row pair
+            if (kDown)
+                row_scale = a.s_down[(int64_t)e * H + m + r];
+            else
+                row_scale = up_side ? a.s_up[(int64_t)e * I + m + j] : a.s_gate[(int64_t)e * I + m + j];
+            // one decision for all 128 epilogue threads (they meet at a named barrier)
+            const bool got = ps_wait(&bars.acc_full[acc], (uint32_t)((it / NACC) & 1), a.status, abort);
             if (bar_any_128(!got)) break;
             tc_fence_after();
-            float v[kPsNT];
-            tmem_ld_sum<kPsNT, kPsNT>(lane_addr + (uint32_t)(kPsAccCol + acc * kPsN), 0, v);
-            tc_fence_before();
-            mbar_arrive(&bars.acc_empty[acc]);  // drained into registers
-            if (kDown) {
-                float* yr = a.ys + blk * kRows + r;
+            const uint32_t base = lane_addr + (uint32_t)(kPsAccCol + acc * Cfg::kN);
+#pragma unroll 1
+            for (int b = 0; b < NT / 16; ++b) {
+                float v[16];
+                tmem_ld_sum<NT, 16>(base, 16 * b, v);
+                if (kDown) {
+                    float* yr = a.ys + m + r;
 #pragma unroll
-                for (int i = 0; i < kPsNT; ++i) {
-                    const int si = __shfl_sync(kFullMask, slot, i);
-                    const float wi = __shfl_sync(kFullMask, tok_scale, i);
-                    if (i < nv) yr[(int64_t)si * H] = wi * (row_scale * v[i]);
-                }
-            } else {
-                float* Xb = X + (size_t)(it & 1) * kPsNT * kRows;
-                const bool up_side = r >= kRows / 2;
+                    for (int i = 0; i < 16; ++i) {
+                        const int t = 16 * b + i;
+                        const int si = __shfl_sync(kFullMask, (t >> 5) ? tslot[TPL - 1] : tslot[0], t & 31);
+                        const float wi = __shfl_sync(kFullMask, (t >> 5) ? tsc[TPL - 1] : tsc[0], t & 31);
+                        if (t < nv) yr[(int64_t)si * H] = wi * (row_scale * v[i]);
+                    }
+                } else {
+                    // gate lane keeps tokens 16b..16b+7, the up lane 16b+8..16b+15; each
+                    // hands the other half to its partner lane (r ^ 1)
 #pragma unroll
-                for (int i = 0; i < kPsNT; ++i) {
-                    const float t = row_scale * __shfl_sync(kFullMask, tok_scale, i) * v[i];
-                    Xb[i * kRows + r] = fminf(up_side ? fmaxf(t, -a.clamp) : t, a.clamp);
-                }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                // thread (q, lane): row pair j, tokens [8 (q >> 1), +8)
-                const int j = 32 * (q & 1) + lane, t0 = 8 * (q >> 1);
-                const int m = blk * (kRows / 2);
+                    for (int i = 0; i < 16; ++i) {
+                        const int t = 16 * b + i;
+                        const float xs = __shfl_sync(kFullMask, (t >> 5) ? tsc[TPL - 1] : tsc[0], t & 31);
+                        const float tt = row_scale * xs * v[i];
+                        v[i] = fminf(up_side ? fmaxf(tt, -a.clamp) : tt, a.clamp);
+                    }
 #pragma unroll
-                for (int i = t0; i < t0 + 8; ++i) {
-                    const float gg = Xb[i * kRows + j], u = Xb[i * kRows + kRows / 2 + j];
-                    const __nv_bfloat16 hb = __float2bfloat16_rn(__fdividef(gg, 1.f + __expf(-gg)) * u);
-                    if (i < nv) a.hrow[(int64_t)(pos0 + i) * I + m + j] = __bfloat16_as_ushort(hb);
+                    for (int i = 0; i < 8; ++i) {
+                        const float got_v = __shfl_xor_sync(kFullMask, up_side ? v[i] : v[8 + i], 1);
+                        const float g = up_side ? got_v : v[i];
+                        const float u = up_side ? v[8 + i] : got_v;
+                        const int t = 16 * b + (up_side ? 8 : 0) + i;
+                        // silu with the fast exponential and division (a quotient of 0 once
+                        // exp(-g) overflows): h is rounded to bf16 next
+                        const __nv_bfloat16 hb = __float2bfloat16_rn(__fdividef(g, 1.f + __expf(-g)) * u);
+                        if (t < nv) a.hrow[(int64_t)(pos0 + t) * I + m + j] = __bfloat16_as_ushort(hb);
+                    }
                 }
             }
+            tc_fence_before();
+            mbar_arrive(&bars.acc_empty[acc]);  // drained
         }
     }
     tc_fence_before();
@@ -1192,10 +874,9 @@ __global__ void __launch_bounds__(1024) tc_tile_prefix_kernel(const int32_t* __r
 
 }  // namespace
 
-// Token-tile width of a call: 128 when the slots average at least 64 per expert
-// (prefill), 16 otherwise (decode batches: fewer padded MMA columns and a smaller
-// TMEM allocation, so that two CTAs share an SM).
-int ffn_tensor_tile_tokens(int S, int E) { return (int64_t)S >= 64 * (int64_t)E ? 128 : 16; }
+// Token-tile width of a call: 64 when the slots average at least 64 per expert
+// (prefill), 16 otherwise (decode batches: fewer padded MMA columns).
+int ffn_tensor_tile_tokens(int S, int E) { return (int64_t)S >= 64 * (int64_t)E ? 64 : 16; }
 
 // An upper bound of the number of tiles, sum over experts of ceil(n_e / NT).
 int ffn_tensor_max_tiles(int S, int E) {
@@ -1203,9 +884,10 @@ int ffn_tensor_max_tiles(int S, int E) {
     return (S + nt - 1) / nt + (E < S ? E : S);
 }
 
-// Whether the grouped kernels can take a call: a shape they support, and at most
-// 65535 tiles (the tiles sit in gridDim.y; beyond that, more than about 8.3 million
-// slots, only the CUDA-core kernels run).
+// Whether the grouped kernels can take a call: a shape they support, and at most 65535
+// tiles, which bounds the operand workspace (2NT (H + I) bytes a tile: 21 GB at the
+// Maple shape); beyond that, more than about 4.2 million slots, only the CUDA-core
+// kernels run.
 bool ffn_tensor_allowed(int T, int k, int E, int H, int I) {
     if (!ffn_tensor_shape_ok(H, I) || T < 1) return false;
     return ffn_tensor_max_tiles(T * k, E) <= 65535;
@@ -1221,9 +903,9 @@ bool ffn_use_tensor(int T, int k, int E, int H, int I) {
     return ffn_tensor_allowed(T, k, E, H, I) && S >= 32 && 8 * S >= (int64_t)E;
 }
 
-// H a multiple of the 128 down rows of a CTA, I of the 64 gate (and up) rows; both at
-// least 128, and at most 2080 so that a CTA's packed rows and its four B stages fit in
-// shared memory.
+// H a multiple of the 128 down rows of an item, I of the 64 gate (and up) rows; both at
+// least 128, and at most 2080 so that a CTA's two packed-row buffers and its B stages
+// fit in shared memory.
 bool ffn_tensor_shape_ok(int H, int I) {
     return H % kRows == 0 && I % (kRows / 2) == 0 && H >= 128 && I >= 128 && H <= 2080 && I <= 2080;
 }
@@ -1244,18 +926,22 @@ size_t ffn_tensor_scale_bytes(int S, int E) {
 
 namespace {
 
-// 16-token tiles: the streaming kernels, one CTA per SM (fewer when there are fewer
-// items), the down stage with as many packed-row buffers as shared memory holds.
+// The streaming kernels, one CTA per SM (fewer when there are fewer items), each stage
+// with as many packed-row buffers (2 to 4) as shared memory holds.
+template <int NT>
 cudaError_t launch_tc_ffn_stream(const TcArgs& a, int S, cudaStream_t stream, int sm_count) {
-    constexpr int NT = kPsNT;
     const int tiles = ffn_tensor_max_tiles(S, a.E);
     const int Bh = (a.H + 4) / 5, Bi = (a.I + 4) / 5;
     constexpr size_t kSmemLimit = 227 * 1024;
-    int npk_dn = kPsMaxPacked;
-    while (npk_dn > 2 && ps_smem_bytes(Bi, npk_dn, true) > kSmemLimit) --npk_dn;
-    const size_t smem_gu = ps_smem_bytes(Bh, 2, false), smem_dn = ps_smem_bytes(Bi, npk_dn, true);
-    auto gu = tc_stream_kernel<false>;
-    auto dn = tc_stream_kernel<true>;
+    auto npk_for = [&](int rb) {
+        int n = kPsMaxPacked;
+        while (n > 2 && ps_smem_bytes<NT>(rb, n) > kSmemLimit) --n;
+        return n;
+    };
+    const int npk_gu = npk_for(Bh), npk_dn = npk_for(Bi);
+    const size_t smem_gu = ps_smem_bytes<NT>(Bh, npk_gu), smem_dn = ps_smem_bytes<NT>(Bi, npk_dn);
+    auto gu = tc_stream_kernel<NT, false>;
+    auto dn = tc_stream_kernel<NT, true>;
     cudaError_t err = ensure_dynamic_smem(gu, smem_gu);
     if (err != cudaSuccess) return err;
     err = ensure_dynamic_smem(dn, smem_dn);
@@ -1265,33 +951,11 @@ cudaError_t launch_tc_ffn_stream(const TcArgs& a, int S, cudaStream_t stream, in
     const int grid_dn = (int)(items_dn < sm_count ? items_dn : sm_count);
     err = launch_pdl(tc_gather_kernel<NT>, dim3(tiles, NT / kSplitRows), dim3(256), 0, stream, a);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(gu, dim3(grid_gu), dim3(kPsThreads), smem_gu, stream, a, 2);
+    err = launch_pdl(gu, dim3(grid_gu), dim3(kPsThreads), smem_gu, stream, a, npk_gu);
     if (err != cudaSuccess) return err;
     err = launch_pdl(tc_split_h_kernel<NT>, dim3(tiles, NT / kSplitRows), dim3(256), 0, stream, a);
     if (err != cudaSuccess) return err;
     return launch_pdl(dn, dim3(grid_dn), dim3(kPsThreads), smem_dn, stream, a, npk_dn);
-}
-
-template <int NT>
-cudaError_t launch_tc_ffn(const TcArgs& a, int S, cudaStream_t stream) {
-    const int tiles = ffn_tensor_max_tiles(S, a.E);
-    const int Bh = (a.H + 4) / 5, Bi = (a.I + 4) / 5;
-    const size_t smem_gu = tc_smem_bytes<NT>(Bh);
-    const size_t smem_dn = tc_smem_bytes<NT>(Bi);
-    auto gu = tc_gateup_kernel<NT>;
-    auto dn = tc_down_kernel<NT>;
-    const dim3 dn_grid(a.H / kRows, tiles);
-    cudaError_t err = ensure_dynamic_smem(gu, smem_gu);
-    if (err != cudaSuccess) return err;
-    err = ensure_dynamic_smem(dn, smem_dn);
-    if (err != cudaSuccess) return err;
-    err = launch_pdl(tc_gather_kernel<NT>, dim3(tiles, NT / kSplitRows), dim3(256), 0, stream, a);
-    if (err != cudaSuccess) return err;
-    err = launch_pdl(gu, dim3(a.I / (kRows / 2), tiles), dim3(kThreads), smem_gu, stream, a);
-    if (err != cudaSuccess) return err;
-    err = launch_pdl(tc_split_h_kernel<NT>, dim3(tiles, NT / kSplitRows), dim3(256), 0, stream, a);
-    if (err != cudaSuccess) return err;
-    return launch_pdl(dn, dn_grid, dim3(kThreads), smem_dn, stream, a);
 }
 
 }  // namespace
@@ -1338,7 +1002,8 @@ cudaError_t launch_moe_ffn_tensor(const FfnArgs& f, cudaStream_t stream, const D
     a.y = f.y;
     a.T = f.T;
     a.status = f.status;
-    err = nt == 128 ? launch_tc_ffn<128>(a, S, stream) : launch_tc_ffn_stream(a, S, stream, dev.sm_count);
+    err = nt == 64 ? launch_tc_ffn_stream<64>(a, S, stream, dev.sm_count)
+                  : launch_tc_ffn_stream<16>(a, S, stream, dev.sm_count);
     if (err != cudaSuccess) return err;
     const int64_t work = (int64_t)f.T * (f.H / 4);
     const int64_t want = (work + 255) / 256;

@@ -120,8 +120,8 @@ def test_ffn_decode_batches_full_layer(layer256, router256, T):
 
 def test_ffn_prefill_4096_every_tile(layer256, router256):
     """4096-token prefill, Zipf(1.1) router bias; the GPU runs all tokens in one call
-    (grouped tensor-core path, 128-token tiles).  The oracle checks, for every expert
-    with a non-zero load, the first and the last token of each of its 128-token tiles
+    (grouped tensor-core path, 64-token tiles).  The oracle checks, for every expert
+    with a non-zero load, the first and the last token of each of its 64-token tiles
     (tiles follow the stable grouping of slots by expert, which the oracle's own
     grouping gives), plus the first tokens of the busiest and the idlest expert, the
     first and last token of the call and random picks: every tile record of the call,
@@ -129,7 +129,7 @@ def test_ffn_prefill_4096_every_tile(layer256, router256):
     the grouping, has at least one checked token."""
     from support import oracle_moe_ffn_rows
     packed, ex = layer256
-    T, k, E, NT = 4096, 8, 256, 128
+    T, k, E, NT = 4096, 8, 256, 64
     x = synth.tokens(T, 2048, seed=42)
     idx, w32 = _route_oracle(x, router256.cpu(), synth.bias_zipf(E, seed=0, gamma=1.0), k)
     counts, offsets, perm = oracle.group(idx, E)

@@ -58,7 +58,8 @@ def test_tensor_path_shapes(E, H, I, T, k):
 
 def test_tensor_path_several_token_tiles_per_expert():
     """Four experts, 300 tokens, top-2: about 150 tokens per expert, so each expert
-    spans two 128-token tiles; expert 0 gets exactly 128 + 1 tokens."""
+    spans three 64-token tiles; expert 0 gets exactly 128 + 1 tokens (its last tile
+    holds one token)."""
     E, H, I, T, k = 4, 256, 128, 300, 2
     packed, ex = _layer(E, H, I, seed=11)
     x = synth.tokens(T, H, seed=11)
@@ -74,7 +75,7 @@ def test_tensor_path_several_token_tiles_per_expert():
 
 def test_tensor_path_many_slots_chunked_grouping():
     """5600 slots (700 tokens, top-8, 16 experts): the grouping runs over six chunks of
-    1024 slots (the last one partial) and the tiles are 128 tokens wide."""
+    1024 slots (the last one partial) and the tiles are 64 tokens wide."""
     E, H, I, T, k = 16, 256, 128, 700, 8
     packed, ex = _layer(E, H, I, seed=17)
     x = synth.tokens(T, H, seed=17)

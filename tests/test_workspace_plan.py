@@ -3,7 +3,7 @@ for follows the FFN path the call will take.  The CUDA-core layout is counts, of
 the slot permutation, the active-expert list and h fp32 [T*k][I], each region 256-byte
 aligned; the grouped tensor-core path adds its own regions.  That path is taken for
 T*k >= 32 and 8*T*k >= E on shapes it accepts (maple_moe_ffn_workspace_size_ex names a path), and
-never when its tile count would pass the 65535 limit of a grid's y dimension; asking
+never when its tile count would pass 65535 (a cap on its operand workspace); asking
 for the tensor path where it cannot run sizes nothing (0: the call would be rejected)."""
 import ctypes
 
@@ -64,10 +64,10 @@ def test_shapes_the_tensor_path_rejects_stay_on_cuda_cores():
 
 
 def test_calls_beyond_the_grid_limit_take_cuda_cores():
-    """128-token tiles: at most S/128 + E tiles.  2^19 tokens x 8 slots (33,024 tiles)
-    fit; 2^20 tokens (65,792 tiles) and the API's maximum of 2^24 slots do not."""
+    """64-token tiles: at most S/64 + E tiles.  2^18 tokens x 8 slots (33,024 tiles)
+    fit; 2^19 tokens (65,792 tiles) and the API's maximum of 2^24 slots do not."""
     E, H, I, k = 256, 2048, 512, 8
-    assert ws(1 << 19, k, E, H, I, "tensor") > cores_bytes(1 << 19, k, E, I)
-    for T in (1 << 20, 1 << 21):
+    assert ws(1 << 18, k, E, H, I, "tensor") > cores_bytes(1 << 18, k, E, I)
+    for T in (1 << 19, 1 << 21):
         assert ws(T, k, E, H, I) == cores_bytes(T, k, E, I)
         assert ws(T, k, E, H, I, "tensor") == 0
