@@ -415,6 +415,7 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ PsBars bars;
     __shared__ uint32_t tmem_slot;
+    __shared__ float2 s_tok[NACC][NT];  // per-token epilogue values of the items in flight
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, I = a.I;
     const int Kdim = kDown ? I : H;
@@ -607,7 +608,6 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
     } else {
         // ---- epilogue: TMEM lane quarter warp % 4, lane r of the item's 128
         pdl_wait();
-        constexpr int TPL = NT / 32 > 0 ? NT / 32 : 1;  // tokens per lane in the scale preload
         const int q = warp & 3, r = 32 * q + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
         const bool up_side = !kDown && (r & 1);
@@ -616,34 +616,30 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
             const int tile = item / nblk, blk = item % nblk, acc = it % NACC;
             const int4 info = __ldcg(a.tile_info + tile);
             const int e = info.x, nv = info.z, pos0 = info.w;
-            // per-item scalars, loaded while the accumulator fills: the row's scale, and
-            // per token (token t held by lane t % 32, register t / 32) its x split scale
-            // (gate/up) or its slot and routing weight times its h split scale (down)
-            float row_scale;
-            float tsc[TPL];
-            int tslot[TPL];
+            // per-token values of the item, loaded by the first epilogue warp while the
+            // accumulator fills and published in shared memory (the named barrier below
+            // orders them): the x split scale (gate/up), or the slot and the routing
+            // weight times the h split scale (down)
+            if (warp == kPsEpiWarp0) {
 #pragma unroll
-            for (int u = 0; u < TPL; ++u) {
-                const int t = lane + 32 * u;
-                tsc[u] = 0.f;
-                tslot[u] = 0;
-                if (t < NT) {
-                    if (kDown) {
-                        if (t < nv) {
-                            tslot[u] = __ldcg(a.perm + pos0 + t);
-                            tsc[u] = __ldcg(a.w + tslot[u]) * a.hscale[(size_t)tile * NT + t];
+                for (int t = lane; t < NT; t += 32) {
+                    float2 tv = make_float2(0.f, 0.f);
+                    if (t < nv) {
+                        if (kDown) {
+                            const int slot = __ldcg(a.perm + pos0 + t);
+                            tv = make_float2(__int_as_float(slot),
+                                             __ldcg(a.w + slot) * a.hscale[(size_t)tile * NT + t]);
+                        } else {
+                            tv.x = a.xscale[(size_t)tile * NT + t];
                         }
-                    } else {
-                        tsc[u] = a.xscale[(size_t)tile * NT + t];
                     }
+                    s_tok[acc][t] = tv;
                 }
             }
             const int m = kDown ? blk * kRows : blk * (kRows / 2);
             const int j = kDown ? r : (r >> 1);  // down row, or gate/up row pair
-            if (kDown)
-                row_scale = a.s_down[(int64_t)e * H + m + r];
-            else
-                row_scale = up_side ? a.s_up[(int64_t)e * I + m + j] : a.s_gate[(int64_t)e * I + m + j];
+            const float row_scale = kDown ? a.s_down[(int64_t)e * H + m + r]
+                                          : (up_side ? a.s_up[(int64_t)e * I + m + j] : a.s_gate[(int64_t)e * I + m + j]);
             // one decision for all 128 epilogue threads (they meet at a named barrier)
             const bool got = ps_wait(&bars.acc_full[acc], (uint32_t)((it / NACC) & 1), a.status, abort);
             if (bar_any_128(!got)) break;
@@ -658,18 +654,15 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int t = 16 * b + i;
-                        const int si = __shfl_sync(kFullMask, (t >> 5) ? tslot[TPL - 1] : tslot[0], t & 31);
-                        const float wi = __shfl_sync(kFullMask, (t >> 5) ? tsc[TPL - 1] : tsc[0], t & 31);
-                        if (t < nv) yr[(int64_t)si * H] = wi * (row_scale * v[i]);
+                        const float2 tv = s_tok[acc][t];
+                        if (t < nv) yr[(int64_t)__float_as_int(tv.x) * H] = tv.y * (row_scale * v[i]);
                     }
                 } else {
                     // gate lane keeps tokens 16b..16b+7, the up lane 16b+8..16b+15; each
                     // hands the other half to its partner lane (r ^ 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const int t = 16 * b + i;
-                        const float xs = __shfl_sync(kFullMask, (t >> 5) ? tsc[TPL - 1] : tsc[0], t & 31);
-                        const float tt = row_scale * xs * v[i];
+                        const float tt = row_scale * s_tok[acc][16 * b + i].x * v[i];
                         v[i] = fminf(up_side ? fmaxf(tt, -a.clamp) : tt, a.clamp);
                     }
 #pragma unroll
