@@ -19,7 +19,8 @@
 //     accumulator in tensor memory, committing the stage's "empty" barrier, and the
 //     "done" barrier after the last stage;
 //   all four warps (epilogue): thread r of lane quarter r / 32 reads token row r's 128
-//     logits from tensor memory, adds the bias and stores them.
+//     logits from tensor memory into shared memory; then each warp stores whole rows
+//     (lane l the experts l + 32 j) with the bias added.
 // Token rows past T, expert rows past E and values past H read as zeros (the TMA
 // out-of-bounds fill) and are not stored.  Every wait is bounded (MAPLE_ERR_TIMEOUT).
 #include <cuda.h>
@@ -42,6 +43,8 @@ constexpr int kRtStageA = kRtM * kRtK * 2;     // 16 KB
 constexpr int kRtStageB = kRtN * kRtK * 2;     // 16 KB
 constexpr int kRtSmem = kRtStages * (kRtStageA + kRtStageB);
 constexpr int kRtThreads = 128;
+constexpr int kRtPitch = kRtN + 1;             // floats per row of the staged logits block
+static_assert(kRtM * kRtPitch * 4 <= kRtSmem, "staged block fits the operand stages");
 // instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9 and
 // 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24
 constexpr uint32_t kRtIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kRtN >> 3) << 17) |
@@ -138,22 +141,41 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         __syncwarp();
     }
     pdl_launch_dependents();
-    // epilogue: token row t0 + r of the block, experts e0 .. e0 + 127
+    // epilogue: the block's logits go through shared memory (the operand stages are
+    // free once every MMA is done), so that each warp stores whole 512-byte runs of a
+    // token's row instead of one word of 32 different rows per store
     const bool got = mbar_wait_bounded(&bars.done, 0, status);
     tc_fence_after();
-    const int r = 32 * warp + lane, t = t0 + r;
-    const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // stages: TMA writes -> generic
+    float* blk = reinterpret_cast<float*>(smem);                    // [kRtM][kRtPitch]
+    {
+        const int r = 32 * warp + lane;
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll 1
-    for (int c0 = 0; c0 < kRtN; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(lane_addr + (uint32_t)c0, v);
-        tmem_wait_ld();
-        if (got && t < T) {
-            float* out = logits + (int64_t)t * E + e0 + c0;
+        for (int c0 = 0; c0 < kRtN; c0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(lane_addr + (uint32_t)c0, v);
+            tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int e = e0 + c0 + i;
-                if (e < E) out[i] = __uint_as_float(v[i]) + (bias != nullptr ? bias[e] : 0.f);
+            for (int i = 0; i < 16; ++i) blk[r * kRtPitch + c0 + i] = __uint_as_float(v[i]);
+        }
+    }
+    __syncthreads();
+    if (got) {
+        float b[kRtN / 32];
+#pragma unroll
+        for (int jj = 0; jj < kRtN / 32; ++jj) {
+            const int e = e0 + lane + 32 * jj;
+            b[jj] = (bias != nullptr && e < E) ? bias[e] : 0.f;
+        }
+        for (int row = warp; row < kRtM; row += kRtThreads / 32) {
+            const int t = t0 + row;
+            if (t >= T) break;
+            float* out = logits + (int64_t)t * E;
+#pragma unroll
+            for (int jj = 0; jj < kRtN / 32; ++jj) {
+                const int e = e0 + lane + 32 * jj;
+                if (e < E) out[e] = blk[row * kRtPitch + lane + 32 * jj] + b[jj];
             }
         }
     }
