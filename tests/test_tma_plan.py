@@ -395,13 +395,12 @@ def test_integer_pack_unit_matches_the_oracle_packing():
 
 
 TC_ROWS, TC_KTILE = 128, 160
-TC_A_STRIDE = 48
-TC_STATIC_SMEM = 1152  # largest static shared memory of the grouped kernels (ptxas -v)
-
-
-def tc_stage_b(nt):
-    """A B stage: 10 core-matrix columns of 16 e4m3 values for 2 NT rows (hi, lo)."""
-    return TC_KTILE // 16 * 2 * nt * 16
+TC_LUT = 256 * 16 * 8        # 256 entries x 16 copies x 8 bytes
+TC_STATIC_SMEM = 2048        # static shared memory of the streaming kernels, rounded up (ptxas -v)
+TC_SMEM_OPTIN = 232448       # 227 KB of dynamic shared memory per CTA
+PS_SUPER = 2                 # K tiles per ring stage
+PS_KS = PS_SUPER * TC_KTILE  # K values per stage: 64 packed bytes of a row
+PS_MAX_PACKED = 4
 
 
 def tc_shape_ok(H, I):
@@ -409,70 +408,70 @@ def tc_shape_ok(H, I):
             and H <= 2080 and I <= 2080)
 
 
-def tc_a_stages(nt):
-    return 3 if nt >= 128 else 4
+def ps_stage_b(nt):
+    """A B stage: PS_KS / 16 core-matrix columns of 16 e4m3 values for 2 NT rows (hi, lo)."""
+    return PS_KS // 16 * 2 * nt * 16
 
 
-def tc_b_stages(nt):
-    return tc_a_stages(nt)  # one ring: a K tile's A and B stages are freed together
+def ps_stages(nt):
+    return 3 if nt <= 16 else 2
 
 
-def tc_lut(nt):
-    """256 entries x 16 copies x 8 bytes."""
-    return 256 * 16 * 8
+def ps_accs(nt):
+    return min(256 // (2 * nt), 4)
 
 
-def tc_smem(row_bytes, nt):
-    stage_off = -(-(tc_lut(nt) + TC_ROWS * row_bytes) // 128) * 128
-    return stage_off, stage_off + tc_b_stages(nt) * tc_stage_b(nt)
+def ps_pk_stride(rb):
+    return -(-(TC_ROWS * rb) // 128) * 128
 
 
-def tc_tmem(nt):
-    a_base = max(2 * nt, 32)
-    used = a_base + tc_a_stages(nt) * TC_A_STRIDE
-    return a_base, used, 256 if used <= 256 else 512
+def ps_smem(rb, nt, npk):
+    return TC_LUT + npk * ps_pk_stride(rb) + ps_stages(nt) * ps_stage_b(nt)
 
 
-def test_tensor_path_plan_fits_and_is_aligned():
-    """The grouped tcgen05 kernels (csrc/ffn_tensor.cu), for both token-tile widths:
-    shared memory within the opt-in limit for every accepted shape (two CTAs per SM
-    for the 16-token tiles) and the epilogue buffers inside it, the packed-row bulk copies 16-byte aligned, every MMA read of a
-    B stage (5 MMAs of K = 32, 2NT/8 row groups at 128 B, 2 core-matrix columns at
-    2NT * 16 B) inside the stage, and the tensor-memory columns (accumulator of 2NT
-    columns, A stages of 40 columns at a 48-column stride, three or four stages) inside
-    the power-of-two allocation.  B stages (shared memory) follow the same ring: three
-    stages of 40 KB for 128-token tiles, four of 5 KB for 16-token tiles."""
+def ps_npk(rb, nt):
+    """Packed-row buffers the launcher picks: as many as fit, from 4 down to 2."""
+    n = PS_MAX_PACKED
+    while n > 2 and ps_smem(rb, nt, n) > 227 * 1024:
+        n -= 1
+    return n
+
+
+def test_streaming_tensor_plan_fits_and_is_aligned():
+    """The streaming tcgen05 kernels (csrc/ffn_tensor.cu), for both token-tile widths
+    (16 for decode batches, 64 for prefill) and every accepted shape: shared memory
+    (decode table, 2-4 packed-row buffers, the B ring) within the opt-in limit with at
+    least two packed buffers; the producers' word loads inside the allocation (five
+    aligned words from byte 16 part + 64 st of a row, reading up to 3 bytes past);
+    every MMA read of a B stage (2 core-matrix columns at 2NT * 16 B, 2NT / 8 row groups
+    at 128 B) inside the stage; the tensor-memory plan (A stages of 80 columns below
+    column 256, the accumulators of 2NT columns from 256 on, within 512); and each
+    item's packed-row bulk copies (64 gate rows and 64 up rows, or 128 down rows)
+    16-byte aligned and inside the expert's matrix."""
     shapes = [(H, I) for H in range(128, 2081, 128) for I in range(128, 2081, 64)]
-    for nt in (16, 128):
-        a_base, used, alloc = tc_tmem(nt)
-        assert 2 * nt <= a_base and a_base % 16 == 0
-        assert a_base + (tc_a_stages(nt) - 1) * TC_A_STRIDE + TC_KTILE // 4 <= used <= alloc
-        assert alloc in (256, 512) and (nt == 16) == (alloc == 256)
-        sb = tc_stage_b(nt)
+    for nt in (16, 64):
         n = 2 * nt
-        for q in range(TC_KTILE // 32):
+        sb = ps_stage_b(nt)
+        assert ps_stages(nt) * (PS_KS // 4) <= 256            # A stages below column 256
+        assert 256 + ps_accs(nt) * n <= 512 and ps_accs(nt) >= 2
+        for q in range(PS_KS // 32):
             assert q * 2 * n * 16 + n * 16 + (n // 8 - 1) * 128 + 127 < sb
         for H, I in shapes:
             assert tc_shape_ok(H, I)
-            for cols in (H, I):
-                assert cols % 16 == 0
-            for rb, rows_per_cta, mstep, mtot, epi in (
-                    (nbytes(H), TC_ROWS // 2, TC_ROWS // 2, I, nt * 64 * 4),
-                    (nbytes(I), TC_ROWS, TC_ROWS, H, 0)):
-                stage_off, total = tc_smem(rb, nt)
-                assert total + TC_STATIC_SMEM <= 232448, (H, I, nt, total)
-                if nt == 16:  # two CTAs per SM (228 KB, 1 KB reserved per CTA)
-                    assert 2 * (total + TC_STATIC_SMEM + 1024) <= 233472, (H, I, total)
-                # the producers' word loads: 5 aligned words from byte 127 rb + 32 kt + 16 h
-                K = H if rb == nbytes(H) else I
-                kt_last = -(-K // TC_KTILE) - 1
-                far = ((127 * rb + 32 * kt_last + 16) & ~3) + 20
-                assert tc_lut(nt) + far <= total, (H, I, nt)
-                assert tc_lut(nt) % 128 == 0 and tc_lut(nt) + epi <= total
-                size = rows_per_cta * rb
+            for rb, rows, mtot, K in ((nbytes(H), TC_ROWS // 2, I, H), (nbytes(I), TC_ROWS, H, I)):
+                npk = ps_npk(rb, nt)
+                total = ps_smem(rb, nt, npk)
+                assert npk >= 2 and total + TC_STATIC_SMEM <= TC_SMEM_OPTIN, (H, I, nt, total)
+                assert K % 32 == 0                             # MMAs cover whole K = 32 steps
+                ns = -(-K // PS_KS)
+                # farthest producer read: last row of the last buffer, last stage, last part
+                far = TC_LUT + (npk - 1) * ps_pk_stride(rb) + ((127 * rb + PS_KS // 5 * (ns - 1) + 48) & ~3) + 20
+                assert far <= total, (H, I, nt)
+                size = rows * rb
+                assert size % 16 == 0
                 for e in (0, 1, 7):
-                    for m0 in range(0, mtot, mstep):
-                        _check((e * mtot + m0) * rb, size, (e + 1) * mtot * rb, f"tc H={H} I={I}")
+                    for m0 in range(0, mtot, rows):
+                        _check((e * mtot + m0) * rb, size, (e + 1) * mtot * rb, f"stream H={H} I={I}")
     assert not tc_shape_ok(2080, 512) and not tc_shape_ok(2048, 520) and not tc_shape_ok(40, 24)
     assert not tc_shape_ok(128, 64)
 
@@ -480,21 +479,21 @@ def test_tensor_path_plan_fits_and_is_aligned():
 def test_tensor_path_operand_blocks_are_aligned_and_in_bounds():
     """The B operand of a tile lives in global memory as [K / 16][2NT][16] e4m3 bytes
     (the split kernels write x and h that way: hi rows 0..NT-1, lo rows NT..2NT-1); each
-    K tile's stage is one bulk copy of up to 10 chunks, fewer at the K tail.  Every copy
-    starts on a 16-byte boundary, has a multiple of 16 bytes and stays inside its tile's
-    block, and the split kernels' 8-byte stores stay inside the block too."""
-    for nt in (16, 128):
+    ring stage is one bulk copy of up to PS_KS / 16 chunks, fewer at the K tail.  Every
+    copy starts on a 16-byte boundary, has a multiple of 16 bytes and stays inside its
+    tile's block, and the split kernels' 8-byte stores stay inside the block too."""
+    for nt in (16, 64):
         for K in (128, 192, 384, 512, 2048):
             block = K * 2 * nt
-            KT = -(-K // TC_KTILE)
+            ns = -(-K // PS_KS)
             covered = 0
-            for j in range(KT):
-                left = K // 16 - j * (TC_KTILE // 16)
-                nb = min(left, TC_KTILE // 16) * 2 * nt * 16
-                off = j * tc_stage_b(nt)
+            for st in range(ns):
+                left = K // 16 - st * (PS_KS // 16)
+                nb = min(left, PS_KS // 16) * 2 * nt * 16
+                off = st * ps_stage_b(nt)
                 for tile in (0, 1, 5):
-                    _check(tile * block + off, nb, (tile + 1) * block, f"B nt={nt} K={K} j={j}")
-                assert nb <= tc_stage_b(nt)
+                    _check(tile * block + off, nb, (tile + 1) * block, f"B nt={nt} K={K} st={st}")
+                assert nb <= ps_stage_b(nt)
                 covered += nb
             assert covered == block
             for c in range(K // 8):
@@ -597,32 +596,6 @@ def test_grouped_decode_81_entry_table_matches_the_oracle_unpack():
             continue
         trits = oracle.unpack(np.array([[c]], np.uint8), 5)[0]
         assert vals == [e4m3_of[int(t)] for t in trits], (c, vals, trits)
-
-
-def test_multi_block_down_plan_fits_and_is_aligned():
-    """The down kernel for 16-token tiles whose whole h operand fits the B stages (K tiles
-    of 160 values <= 4, i.e. I <= 640) walks 4 consecutive 128-row blocks: the decode
-    table, two packed-row buffers (rounded to 128 B) and four 5 KB B stages must fit two
-    CTAs per SM, and every block's packed-row copy (128 rows of ceil(I/5) bytes) must be
-    16-byte aligned and inside the expert's down matrix."""
-    nt, blocks = 16, 4
-    for H in range(128, 2081, 128):
-        for I in range(128, 641, 64):
-            if not tc_shape_ok(H, I):
-                continue
-            rb = nbytes(I)
-            assert -(-I // TC_KTILE) <= tc_a_stages(nt)
-            pk = -(-(TC_ROWS * rb) // 128) * 128
-            total = tc_lut(nt) + 2 * pk + tc_a_stages(nt) * tc_stage_b(nt)
-            assert 2 * (total + TC_STATIC_SMEM + 1024) <= 233472, (H, I, total)
-            nblk_all = H // TC_ROWS
-            for e in (0, 3):
-                for bx in range(-(-nblk_all // blocks)):
-                    blk0 = bx * blocks
-                    for b in range(min(blocks, nblk_all - blk0)):
-                        off = (e * H + (blk0 + b) * TC_ROWS) * rb
-                        _check(off, TC_ROWS * rb, (e + 1) * H * rb, f"multi down H={H} I={I}")
-
 
 
 def test_packed_magnitude_fold_has_no_cross_half_borrow():
