@@ -651,12 +651,15 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
                 tmem_ld_sum<NT, 16>(base, 16 * b, v);
                 if (kDown) {
                     float* yr = a.ys + m + r;
+                    // every shared-memory read before the first store: the stores go
+                    // through a generic pointer, which the compiler cannot tell apart
+                    // from shared memory, so interleaving them would serialise the loop
+                    float2 tv[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int t = 16 * b + i;
-                        const float2 tv = s_tok[acc][t];
-                        if (t < nv) yr[(int64_t)__float_as_int(tv.x) * H] = tv.y * (row_scale * v[i]);
-                    }
+                    for (int i = 0; i < 16; ++i) tv[i] = s_tok[acc][16 * b + i];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (16 * b + i < nv) yr[(int64_t)__float_as_int(tv[i].x) * H] = tv[i].y * (row_scale * v[i]);
                 } else {
                     // gate lane keeps tokens 16b..16b+7, the up lane 16b+8..16b+15; each
                     // hands the other half to its partner lane (r ^ 1)
