@@ -611,35 +611,66 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
         const int q = warp & 3, r = 32 * q + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
         const bool up_side = !kDown && (r & 1);
-        for (int it = 0; (int)blockIdx.x + it * stride < n_items; ++it) {
-            const int item = (int)blockIdx.x + it * stride;
-            const int tile = item / nblk, blk = item % nblk, acc = it % NACC;
-            const int4 info = __ldcg(a.tile_info + tile);
-            const int e = info.x, nv = info.z, pos0 = info.w;
-            // per-token values of the item, loaded by the first epilogue warp while the
-            // accumulator fills and published in shared memory (the named barrier below
-            // orders them): the x split scale (gate/up), or the slot and the routing
-            // weight times the h split scale (down)
-            if (warp == kPsEpiWarp0) {
+        // An item's per-item values are loaded one item ahead, so that their dependent
+        // global loads overlap the previous item's work: each thread's row scale, and
+        // the per-token values, which the first epilogue warp loads into registers and
+        // publishes in shared memory once the previous item is stored (the named
+        // barrier of the item orders them): the x split scale (gate/up), or the slot and
+        // the routing weight times the h split scale (down).
+        constexpr int TPL = (NT + 31) / 32;  // per-token values a lane of that warp loads
+        auto valid = [&](int it) { return (int)blockIdx.x + it * stride < n_items; };
+        auto record = [&](int it) {
+            return valid(it) ? __ldcg(a.tile_info + ((int)blockIdx.x + it * stride) / nblk) : make_int4(0, 0, 0, 0);
+        };
+        auto load_tokens = [&](int it, int4 info, float2* tv) {
+            const int tile = ((int)blockIdx.x + it * stride) / nblk, nv = valid(it) ? info.z : 0, pos0 = info.w;
 #pragma unroll
-                for (int t = lane; t < NT; t += 32) {
-                    float2 tv = make_float2(0.f, 0.f);
-                    if (t < nv) {
-                        if (kDown) {
-                            const int slot = __ldcg(a.perm + pos0 + t);
-                            tv = make_float2(__int_as_float(slot),
-                                             __ldcg(a.w + slot) * a.hscale[(size_t)tile * NT + t]);
-                        } else {
-                            tv.x = a.xscale[(size_t)tile * NT + t];
-                        }
+            for (int u = 0; u < TPL; ++u) {
+                const int t = lane + 32 * u;
+                tv[u] = make_float2(0.f, 0.f);
+                if (t < NT && t < nv) {
+                    if (kDown) {
+                        const int slot = __ldcg(a.perm + pos0 + t);
+                        tv[u] = make_float2(__int_as_float(slot), __ldcg(a.w + slot) * a.hscale[(size_t)tile * NT + t]);
+                    } else {
+                        tv[u].x = a.xscale[(size_t)tile * NT + t];
                     }
-                    s_tok[acc][t] = tv;
                 }
             }
+        };
+        auto publish = [&](int it, const float2* tv) {
+#pragma unroll
+            for (int u = 0; u < TPL; ++u)
+                if (lane + 32 * u < NT) s_tok[it % NACC][lane + 32 * u] = tv[u];
+        };
+        auto load_row_scale = [&](int it, int4 info) {
+            if (!valid(it)) return 0.f;
+            const int blk = ((int)blockIdx.x + it * stride) % nblk, e = info.x;
+            return kDown ? a.s_down[(int64_t)e * H + blk * kRows + r]
+                         : (up_side ? a.s_up[(int64_t)e * I + blk * (kRows / 2) + (r >> 1)]
+                                    : a.s_gate[(int64_t)e * I + blk * (kRows / 2) + (r >> 1)]);
+        };
+        int4 info_cur = record(0), info_nxt = record(1);
+        float row_scale_cur = load_row_scale(0, info_cur);
+        {
+            float2 tv0[TPL];
+            if (warp == kPsEpiWarp0) {
+                load_tokens(0, info_cur, tv0);
+                publish(0, tv0);
+            }
+        }
+        for (int it = 0; valid(it); ++it) {
+            const int item = (int)blockIdx.x + it * stride;
+            const int blk = item % nblk, acc = it % NACC;
+            const int nv = info_cur.z, pos0 = info_cur.w;
+            const float row_scale = row_scale_cur;
             const int m = kDown ? blk * kRows : blk * (kRows / 2);
             const int j = kDown ? r : (r >> 1);  // down row, or gate/up row pair
-            const float row_scale = kDown ? a.s_down[(int64_t)e * H + m + r]
-                                          : (up_side ? a.s_up[(int64_t)e * I + m + j] : a.s_gate[(int64_t)e * I + m + j]);
+            // the next item's values, in flight while this one is finished
+            const int4 info_after = record(it + 2);
+            const float row_scale_nxt = load_row_scale(it + 1, info_nxt);
+            float2 tv_nxt[TPL];
+            if (warp == kPsEpiWarp0) load_tokens(it + 1, info_nxt, tv_nxt);
             // one decision for all 128 epilogue threads (they meet at a named barrier)
             const bool got = ps_wait(&bars.acc_full[acc], (uint32_t)((it / NACC) & 1), a.status, abort);
             if (bar_any_128(!got)) break;
@@ -683,6 +714,10 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
             }
             tc_fence_before();
             mbar_arrive(&bars.acc_empty[acc]);  // drained
+            if (warp == kPsEpiWarp0 && valid(it + 1)) publish(it + 1, tv_nxt);
+            info_cur = info_nxt;
+            info_nxt = info_after;
+            row_scale_cur = row_scale_nxt;
         }
     }
     tc_fence_before();
