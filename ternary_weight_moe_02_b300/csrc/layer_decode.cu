@@ -192,7 +192,6 @@ __global__ void __launch_bounds__(kLcThreads, 1) moe_layer_b1_kernel(LcArgs a) {
     __shared__ __align__(16) uint64_t s_key[kLcMaxE];       // selection keys of the logits
     __shared__ __align__(16) uint64_t s_cand[kLcMaxE / 32 * kLcMaxK];
     __shared__ uint64_t s_sel[kLcMaxK];
-    __shared__ int s_idx[kLcMaxK];
     __shared__ float s_w[kLcMaxK];
     __shared__ int s_fail, s_last;
 
@@ -321,14 +320,17 @@ __global__ void __launch_bounds__(kLcThreads, 1) moe_layer_b1_kernel(LcArgs a) {
             if (cand < ncand && sub == 0 && rank < k) s_sel[rank] = K;
         }
         __syncthreads();
-        if (warp == 0) {  // softmax over the k selected: exp(l_i - l_0) / sum_j exp(l_j - l_0)
+        // the copies need only the selected ids (from the keys); the softmax weights are
+        // first read after the h exchange, so the last warp forms them off the critical
+        // path while the copies are issued
+        auto sel_id = [&](int i) { return (int)(0xffffffffu - (uint32_t)s_sel[i]); };
+        if (warp == kLcWarps - 1) {  // softmax over the k selected: exp(l_i - l_0) / sum_j exp(l_j - l_0)
             const int my_idx = lane < k ? (int)(0xffffffffu - (uint32_t)s_sel[lane]) : 0;
             const float my_val = lane < k ? lg[my_idx] : -INFINITY;
             const float top = lg[(int)(0xffffffffu - (uint32_t)s_sel[0])];
             const float ex = lane < k ? expf(my_val - top) : 0.f;
             const float denom = warp_sum(ex);
             if (lane < k) {
-                s_idx[lane] = my_idx;
                 s_w[lane] = ex / denom;
                 if (blockIdx.x == 0) {
                     a.idx[lane] = my_idx;
@@ -336,12 +338,12 @@ __global__ void __launch_bounds__(kLcThreads, 1) moe_layer_b1_kernel(LcArgs a) {
                 }
             }
         }
-        __syncthreads();  // also: every warp is done reading the router rows
-        // bulk copies, one issuing thread per group of barriers (lane 0 of warps 0..2+2S)
+        // bulk copies, one issuing thread per group of barriers (lane 0 of warps 0..2+2S;
+        // every warp finished reading the router rows before the cluster barrier)
         if (lane == 0 && warp < 3 + 2 * nsplit) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // router rows -> copies
             if (warp < 2) {  // whole slot: gate/up chunks 2w, 2w + 1
-                const int e = s_idx[c], cr = L.chunk_rows;
+                const int e = sel_id(c), cr = L.chunk_rows;
                 const uint32_t rows = (uint32_t)(cr * Bh);
                 for (int q = 2 * warp; q < 2 * warp + 2; ++q) {
                     unsigned char* ch = un + q * L.chunk_bytes;
@@ -354,12 +356,12 @@ __global__ void __launch_bounds__(kLcThreads, 1) moe_layer_b1_kernel(LcArgs a) {
                     bulk_copy_g2s(ch + 2 * rows + 4 * cr, a.s_up + r0, 4u * cr, &bar_gu[q]);
                 }
             } else if (warp == 2) {  // whole slot: down rows + scales
-                const int64_t d0 = (int64_t)s_idx[c] * H + r * rd;
+                const int64_t d0 = (int64_t)sel_id(c) * H + r * rd;
                 mbar_arrive_expect_tx(&bar_dn, (uint32_t)L.dn_bytes);
                 bulk_copy_g2s(un + L.dn, a.down + d0 * Bi, (uint32_t)(rd * Bi), &bar_dn);
                 bulk_copy_g2s(un + L.dn + rd * Bi, a.s_down + d0, 4u * rd, &bar_dn);
             } else {
-                const int s = (warp - 3) >> 1, e = s_idx[C + s];
+                const int s = (warp - 3) >> 1, e = sel_id(C + s);
                 unsigned char* sp = un + L.sp + s * L.sp_bytes;
                 if (((warp - 3) & 1) == 0) {  // split slot s: the 8-row groups holding this CTA's pairs
                     const int64_t r0 = (int64_t)e * I + col0 + sg0;
