@@ -994,15 +994,20 @@ cudaError_t launch_tc_ffn_stream(const TcArgs& a, int S, cudaStream_t stream, in
 cudaError_t launch_moe_ffn_tensor(const FfnArgs& f, cudaStream_t stream, const DeviceInfo& dev) {
     const int S = f.T * f.k;
     const int nt = ffn_tensor_tile_tokens(S, f.E);
-    // one CTA groups a few thousand slots fastest; beyond that, chunks in parallel
-    cudaError_t err = S > 4096 ? launch_group_tokens_chunked(f.idx, S, f.E, f.counts, f.offsets, f.perm, f.active,
-                                                             f.n_active, f.chunks, stream)
-                               : launch_group_tokens(f.idx, S, f.k, f.E, f.counts, f.offsets, f.perm, f.active,
-                                                     f.n_active, stream, dev);
-    if (err != cudaSuccess) return err;
-    err = launch_pdl(tc_tile_prefix_kernel, dim3(1), dim3(1024), 0, stream, (const int32_t*)f.counts,
-                     (const int32_t*)f.offsets, f.E, nt, f.tile_off,
-                     reinterpret_cast<int4*>(f.tile_off + ((f.E + 1 + 3) & ~3)));
+    int4* tile_info = reinterpret_cast<int4*>(f.tile_off + ((f.E + 1 + 3) & ~3));
+    // one CTA groups a few thousand slots fastest, writing the tile table as it goes;
+    // beyond that, chunks in parallel, then the tile table
+    cudaError_t err;
+    if (S > 4096) {
+        err = launch_group_tokens_chunked(f.idx, S, f.E, f.counts, f.offsets, f.perm, f.active, f.n_active, f.chunks,
+                                          stream);
+        if (err != cudaSuccess) return err;
+        err = launch_pdl(tc_tile_prefix_kernel, dim3(1), dim3(1024), 0, stream, (const int32_t*)f.counts,
+                         (const int32_t*)f.offsets, f.E, nt, f.tile_off, tile_info);
+    } else {
+        err = launch_group_tokens(f.idx, S, f.k, f.E, f.counts, f.offsets, f.perm, f.active, f.n_active, stream,
+                                  dev, nt, f.tile_off, tile_info);
+    }
     if (err != cudaSuccess) return err;
     TcArgs a;
     a.gate = f.gate;

@@ -23,7 +23,8 @@ __global__ void __launch_bounds__(kGroupThreads)
     group_tokens_kernel(const int32_t* __restrict__ idx, int S, int E,
                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                         int32_t* __restrict__ perm, int32_t* __restrict__ active,
-                        int32_t* __restrict__ n_active) {
+                        int32_t* __restrict__ n_active, int nt, int32_t* __restrict__ tile_off,
+                        int4* __restrict__ tile_info) {
     extern __shared__ int32_t smem[];
     int32_t* hist = smem;                 // [E]
     int32_t* cursor = hist + E;           // [E]
@@ -92,6 +93,38 @@ __global__ void __launch_bounds__(kGroupThreads)
         if (tid == E - 1) {
             offsets[E] = excl_c + c;
             if (n_active != nullptr) *n_active = excl_f + f;
+        }
+        // the grouped tensor-core path's tile table (nt > 0): tile_off[e] = sum over
+        // e' < e of ceil(counts[e'] / nt), and per tile (expert, first token, tokens,
+        // grouped position of its first token)
+        if (nt > 0) {
+            const int v = (c + nt - 1) / nt;
+            int vi = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int vn = __shfl_up_sync(kFullMask, vi, o);
+                if (lane >= o) vi += vn;
+            }
+            __syncthreads();  // every thread has read the counts scan's partials
+            if (lane == 31) scan_part[warp] = vi;
+            __syncthreads();
+            if (warp == 0) {
+                int p = scan_part[lane];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int pn = __shfl_up_sync(kFullMask, p, o);
+                    if (lane >= o) p += pn;
+                }
+                scan_part[lane] = p;
+            }
+            __syncthreads();
+            const int excl_v = (warp > 0 ? scan_part[warp - 1] : 0) + vi - v;
+            if (tid < E) tile_off[tid] = excl_v;
+            if (tid == E - 1) tile_off[E] = excl_v + v;
+            for (int t = 0; t < v; ++t) {
+                const int n0 = t * nt, left = c - n0;
+                tile_info[excl_v + t] = make_int4(tid, n0, left < nt ? left : nt, excl_c + n0);
+            }
         }
     }
     __syncthreads();
@@ -260,7 +293,8 @@ size_t group_tokens_smem_bytes(int E) { return sizeof(int32_t) * (size_t)E * (2 
 
 cudaError_t launch_group_tokens(const int32_t* idx, int S, int k, int E, int32_t* counts,
                                 int32_t* offsets, int32_t* perm, int32_t* active,
-                                int32_t* n_active, cudaStream_t stream, const DeviceInfo& dev) {
+                                int32_t* n_active, cudaStream_t stream, const DeviceInfo& dev, int nt,
+                                int32_t* tile_off, int4* tile_info) {
     (void)k;
     const size_t smem = group_tokens_smem_bytes(E);
     if (smem > 48 * 1024) {
@@ -270,7 +304,7 @@ cudaError_t launch_group_tokens(const int32_t* idx, int S, int k, int E, int32_t
     }
     (void)dev;
     return launch_pdl(group_tokens_kernel, dim3(1), dim3(kGroupThreads), smem, stream, idx, S, E,
-                      counts, offsets, perm, active, n_active);
+                      counts, offsets, perm, active, n_active, nt, tile_off, tile_info);
 }
 
 }  // namespace maple

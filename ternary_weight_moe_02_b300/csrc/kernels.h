@@ -47,9 +47,12 @@ cudaError_t launch_route_topk(const uint16_t* x, const uint16_t* Wr, const float
 
 // Grouping with optional outputs used by the FFN: `active` lists the experts with a
 // non-zero count in increasing id order and `n_active` receives their number.
+// With nt > 0 it also writes the grouped tensor-core path's tile table (tile_off[E + 1],
+// tile_info: one record per tile of nt tokens), as tc_tile_prefix_kernel does.
 cudaError_t launch_group_tokens(const int32_t* idx, int S, int k, int E, int32_t* counts,
                                 int32_t* offsets, int32_t* perm, int32_t* active,
-                                int32_t* n_active, cudaStream_t stream, const DeviceInfo& dev);
+                                int32_t* n_active, cudaStream_t stream, const DeviceInfo& dev, int nt = 0,
+                                int32_t* tile_off = nullptr, int4* tile_info = nullptr);
 size_t group_tokens_smem_bytes(int E);
 // The same grouping spread over chunks of 1024 slots (for many slots); chunk_scratch
 // holds group_chunked_bytes(S, E) bytes.
