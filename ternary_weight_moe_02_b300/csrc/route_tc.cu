@@ -11,10 +11,10 @@
 // the fp32 summation bound of a K-deep sum).
 //
 // A CTA computes a block of 128 tokens x 128 experts over all of H:
-//   warp 0, lane 0 (loads): per K stage of 64 values, eight TMA box loads of x (8
-//     values x 128 token rows each) and eight of Wr (8 values x 128 expert rows), which
-//     land in the K-major core-matrix layout the MMA descriptors name (the 8 values of
-//     row r of chunk c at c * 2048 + 16 r), on the stage's "full" barrier;
+//   warp 0, lane 0 (loads): per K stage of 64 values, one TMA box load of x (64 values
+//     x 128 token rows, whole 128-byte lines) and one of Wr (64 values x 128 expert
+//     rows), in the 128-byte swizzled K-major layout the MMA descriptors name, on the
+//     stage's "full" barrier;
 //   warp 1, lane 0 (MMA): four MMAs (K = 16) per stage into one 128-column fp32
 //     accumulator in tensor memory, committing the stage's "empty" barrier, and the
 //     "done" barrier after the last stage;
@@ -38,10 +38,11 @@ constexpr int kRtM = 128;                      // tokens per CTA (MMA M)
 constexpr int kRtN = 128;                      // experts per CTA (MMA N)
 constexpr int kRtK = 64;                       // K values per stage
 constexpr int kRtStages = 4;
-constexpr int kRtChunk = 8;                    // bf16 values of a 16-byte core-matrix row
+constexpr int kRtSwizzleBytes = 128;           // 128-byte swizzle: one 64-value row of a stage
 constexpr int kRtStageA = kRtM * kRtK * 2;     // 16 KB
 constexpr int kRtStageB = kRtN * kRtK * 2;     // 16 KB
-constexpr int kRtSmem = kRtStages * (kRtStageA + kRtStageB);
+constexpr int kRtSmem = kRtStages * (kRtStageA + kRtStageB) + 1024;  // + alignment of the stages
+static_assert(kRtK * 2 == kRtSwizzleBytes, "a stage row is one swizzle row");
 constexpr int kRtThreads = 128;
 constexpr int kRtPitch = kRtN + 1;             // floats per row of the staged logits block
 static_assert(kRtM * kRtPitch * 4 <= kRtSmem, "staged block fits the operand stages");
@@ -60,6 +61,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
             "r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
         : "memory");
+}
+
+// Shared-memory descriptor of a K-major operand in the 128-byte swizzled layout that TMA
+// writes with CU_TENSOR_MAP_SWIZZLE_128B: rows of 128 bytes (64 bf16), the 16-byte
+// pieces of row r XOR-permuted by r % 8, 8-row groups 1024 bytes apart (SBO); the
+// leading offset is unused for this layout (1).  Start address >> 4 in bits 0-13,
+// version 1 at bit 46, layout type 2 (128-byte swizzle) in bits 61-63.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           (1ull << 46) | (2ull << 61);
 }
 
 // D[tmem] (+)= A[smem descriptor] . B[smem descriptor]^T, bf16 x bf16 -> fp32
@@ -81,8 +92,9 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = blockIdx.x * kRtM, e0 = blockIdx.y * kRtN;
     const int KS = (H + kRtK - 1) / kRtK;
-    unsigned char* sa = smem;
-    unsigned char* sb = smem + kRtStages * kRtStageA;
+    // the stages on a 1024-byte boundary (the 128-byte swizzle repeats every 8 rows)
+    unsigned char* sa = smem + ((1024u - (smem_addr(smem) & 1023u)) & 1023u);
+    unsigned char* sb = sa + kRtStages * kRtStageA;
     if (tid == 0) {
         for (int s = 0; s < kRtStages; ++s) {
             mbar_init_nofence(&bars.full[s], 1);
@@ -108,11 +120,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(&bars.full[s], (uint32_t)(kRtStageA + kRtStageB));
-                for (int c = 0; c < kRtK / kRtChunk; ++c) {
-                    const int k = ks * kRtK + c * kRtChunk;
-                    tma_load_2d(sa + s * kRtStageA + c * (kRtM * 16), &map_x, k, t0, &bars.full[s]);
-                    tma_load_2d(sb + s * kRtStageB + c * (kRtN * 16), &map_w, k, e0, &bars.full[s]);
-                }
+                tma_load_2d(sa + s * kRtStageA, &map_x, ks * kRtK, t0, &bars.full[s]);
+                tma_load_2d(sb + s * kRtStageB, &map_w, ks * kRtK, e0, &bars.full[s]);
                 issued = ks + 1;
             }
             // the last loads into each stage land before the CTA leaves
@@ -129,9 +138,9 @@ __global__ void __launch_bounds__(kRtThreads, 1)
                 const uint32_t a0 = smem_addr(sa + s * kRtStageA), b0 = smem_addr(sb + s * kRtStageB);
 #pragma unroll
                 for (int kk = 0; kk < kRtK / 16; ++kk) {
-                    // K = 16 values = two 16-byte chunks
-                    const uint64_t ad = smem_desc(a0 + kk * 2 * (kRtM * 16), kRtM * 16, 128);
-                    const uint64_t bd = smem_desc(b0 + kk * 2 * (kRtN * 16), kRtN * 16, 128);
+                    // K = 16 values = 32 bytes along the swizzled 128-byte rows
+                    const uint64_t ad = smem_desc_sw128(a0 + kk * 32);
+                    const uint64_t bd = smem_desc_sw128(b0 + kk * 32);
                     mma_bf16_ss(tmem, ad, bd, (ks | kk) != 0 ? 1u : 0u);
                 }
                 mma_commit(&bars.empty[s]);
@@ -197,16 +206,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// A [rows][H] bf16 row-major matrix as a TMA map with boxes of 8 values x box_rows rows.
+// A [rows][H] bf16 row-major matrix as a TMA map with boxes of 64 values x box_rows rows,
+// written to shared memory in the 128-byte swizzled layout.
 bool encode_rows(CUtensorMap* map, const uint16_t* base, int rows, int H, int box_rows) {
     const auto enc = tensor_map_encoder();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kRtChunk, (cuuint32_t)box_rows};
+    const cuuint32_t box[2] = {(cuuint32_t)kRtK, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
