@@ -44,11 +44,16 @@ def _random_routing(T, E, k, seed):
 
 
 @pytest.mark.parametrize("E,H,I,T,k", [(8, 256, 128, 40, 4), (4, 384, 192, 33, 3),
-                                       (6, 128, 128, 17, 6), (16, 2048, 512, 24, 8)])
+                                       (6, 128, 128, 17, 6), (16, 2048, 512, 24, 8),
+                                       (4, 384, 192, 200, 2), (2, 256, 2048, 150, 2),
+                                       (2, 2048, 2048, 40, 1)])
 def test_tensor_path_shapes(E, H, I, T, k):
-    """Ragged token tiles (n_e not a multiple of 16), K tails (H = 384: 77 packed bytes
-    per row, the fifth K tile half padding; I = 192: 39 bytes), the smallest shape the
-    path takes (H = I = 128) and the Maple expert shape."""
+    """Ragged token tiles (n_e not a multiple of the tile width), K tails (H = 384: 77
+    packed bytes per row, the last 320-value stage 64 values long; I = 192: 39 bytes),
+    the smallest shape the path takes (H = I = 128), the Maple expert shape, the same
+    K tails on 64-token tiles (400 slots over 4 experts), a wide intermediate dimension
+    (I = 2048: down rows of 410 packed bytes, two packed-row buffers) on 64-token tiles,
+    and H = I = 2048 on 16-token tiles."""
     packed, ex = _layer(E, H, I, seed=E + H + T)
     x = synth.tokens(T, H, seed=T)
     idx, w32 = _random_routing(T, E, k, seed=T)
