@@ -417,11 +417,19 @@ int maple_moe_layer_host(const uint16_t* x_host, uint16_t* x_dev, const uint16_t
     if (!x_host || !y_host) return fail(MAPLE_ERR_INVALID_ARG, "moe_layer_host: null host buffer");
     const size_t x_bytes = (size_t)T * (size_t)ex->H * 2, y_bytes = (size_t)T * (size_t)ex->H * 4;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t err = cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, s);
+    // pinned host buffers the device can address: copy kernels chained with the layer
+    // by programmatic dependent launch; other host memory: plain async copies
+    maple::DeviceInfo dev;
+    if (int st = get_device(&dev, "moe_layer_host")) return st;
+    void* xm = maple::mapped_host_pointer(x_host);
+    void* ym = maple::mapped_host_pointer(y_host);
+    cudaError_t err = xm && ym ? maple::launch_io_copy(xm, x_dev, x_bytes, s, dev)
+                   : cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, s);
     if (err != cudaSuccess) return cuda_fail(err, "moe_layer_host: copy x in");
     const int st = maple_moe_layer(x_dev, Wr, bias, ex, T, k, logits, idx, w, y, ws, ws_bytes, stream);
     if (st != MAPLE_OK) return st;
-    err = cudaMemcpyAsync(y_host, y, y_bytes, cudaMemcpyDeviceToHost, s);
+    err = xm && ym ? maple::launch_io_copy(y, ym, y_bytes, s, dev)
+                   : cudaMemcpyAsync(y_host, y, y_bytes, cudaMemcpyDeviceToHost, s);
     if (err != cudaSuccess) return cuda_fail(err, "moe_layer_host: copy y out");
     return ok();
 }

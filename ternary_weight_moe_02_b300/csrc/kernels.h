@@ -47,6 +47,11 @@ cudaError_t launch_route_topk(const uint16_t* x, const uint16_t* Wr, const float
 
 // Grouping with optional outputs used by the FFN: `active` lists the experts with a
 // non-zero count in increasing id order and `n_active` receives their number.
+// Host I/O (host_io.cu): the device address of mapped pinned host memory (nullptr for
+// other memory), and a copy kernel chained by programmatic dependent launch.
+void* mapped_host_pointer(const void* host);
+cudaError_t launch_io_copy(const void* src, void* dst, size_t bytes, cudaStream_t stream, const DeviceInfo& dev);
+
 // With nt > 0 it also writes the grouped tensor-core path's tile table (tile_off[E + 1],
 // tile_info: one record per tile of nt tokens), as tc_tile_prefix_kernel does.
 cudaError_t launch_group_tokens(const int32_t* idx, int S, int k, int E, int32_t* counts,

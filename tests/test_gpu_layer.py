@@ -157,7 +157,8 @@ def test_layer_small_shapes_single_token():
 
 def test_layer_host_buffers_match_the_device_call(layer256):
     """maple_moe_layer_host (token copied in from pinned host memory, y copied out)
-    gives the device call's results bit for bit, twice in a row; the bound form too."""
+    gives the device call's results bit for bit, twice in a row; the bound form too, and
+    pageable host buffers."""
     from ternary_weight_moe_02_b300 import maple
     packed, ex, router = layer256
     ws = torch.zeros(maple.maple_moe_layer_workspace_size(1, 8, ex), dtype=torch.uint8, device="cuda")
@@ -177,3 +178,27 @@ def test_layer_host_buffers_match_the_device_call(layer256):
         maple.bind_moe_layer_host(x_host, x_dev, router, None, ex, 8, l2, i2, w2, y2, y_host, ws)()
         torch.cuda.synchronize()
         assert torch.equal(y.cpu(), y_host)
+        # pageable host buffers take asynchronous copies instead of the copy kernels
+        x_page, y_page = x.cpu(), torch.full((1, 2048), float("nan"))
+        maple.maple_moe_layer_host(x_page, x_dev, router, None, ex, 8, l2, i2, w2, y2, y_page, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(y.cpu(), y_page)
+
+
+def test_layer_host_buffers_several_tokens(layer256):
+    """Three tokens through maple_moe_layer_host (the route + FFN calls, copy kernels on
+    pinned buffers) against the device call, bit for bit."""
+    from ternary_weight_moe_02_b300 import maple
+    packed, ex, router = layer256
+    T = 3
+    ws = torch.zeros(maple.maple_moe_layer_workspace_size(T, 8, ex), dtype=torch.uint8, device="cuda")
+    x = synth.tokens(T, 2048, seed=31, device="cuda")
+    logits, idx, w, y, _ = _layer_call(ex, x, router, None, 8, ws)
+    x_host = x.cpu().pin_memory()
+    y_host = torch.full((T, 2048), float("nan")).pin_memory()
+    x_dev = torch.empty_like(x)
+    l2, i2, w2, y2 = (torch.empty_like(logits), torch.empty_like(idx), torch.empty_like(w), torch.empty_like(y))
+    maple.maple_moe_layer_host(x_host, x_dev, router, None, ex, 8, l2, i2, w2, y2, y_host, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(logits, l2) and torch.equal(idx, i2) and torch.equal(w, w2)
+    assert torch.equal(y.cpu(), y_host)
