@@ -570,10 +570,12 @@ def test_grouped_decode_table_matches_the_oracle_unpack():
 
 
 def test_grouped_decode_81_entry_table_matches_the_oracle_unpack():
-    """The 128-token tiles decode a byte c as c = low + 81 q4 with q4 = (c * 203) >> 14:
-    the first four trits from entry `low` of an 82-entry table (entry 81 all zero, taken
-    for the invalid codes 243..255), the fifth from q4 (byte q4 of 0x003800B8 as e4m3:
-    -1, 0, +1, and 0 for q4 = 3).  Every byte value against oracle.unpack."""
+    """The alternative decode that was measured (slower, not used by the kernels): a byte
+    c = low + 81 q4 with q4 = (c * 203) >> 14, the first four trits from entry `low` of
+    an 82-entry table (entry 81 all zero, taken for the invalid codes 243..255), the
+    fifth from q4 (byte q4 of 0x003800B8 as e4m3: -1, 0, +1, and 0 for q4 = 3).  Every
+    byte value against oracle.unpack, so the comparison of the two decodes compared
+    correct ones."""
     import oracle
 
     e4m3_of = {-1: 0xB8, 0: 0x00, 1: 0x38}
