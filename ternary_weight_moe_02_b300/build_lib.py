@@ -52,10 +52,20 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             os.replace(obj + ".tmp", obj)
             changed = True
         objs.append(obj)
-    if changed or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
+    # the objects a library was linked from: a source switched back to an earlier
+    # version finds its (older) object cached, which a time comparison would miss
+    manifest = LIB + ".objs"
+    linked = ""
+    if os.path.exists(manifest) and os.path.exists(LIB):
+        with open(manifest) as fh:
+            linked = fh.read()
+    names = "\n".join(os.path.basename(o) for o in objs)
+    if changed or linked != names:
         tmp = LIB + f".tmp{os.getpid()}"
         subprocess.check_call([NVCC] + LDFLAGS + objs + ["-o", tmp])
         os.replace(tmp, LIB)
+        with open(manifest, "w") as fh:
+            fh.write(names)
     return LIB
 
 

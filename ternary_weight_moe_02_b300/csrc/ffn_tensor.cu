@@ -289,8 +289,9 @@ __device__ __forceinline__ void tmem_ld_sum(uint32_t lane_addr, int c0, float* v
 //   17    lane 0 copies the items' packed rows into npk buffers, as far ahead as the
 //         producers free them (weights: issued before the PDL wait);
 //   18    lane 0 copies the tiles' B operands (split x or h) into the ring;
-//   19-22 epilogue: drain the item's accumulator (TMEM lane quarter warp % 4) 16 tokens
-//         at a time, free it, and finish the item as the per-item kernels do.
+//   19-   epilogue (4 warps, or 8 on 64-token tiles): drain the item's accumulator (TMEM
+//         lane quarter warp % 4) 16 tokens at a time, free it, and finish the item as
+//         the per-item kernels do.
 // Gate/up items interleave their rows in tensor memory: lane 2j holds gate row j and
 // lane 2j + 1 the same up row, so that the two values h needs meet in one warp (a
 // shuffle) instead of in shared memory.
@@ -302,7 +303,6 @@ __device__ __forceinline__ void tmem_ld_sum(uint32_t lane_addr, int c0, float* v
 // still in flight are waited for before the CTA frees its tensor memory and exits.
 constexpr int kPsProducers = 16;             // producer warps
 constexpr int kPsMmaWarp = 16, kPsPackWarp = 17, kPsBWarp = 18, kPsEpiWarp0 = 19;
-constexpr int kPsThreads = (kPsEpiWarp0 + 4) * 32;
 constexpr int kPsMaxPacked = 4;              // packed-row buffers (at least 2)
 constexpr int kPsMaxStages = 4;
 constexpr int kPsMaxAccs = 4;
@@ -321,6 +321,11 @@ struct PsCfg {
     static constexpr int kStageCols = kKS / 4;                // A columns per stage
     static constexpr int kStages = NT <= 16 ? 3 : 2;          // ring depth (shared memory)
     static constexpr int kAccs = 256 / kN < kPsMaxAccs ? 256 / kN : kPsMaxAccs;
+    // epilogue warps: one per tensor-memory lane quarter, two (taking alternate groups
+    // of 16 tokens) when a tile has several groups
+    static constexpr int kEpiWarps = NT >= 32 ? 8 : 4;
+    static constexpr int kEpiThreads = 32 * kEpiWarps;
+    static constexpr int kThreads = 32 * kPsEpiWarp0 + kEpiThreads;
     // instruction descriptor as in TileCfg: D fp32, A and B e4m3, both K-major, N, M = 128
     static constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
     static_assert(kRowBytesS == 4 * 16, "four producer parts of 16 bytes per stage row");
@@ -384,17 +389,18 @@ __device__ __forceinline__ bool ps_wait(uint64_t* bar, uint32_t parity, int* sta
     return ps_give_up(status, abort);
 }
 
-// Whether any of the 128 epilogue threads (named barrier 1) passes pred = true; all of
-// them must call it.
-__device__ __forceinline__ bool bar_any_128(bool pred) {
+// Whether any of the kThreads epilogue threads (named barrier 1) passes pred = true;
+// all of them must call it.
+template <int kThreads>
+__device__ __forceinline__ bool bar_any_epi(bool pred) {
     uint32_t r;
     asm volatile(
         "{\n.reg .pred p, q;\n"
         "setp.ne.u32 q, %1, 0;\n"
-        "bar.red.or.pred p, 1, 128, q;\n"
+        "bar.red.or.pred p, 1, %2, q;\n"
         "selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(r)
-        : "r"((uint32_t)pred)
+        : "r"((uint32_t)pred), "n"(kThreads)
         : "memory");
     return r != 0;
 }
@@ -409,7 +415,7 @@ __device__ __forceinline__ void ps_decode16(uint32_t packed_s, uint32_t row_off,
 }
 
 template <int NT, bool kDown>
-__global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int npk) {
+__global__ void __launch_bounds__(PsCfg<NT>::kThreads, 1) tc_stream_kernel(TcArgs a, int npk) {
     using Cfg = PsCfg<NT>;
     constexpr int S = Cfg::kStages, NACC = Cfg::kAccs;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -442,7 +448,7 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
             }
             for (int i = 0; i < NACC; ++i) {
                 mbar_init(&bars.acc_full[i], 1);
-                mbar_init(&bars.acc_empty[i], 128);
+                mbar_init(&bars.acc_empty[i], Cfg::kEpiThreads);
             }
             mbar_init(&bars.lut, 1);
             mbar_init(&bars.fin, 1);
@@ -504,7 +510,14 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
     } else if (warp == kPsMmaWarp) {
         // ---- MMA issue
         if (lane == 0) {
-            uint32_t g = 0;
+            // ring stage s and its phase ph; B descriptors step through the start-address
+            // field (shared addresses below 256 KB: no carry out of it)
+            int s = 0;
+            uint32_t ph = 0;
+            const uint64_t bdesc0 = smem_desc(smem_addr(bring), Cfg::kN * 16, 128);
+            constexpr uint64_t kQkStep = (uint64_t)((2 * Cfg::kN * 16) >> 4);
+            constexpr uint64_t kStStep = (uint64_t)(Cfg::kStageB >> 4);
+            const int nq_last = (Kdim - (NS - 1) * Cfg::kKS) / 32;
             bool ok = true;
             for (int it = 0; ok && (int)blockIdx.x + it * stride < n_items; ++it) {
                 const int acc = it % NACC;
@@ -513,28 +526,27 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
                     break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(kPsAccCol + acc * Cfg::kN);
-                for (int st = 0; st < NS; ++st, ++g) {
-                    const int s = (int)(g % S);
-                    if (!ps_wait_spin(&bars.full[s], (g / S) & 1, a.status, abort)) {
+                for (int st = 0; st < NS; ++st) {
+                    if (!ps_wait_spin(&bars.full[s], ph, a.status, abort)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t a0 = tmem + (uint32_t)(s * Cfg::kStageCols);
-                    const uint32_t b0 = smem_addr(bring + (size_t)s * Cfg::kStageB);
+                    const uint64_t bd = bdesc0 + (uint64_t)s * kStStep;
                     // only the K range the stage's copy filled (Kdim is a multiple of 32):
                     // the rest of a B stage may hold another tile's rows, whose padding
                     // rows are not guaranteed finite
-                    const int left = Kdim - st * Cfg::kKS;
-                    const int nq = (left < Cfg::kKS ? left : Cfg::kKS) / 32;
+                    const int nq = st == NS - 1 ? nq_last : Cfg::kKS / 32;
 #pragma unroll
-                    for (int qk = 0; qk < Cfg::kKS / 32; ++qk) {
-                        if (qk < nq) {
-                            const uint64_t bd = smem_desc(b0 + qk * 2 * (Cfg::kN * 16), Cfg::kN * 16, 128);
-                            mma_f8_tmem_a(d, a0 + 8 * qk, bd, Cfg::kIdesc, (st | qk) != 0 ? 1u : 0u);
-                        }
-                    }
+                    for (int qk = 0; qk < Cfg::kKS / 32; ++qk)
+                        if (qk < nq)
+                            mma_f8_tmem_a(d, a0 + 8 * qk, bd + qk * kQkStep, Cfg::kIdesc, (st | qk) != 0 ? 1u : 0u);
                     mma_commit(&bars.empty[s]);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
                 if (ok) mma_commit(&bars.acc_full[acc]);
             }
@@ -606,9 +618,11 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
         }
         __syncwarp();
     } else {
-        // ---- epilogue: TMEM lane quarter warp % 4, lane r of the item's 128
+        // ---- epilogue: TMEM lane quarter warp % 4, lane r of the item's 128; with eight
+        // epilogue warps the two of a quarter take alternate groups of 16 tokens
         pdl_wait();
         const int q = warp & 3, r = 32 * q + lane;
+        const int half = Cfg::kEpiWarps > 4 ? (warp - kPsEpiWarp0) >> 2 : 0;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
         const bool up_side = !kDown && (r & 1);
         // An item's per-item values are loaded one item ahead, so that their dependent
@@ -671,13 +685,13 @@ __global__ void __launch_bounds__(kPsThreads, 1) tc_stream_kernel(TcArgs a, int 
             const float row_scale_nxt = load_row_scale(it + 1, info_nxt);
             float2 tv_nxt[TPL];
             if (warp == kPsEpiWarp0) load_tokens(it + 1, info_nxt, tv_nxt);
-            // one decision for all 128 epilogue threads (they meet at a named barrier)
+            // one decision for all epilogue threads (they meet at a named barrier)
             const bool got = ps_wait(&bars.acc_full[acc], (uint32_t)((it / NACC) & 1), a.status, abort);
-            if (bar_any_128(!got)) break;
+            if (bar_any_epi<Cfg::kEpiThreads>(!got)) break;
             tc_fence_after();
             const uint32_t base = lane_addr + (uint32_t)(kPsAccCol + acc * Cfg::kN);
 #pragma unroll 1
-            for (int b = 0; b < NT / 16; ++b) {
+            for (int b = half; b < NT / 16; b += Cfg::kEpiWarps / 4) {
                 float v[16];
                 tmem_ld_sum<NT, 16>(base, 16 * b, v);
                 if (kDown) {
@@ -982,11 +996,11 @@ cudaError_t launch_tc_ffn_stream(const TcArgs& a, int S, cudaStream_t stream, in
     const int grid_dn = (int)(items_dn < sm_count ? items_dn : sm_count);
     err = launch_pdl(tc_gather_kernel<NT>, dim3(tiles, NT / kSplitRows), dim3(256), 0, stream, a);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(gu, dim3(grid_gu), dim3(kPsThreads), smem_gu, stream, a, npk_gu);
+    err = launch_pdl(gu, dim3(grid_gu), dim3(PsCfg<NT>::kThreads), smem_gu, stream, a, npk_gu);
     if (err != cudaSuccess) return err;
     err = launch_pdl(tc_split_h_kernel<NT>, dim3(tiles, NT / kSplitRows), dim3(256), 0, stream, a);
     if (err != cudaSuccess) return err;
-    return launch_pdl(dn, dim3(grid_dn), dim3(kPsThreads), smem_dn, stream, a, npk_dn);
+    return launch_pdl(dn, dim3(grid_dn), dim3(PsCfg<NT>::kThreads), smem_dn, stream, a, npk_dn);
 }
 
 }  // namespace
