@@ -16,15 +16,17 @@
 // distributed shared memory:
 //
 // Phase 0 (before the programmatic-dependent-launch wait, static inputs only): the
-//   decode table and this CTA's router rows (E / 16, one per warp) are bulk-copied
-//   into shared memory.
-// Phase 1: x is bulk-copied in; each CTA computes the logits of its router rows (the
-//   accumulation order of route_logits_kernel, so the logits are the same bits) and
-//   stores them into the logit array of every CTA of its cluster; cluster barrier.
+//   decode table is bulk-copied into shared memory and each warp loads one of this
+//   CTA's router rows (E / 16, one per warp) into registers.
+// Phase 1: x is read into shared memory (plain loads through L2); each CTA computes
+//   the logits of its router rows (the accumulation order of route_logits_kernel, so
+//   the logits are the same bits) and stores them into the logit array of every CTA of
+//   its cluster; cluster barrier.
 //   Every CTA now holds all E logits and selects the same top-k, so the clusters agree
 //   without talking to each other.
 // Phase 2: cluster c takes slot c < C whole: CTA rank r bulk-copies its I / 16 gate/up
-//   row pairs and its H / 16 down rows.  Each slot s >= C (when k > C) is split over the
+//   row pairs and its H / 16 down rows (and lays x out by lane columns while they are
+//   in flight).  Each slot s >= C (when k > C) is split over the
 //   clusters by ranges of the intermediate dimension: cluster c computes h only for
 //   its range of slot s, and the down product only over those columns, since
 //   down(h) is the sum of the down products over any split of h's columns.  Each CTA
@@ -63,6 +65,7 @@ constexpr int kLcUnit = 40;             // split granule: 8 gate/up rows = 8 dow
 constexpr int kLcMaxUnits = 4;          // units per cluster per split slot (32 down-row bytes)
 constexpr int kLcSplitCopyRows = 24;    // gate/up rows a CTA copies per split slot
 constexpr int kLcLutBytes = (int)sizeof(TritLut16);
+constexpr int kLcRouterChunks = 9;      // 16-byte router-row chunks per lane: H <= 2304
 static_assert(kLcThreads >= 2 * kLcMaxE && kLcThreads >= 4 * (kLcMaxE / 32) * kLcMaxK, "top-k thread plan");
 
 __host__ __device__ constexpr int align16(int v) { return (v + 15) / 16 * 16; }
@@ -110,8 +113,7 @@ __host__ __device__ inline void split_pairs(int n, int r, int& p0, int& p1, int&
     g0 = p0 / 8 * 8;
 }
 
-// Shared-memory plan (byte offsets).  The union region holds the router rows in
-// phases 0-1 and the expert rows after.
+// Shared-memory plan (byte offsets).  The expert rows go to the last region.
 struct LcSmem {
     int xb, xcol, hcol, hsp, lg, sh, un;
     int chunk_rows, chunk_bytes, dn, dn_bytes, sp, sp_gu_bytes, sp_bytes, total;
@@ -119,7 +121,6 @@ struct LcSmem {
 
 __host__ __device__ inline LcSmem lc_smem(int H, int I, int E, int MB) {
     const int Bh = (H + 4) / 5, Bi = (I + 4) / 5;
-    const int nr = (E + kCS - 1) / kCS;
     const int rg = I / kCS, rd = H / kCS;
     LcSmem L;
     int o = kLcLutBytes;
@@ -143,8 +144,7 @@ __host__ __device__ inline LcSmem lc_smem(int H, int I, int E, int MB) {
     L.sp = L.dn + L.dn_bytes;
     L.sp_gu_bytes = 2 * kLcSplitCopyRows * Bh + 8 * kLcSplitCopyRows;
     L.sp_bytes = L.sp_gu_bytes + L.dn_bytes;  // per split slot: gate/up groups, then down rows
-    const int router = nr * 2 * H, experts = L.sp + kLcMaxSplit * L.sp_bytes;
-    o += router > experts ? router : experts;
+    o += L.sp + kLcMaxSplit * L.sp_bytes;
     L.total = o;
     return L;
 }
@@ -180,11 +180,28 @@ __device__ __forceinline__ uint64_t sel_key(float v, int e) {
     return ((uint64_t)float_order_key(v + 0.0f) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
 }
 
+// Ranks each of the ncand candidate keys among all of them, kTpc threads per candidate
+// (kLcThreads / kTpc candidates at most), and stores the k best in s_sel in order.
+template <int kTpc>
+__device__ __forceinline__ void rank_candidates(const uint64_t* s_cand, uint64_t* s_sel, int ncand, int k, int tid) {
+    constexpr int kNj = kLcThreads / kTpc / kTpc;  // candidates a thread compares with
+    const int cand = tid / kTpc, sub = tid % kTpc;
+    const uint64_t K = cand < ncand ? s_cand[cand] : 0;
+    int rank = 0;
+#pragma unroll
+    for (int j = 0; j < kNj; ++j) {
+        const int jj = sub + kTpc * j;
+        if (jj < ncand) rank += s_cand[jj] > K ? 1 : 0;
+    }
+#pragma unroll
+    for (int o = kTpc / 2; o > 0; o >>= 1) rank += __shfl_xor_sync(kFullMask, rank, o);
+    if (cand < ncand && sub == 0 && rank < k) s_sel[rank] = K;
+}
+
 template <int MB>
 __global__ void __launch_bounds__(kLcThreads, 1) moe_layer_b1_kernel(LcArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ __align__(8) uint64_t bar_in;                // decode table + router rows
-    __shared__ __align__(8) uint64_t bar_x;                 // the token
     __shared__ __align__(8) uint64_t bar_gu[kLcChunks];     // gate/up chunk q of the whole slot
     __shared__ __align__(8) uint64_t bar_dn;                // its down rows + scales
     __shared__ __align__(8) uint64_t bar_sg[kLcMaxSplit];   // split slot: gate/up groups
@@ -209,7 +226,6 @@ __global__ void __launch_bounds__(kLcThreads, 1) moe_layer_b1_kernel(LcArgs a) {
     float* lg = reinterpret_cast<float*>(smem + L.lg);
     float* sh = reinterpret_cast<float*>(smem + L.sh);    // this CTA's h values
     unsigned char* un = smem + L.un;
-    const uint16_t* wr = reinterpret_cast<const uint16_t*>(un);  // phases 0-1
     const int e_lo = r * nr;
     const int nr_mine = E - e_lo < nr ? (E - e_lo > 0 ? E - e_lo : 0) : nr;
     const int hsp_stride = align16(I);
@@ -221,7 +237,6 @@ __global__ void __launch_bounds__(kLcThreads, 1) moe_layer_b1_kernel(LcArgs a) {
     if (tid == 0) {
         s_fail = 0;
         mbar_init_nofence(&bar_in, 1);
-        mbar_init_nofence(&bar_x, 1);
         for (int q = 0; q < kLcChunks; ++q) mbar_init_nofence(&bar_gu[q], 1);
         mbar_init_nofence(&bar_dn, 1);
         for (int s = 0; s < kLcMaxSplit; ++s) {
@@ -229,45 +244,49 @@ __global__ void __launch_bounds__(kLcThreads, 1) moe_layer_b1_kernel(LcArgs a) {
             mbar_init_nofence(&bar_sd[s], 1);
         }
         mbar_init_fence();
-        mbar_arrive_expect_tx(&bar_in, (uint32_t)(kLcLutBytes + nr_mine * 2 * H));
+        mbar_arrive_expect_tx(&bar_in, (uint32_t)kLcLutBytes);
         bulk_copy_g2s(&lut, &g_lut16_image, kLcLutBytes, &bar_in);
-        if (nr_mine > 0)
-            bulk_copy_g2s(un, a.Wr + (int64_t)e_lo * H, (uint32_t)(nr_mine * 2 * H), &bar_in);
+    }
+    // warp w's router row in registers, 16-byte chunk lane + 32 u in wv[u] (weights: no
+    // dependence on the previous kernel)
+    const int n8 = H >> 3;
+    uint4 wv[kLcRouterChunks];
+#pragma unroll
+    for (int u = 0; u < kLcRouterChunks; ++u) {
+        const int cc = lane + 32 * u;
+        wv[u] = warp < nr_mine && cc < n8 ? __ldg(reinterpret_cast<const uint4*>(a.Wr + (int64_t)(e_lo + warp) * H) + cc)
+                                         : make_uint4(0u, 0u, 0u, 0u);
     }
     pdl_wait();
     pdl_launch_dependents();
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&bar_x, 2u * H);
-        bulk_copy_g2s(xb, a.x, 2u * H, &bar_x);
-    }
-    __syncthreads();  // barriers initialised before anyone waits on them
-    if (!lc_wait(&bar_in, 0, a.status, a.wait_polls) || !lc_wait(&bar_x, 0, a.status, a.wait_polls))
-        s_fail = 1;
+    // the token (written by the previous kernel), 8 bytes per thread through L2
+    for (int i = tid; i < H / 4; i += kLcThreads)
+        reinterpret_cast<uint2*>(xb)[i] = __ldcg(reinterpret_cast<const uint2*>(a.x) + i);
+    __syncthreads();  // barriers initialised before anyone waits on them; x in place
+    if (!lc_wait(&bar_in, 0, a.status, a.wait_polls)) s_fail = 1;
     __syncthreads();
 
-    // ---- phase 1: this CTA's logits, into every CTA of the cluster; x for phase 2
+    // ---- phase 1: this CTA's logits, into every CTA of the cluster
     if (!s_fail) {
         const uint32_t lg_s = smem_addr(lg);
         if (warp < nr_mine) {  // warp w: router row w (the per-row order of route_logits_kernel)
             const int e = e_lo + warp;
-            const uint4* w4 = reinterpret_cast<const uint4*>(wr + warp * H);
             const uint4* x4 = reinterpret_cast<const uint4*>(xb);
-            const int n8 = H >> 3;
             float acc = 0.f;
-            for (int base = 0; base < n8; base += 32 * 8) {
+            {
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int cc = base + lane + 32 * u;
+                for (int u = 0; u < kLcRouterChunks; ++u) {
+                    const int cc = lane + 32 * u;
                     if (cc < n8) {
-                        const uint4 wv = w4[cc], xv = x4[cc];
-                        acc = fmaf(bf16_lo(wv.x), bf16_lo(xv.x), acc);
-                        acc = fmaf(bf16_hi(wv.x), bf16_hi(xv.x), acc);
-                        acc = fmaf(bf16_lo(wv.y), bf16_lo(xv.y), acc);
-                        acc = fmaf(bf16_hi(wv.y), bf16_hi(xv.y), acc);
-                        acc = fmaf(bf16_lo(wv.z), bf16_lo(xv.z), acc);
-                        acc = fmaf(bf16_hi(wv.z), bf16_hi(xv.z), acc);
-                        acc = fmaf(bf16_lo(wv.w), bf16_lo(xv.w), acc);
-                        acc = fmaf(bf16_hi(wv.w), bf16_hi(xv.w), acc);
+                        const uint4 xv = x4[cc];
+                        acc = fmaf(bf16_lo(wv[u].x), bf16_lo(xv.x), acc);
+                        acc = fmaf(bf16_hi(wv[u].x), bf16_hi(xv.x), acc);
+                        acc = fmaf(bf16_lo(wv[u].y), bf16_lo(xv.y), acc);
+                        acc = fmaf(bf16_hi(wv[u].y), bf16_hi(xv.y), acc);
+                        acc = fmaf(bf16_lo(wv[u].z), bf16_lo(xv.z), acc);
+                        acc = fmaf(bf16_hi(wv[u].z), bf16_hi(xv.z), acc);
+                        acc = fmaf(bf16_lo(wv[u].w), bf16_lo(xv.w), acc);
+                        acc = fmaf(bf16_hi(wv[u].w), bf16_hi(xv.w), acc);
                     }
                 }
             }
@@ -278,11 +297,6 @@ __global__ void __launch_bounds__(kLcThreads, 1) moe_layer_b1_kernel(LcArgs a) {
         }
         // entries past E rank last (in this CTA's own array only)
         for (int e = E + tid; e < kLcMaxE; e += kLcThreads) lg[e] = -INFINITY;
-        for (int i = tid; i < 32 * MB * 5; i += kLcThreads) {
-            const int l = i & 31, md = i >> 5, m = md / 5, d = md - 5 * m;
-            const int col = 5 * (l + 32 * m) + d;
-            xcol[i] = col < H ? bf16_bits_to_float(xb[col]) : 0.f;
-        }
     }
     cluster_sync();
 
@@ -305,20 +319,10 @@ __global__ void __launch_bounds__(kLcThreads, 1) moe_layer_b1_kernel(LcArgs a) {
             if (half == 0 && rank < k) s_cand[(i >> 5) * k + rank] = K;
         }
         __syncthreads();
-        {  // kLcThreads / ncand threads per candidate, each against a share of them
-            const int ncand = (kLcMaxE / 32) * k;
-            const int tpc = ncand <= 64 ? 8 : 4, cand = tid / tpc, sub = tid % tpc;
-            const uint64_t K = cand < ncand ? s_cand[cand] : 0;
-            const int nj = (ncand + tpc - 1) / tpc;
-            int rank = 0;
-#pragma unroll 8
-            for (int j = 0; j < nj; ++j) {
-                const int jj = sub + tpc * j;
-                if (jj < ncand) rank += s_cand[jj] > K ? 1 : 0;
-            }
-            for (int o = tpc / 2; o > 0; o >>= 1) rank += __shfl_xor_sync(kFullMask, rank, o);
-            if (cand < ncand && sub == 0 && rank < k) s_sel[rank] = K;
-        }
+        if ((kLcMaxE / 32) * k <= 64)
+            rank_candidates<8>(s_cand, s_sel, (kLcMaxE / 32) * k, k, tid);
+        else
+            rank_candidates<4>(s_cand, s_sel, (kLcMaxE / 32) * k, k, tid);
         __syncthreads();
         // the copies need only the selected ids (from the keys); the softmax weights are
         // first read after the h exchange, so the last warp forms them off the critical
@@ -338,10 +342,8 @@ __global__ void __launch_bounds__(kLcThreads, 1) moe_layer_b1_kernel(LcArgs a) {
                 }
             }
         }
-        // bulk copies, one issuing thread per group of barriers (lane 0 of warps 0..2+2S;
-        // every warp finished reading the router rows before the cluster barrier)
+        // bulk copies, one issuing thread per group of barriers (lane 0 of warps 0..2+2S)
         if (lane == 0 && warp < 3 + 2 * nsplit) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // router rows -> copies
             if (warp < 2) {  // whole slot: gate/up chunks 2w, 2w + 1
                 const int e = sel_id(c), cr = L.chunk_rows;
                 const uint32_t rows = (uint32_t)(cr * Bh);
@@ -385,6 +387,14 @@ __global__ void __launch_bounds__(kLcThreads, 1) moe_layer_b1_kernel(LcArgs a) {
             }
         }
         issued = true;
+        // x in lane-column order for the dot products (xcol[(5 m + d) 32 + l] = x[5 (l +
+        // 32 m) + d]), formed while the expert rows are in flight
+        for (int i = tid; i < 32 * MB * 5; i += kLcThreads) {
+            const int l = i & 31, md = i >> 5, m = md / 5, d = md - 5 * m;
+            const int col = 5 * (l + 32 * m) + d;
+            xcol[i] = col < H ? bf16_bits_to_float(xb[col]) : 0.f;
+        }
+        __syncthreads();
         // lane columns of x
         float2 x01[MB], x23[MB];
         float x4[MB];
@@ -585,7 +595,6 @@ __global__ void __launch_bounds__(kLcThreads, 1) moe_layer_b1_kernel(LcArgs a) {
     // ---- exit: the copies this CTA issued have landed
     if (tid == 0) {
         lc_wait(&bar_in, 0, nullptr, a.wait_polls);
-        lc_wait(&bar_x, 0, nullptr, a.wait_polls);
         if (issued) {
             for (int q = 0; q < kLcChunks; ++q) lc_wait(&bar_gu[q], 0, nullptr, a.wait_polls);
             lc_wait(&bar_dn, 0, nullptr, a.wait_polls);
@@ -715,8 +724,9 @@ size_t layer_b1_part_bytes(int k, int H) {
 
 bool layer_b1_supported(int H, int I, int E, int k, const DeviceInfo& dev) {
     const int Bh = (H + 4) / 5, Bi = (I + 4) / 5;
-    // down: H / 16 rows per CTA, at most 8 per warp
+    // down: H / 16 rows per CTA, at most 8 per warp; a router row in a warp's registers
     if (H % 8 != 0 || H % (kCS * kLcWarps) != 0 || H / kCS / kLcWarps > 8) return false;
+    if ((H / 8 + 31) / 32 > kLcRouterChunks) return false;
     const int rd = H / kCS;
     if ((rd * Bi) % 16 != 0 || ((int64_t)H * Bi) % 16 != 0 || (Bi + 31) / 32 > kLcMaxDownLaneBytes) return false;
     // gate/up: I / 16 row pairs per CTA in four chunks of 16-byte-aligned row groups, at

@@ -132,7 +132,6 @@ def layer_smem(H, I, E):
     """Offsets of the union region and inside it, and the total bytes."""
     Bh, Bi = nbytes(H), nbytes(I)
     MB = (Bh + 31) // 32
-    nr = (E + LC_CS - 1) // LC_CS
     rg, rd = I // LC_CS, H // LC_CS
     o = (LUT16_BYTES + _a16(2 * H) + 4 * 32 * MB * 5 + 4 * 32 * LC_MAX_DOWN_LANE_BYTES * 5
          + 4 * LC_MAX_SPLIT * _a16(I) + 4 * LC_MAX_E + 4 * (rg + LC_MAX_SPLIT * LC_CS))
@@ -144,7 +143,7 @@ def layer_smem(H, I, E):
     sp = dn + dn_bytes
     sp_gu = 2 * LC_SPLIT_COPY_ROWS * Bh + 8 * LC_SPLIT_COPY_ROWS
     sp_bytes = sp_gu + dn_bytes
-    total = un + max(nr * 2 * H, sp + LC_MAX_SPLIT * sp_bytes)
+    total = un + sp + LC_MAX_SPLIT * sp_bytes
     return dict(un=un, cr=cr, chunk=chunk, dn=dn, sp=sp, sp_gu=sp_gu, sp_bytes=sp_bytes, total=total)
 
 
@@ -187,18 +186,12 @@ def layer_transfers(E, H, I, k, C):
     un, total = L["un"], L["total"]
     C = min(k, C)
     nsplit = k - C
-    nr = (E + LC_CS - 1) // LC_CS
     rg, rd = I // LC_CS, H // LC_CS
     cr = L["cr"]
     for c in range(C):
         col0, col1 = split_range(I, C, c)
         for r in range(LC_CS):
             yield 0, LUT16_BYTES, LUT16_BYTES, "table", 0, total
-            e_lo = r * nr
-            n = max(0, min(nr, E - e_lo))
-            if n:
-                yield e_lo * H * 2, n * 2 * H, E * H * 2, "router rows", un, un + nr * 2 * H
-            yield 0, 2 * H, 2 * H, "x", LUT16_BYTES, LUT16_BYTES + _a16(2 * H)
             for e in (0, E - 1):
                 for q in range(LC_CHUNKS):
                     r0 = e * I + r * rg + q * cr
@@ -232,16 +225,16 @@ def layer_transfers(E, H, I, k, C):
 def test_fused_layer_plan_is_aligned_and_in_bounds():
     """Source and shared-memory destination of every copy 16-byte aligned, sizes multiples
     of 16, both inside their buffers, for cluster counts that take every slot whole
-    (C >= k) or split one or two slots; the router rows fit the union region; the copies
-    of one barrier stay below the 2^20 - 1 byte count."""
+    (C >= k) or split one or two slots; the copies of one barrier stay below the 2^20 - 1
+    byte count; a router row fits the 9 16-byte chunks per lane a warp holds in
+    registers."""
     checked = 0
     for H, I in [(2048, 512), (1024, 512), (2048, 256), (4096, 512), (2048, 768)]:
         for E, k in [(256, 8), (32, 8), (8, 8), (250, 3), (16, 9), (256, 1), (256, 16)]:
             for C in (7, 8, 6, 5, 16):
                 if k > E or not layer_ok(H, I, E, k, C):
                     continue
-                nr = (E + LC_CS - 1) // LC_CS
-                assert LUT16_BYTES + nr * 2 * H < 1 << 20
+                assert LUT16_BYTES < 1 << 20 and (H // 8 + 31) // 32 <= 9
                 for off, size, buf, what, dst, dst_end in layer_transfers(E, H, I, k, C):
                     _check(off, size, buf, f"layer H={H} I={I} E={E} k={k} C={C} {what}")
                     assert dst % 16 == 0 and dst + size <= dst_end, f"{what}: smem [{dst}, {dst + size})"
