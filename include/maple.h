@@ -279,8 +279,9 @@ MAPLE_API int maple_moe_layer(const uint16_t* x, const uint16_t* Wr, const float
  * maple_moe_layer, same arguments and results) and the copy y -> y_host, then returns.
  * y_host holds the result once the stream has synchronised.  Pinned host buffers
  * (cudaHostAlloc / cudaHostRegister, mapped: every pinned allocation is under unified
- * addressing) are copied by kernels that chain with the layer's kernels; other host
- * memory by asynchronous copies.
+ * addressing) are copied by kernels that chain with the layer's kernels (the fused
+ * single-token launch writes y_host itself, besides y); other host memory by
+ * asynchronous copies.
  * ("Maple-Preview ...", sections "The claim, verified from the bytes" and "The shipped
  * code does no quantization".)
  *   x_host : [T][H] bf16, host     x_dev : [T][H] bf16 device staging, 16-byte aligned

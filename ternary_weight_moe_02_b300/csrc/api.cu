@@ -363,13 +363,12 @@ int check_layer_args(const uint16_t* x, const uint16_t* Wr, const float* bias, c
     return MAPLE_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-int maple_moe_layer(const uint16_t* x, const uint16_t* Wr, const float* bias,
-                    const maple_experts* ex, int32_t T, int32_t k, float* logits, int32_t* idx,
-                    float* w, float* y, void* ws, size_t ws_bytes, void* stream) {
+// maple_moe_layer; y_mirror (may be null): where the fused single-token launch also
+// writes y, *mirrored telling whether it did (the two-call path does not).
+int moe_layer_impl(const uint16_t* x, const uint16_t* Wr, const float* bias, const maple_experts* ex, int32_t T,
+                   int32_t k, float* logits, int32_t* idx, float* w, float* y, void* ws, size_t ws_bytes,
+                   void* stream, float* y_mirror, bool* mirrored) {
+    *mirrored = false;
     if (int st = check_layer_args(x, Wr, bias, ex, T, k, logits, idx, w, y, ws, ws_bytes)) return st;
     if (T == 0) return ok();
     const int E = ex->E, H = ex->H, I = ex->I;
@@ -398,14 +397,27 @@ int maple_moe_layer(const uint16_t* x, const uint16_t* Wr, const float* bias,
         p.y = y;
         p.part = reinterpret_cast<float*>(base + 256);
         p.sync = reinterpret_cast<unsigned*>(base);
+        p.y_mirror = y_mirror;
         cudaError_t err = maple::launch_moe_layer_b1(p, (cudaStream_t)stream, dev);
         if (err != cudaSuccess) return cuda_fail(err, "moe_layer launch");
+        *mirrored = y_mirror != nullptr;
         return ok();
     }
     // general sizes: the two calls in sequence
     int st = maple_route_topk(x, Wr, bias, T, H, E, k, logits, idx, w, stream);
     if (st != MAPLE_OK) return st;
     return maple_moe_ffn(ex, x, idx, w, T, k, y, base + 256, ws_bytes - 256, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int maple_moe_layer(const uint16_t* x, const uint16_t* Wr, const float* bias,
+                    const maple_experts* ex, int32_t T, int32_t k, float* logits, int32_t* idx,
+                    float* w, float* y, void* ws, size_t ws_bytes, void* stream) {
+    bool mirrored = false;
+    return moe_layer_impl(x, Wr, bias, ex, T, k, logits, idx, w, y, ws, ws_bytes, stream, nullptr, &mirrored);
 }
 
 int maple_moe_layer_host(const uint16_t* x_host, uint16_t* x_dev, const uint16_t* Wr, const float* bias,
@@ -426,8 +438,12 @@ int maple_moe_layer_host(const uint16_t* x_host, uint16_t* x_dev, const uint16_t
     cudaError_t err = xm && ym ? maple::launch_io_copy(xm, x_dev, x_bytes, s, dev)
                    : cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, s);
     if (err != cudaSuccess) return cuda_fail(err, "moe_layer_host: copy x in");
-    const int st = maple_moe_layer(x_dev, Wr, bias, ex, T, k, logits, idx, w, y, ws, ws_bytes, stream);
+    // the fused single-token launch writes y to the mapped host buffer itself
+    bool mirrored = false;
+    const int st = moe_layer_impl(x_dev, Wr, bias, ex, T, k, logits, idx, w, y, ws, ws_bytes, stream,
+                                  xm && ym ? static_cast<float*>(ym) : nullptr, &mirrored);
     if (st != MAPLE_OK) return st;
+    if (mirrored) return ok();
     err = xm && ym ? maple::launch_io_copy(y, ym, y_bytes, s, dev)
                    : cudaMemcpyAsync(y_host, y, y_bytes, cudaMemcpyDeviceToHost, s);
     if (err != cudaSuccess) return cuda_fail(err, "moe_layer_host: copy y out");

@@ -149,6 +149,7 @@ struct LayerLaunch {
     float* y;
     float* part;     // [k][H] scratch (layer_b1_part_bytes)
     unsigned* sync;  // 16 combine counters, zero on entry and on exit
+    float* y_mirror = nullptr;  // optional second copy of y (a device address of mapped host memory)
 };
 // How many 16-CTA clusters of the fused kernel for (H, I, E) the current device runs
 // at once (0 if it cannot tell).

@@ -87,6 +87,7 @@ struct LcArgs {
     int32_t* idx;
     float* w;
     float* y;
+    float* y_mirror;   // null, or a second copy of y (e.g. mapped host memory)
     float* part;       // [C (1 + k - C)][H] per-slot (and per column range) contributions
     unsigned* counts;  // [kCS] combine counters: zero on entry, zero on exit
     int* status;
@@ -588,6 +589,7 @@ __global__ void __launch_bounds__(kLcThreads, 1) moe_layer_b1_kernel(LcArgs a) {
             for (int g = 0; g < kLcMaxK * (1 + kLcMaxSplit); ++g)
                 if (g < G) yv += v[g];
             a.y[r * rd + t] = yv;
+            if (a.y_mirror != nullptr) a.y_mirror[r * rd + t] = yv;
         }
         if (tid == 0) atomicExch(a.counts + r, 0u);
     }
@@ -777,6 +779,7 @@ cudaError_t launch_moe_layer_b1(const LayerLaunch& p, cudaStream_t stream, const
     a.idx = p.idx;
     a.w = p.w;
     a.y = p.y;
+    a.y_mirror = p.y_mirror;
     a.part = p.part;
     a.counts = p.sync;
     a.status = dev.status;

@@ -156,9 +156,10 @@ def test_layer_small_shapes_single_token():
 
 
 def test_layer_host_buffers_match_the_device_call(layer256):
-    """maple_moe_layer_host (token copied in from pinned host memory, y copied out)
-    gives the device call's results bit for bit, twice in a row; the bound form too, and
-    pageable host buffers."""
+    """maple_moe_layer_host (token copied in from pinned host memory; y written to it by
+    the fused launch, or copied out for pageable buffers) gives the device call's results
+    bit for bit, twice in a row, in y and in y_host; the bound form too, and pageable
+    host buffers."""
     from ternary_weight_moe_02_b300 import maple
     packed, ex, router = layer256
     ws = torch.zeros(maple.maple_moe_layer_workspace_size(1, 8, ex), dtype=torch.uint8, device="cuda")
@@ -170,10 +171,11 @@ def test_layer_host_buffers_match_the_device_call(layer256):
         x_dev = torch.empty_like(x)
         l2, i2, w2, y2 = (torch.empty_like(logits), torch.empty_like(idx), torch.empty_like(w),
                           torch.empty_like(y))
+        y2.fill_(float("nan"))
         maple.maple_moe_layer_host(x_host, x_dev, router, None, ex, 8, l2, i2, w2, y2, y_host, ws)
         torch.cuda.synchronize()
         assert torch.equal(logits, l2) and torch.equal(idx, i2) and torch.equal(w, w2)
-        assert torch.equal(y.cpu(), y_host)
+        assert torch.equal(y.cpu(), y_host) and torch.equal(y, y2)
         y_host.fill_(float("nan"))
         maple.bind_moe_layer_host(x_host, x_dev, router, None, ex, 8, l2, i2, w2, y2, y_host, ws)()
         torch.cuda.synchronize()
