@@ -387,8 +387,9 @@ def _layer_host_args(x_host, x_dev, Wr, bias, experts, k, logits, idx, w, y, y_h
 def maple_moe_layer_host(x_host, x_dev, Wr, bias, experts: Experts, k, logits, idx, w, y, y_host, ws,
                          stream=None):
     """maple_moe_layer with the tokens in host memory: x_host (bf16 [T,H]) is copied
-    into x_dev, the layer runs, and y is copied into y_host (fp32 [T,H]), all enqueued on
-    the stream; pinned host buffers are copied by kernels chained with the layer's."""
+    into x_dev, the layer runs, and y reaches y_host (fp32 [T,H]) as well, all enqueued
+    on the stream; pinned host buffers are copied by kernels chained with the layer's
+    (a single token's fused launch writes y_host itself)."""
     _check(_lib.maple_moe_layer_host(*_layer_host_args(x_host, x_dev, Wr, bias, experts, k, logits, idx, w,
                                                        y, y_host, ws, stream)), "maple_moe_layer_host")
 
