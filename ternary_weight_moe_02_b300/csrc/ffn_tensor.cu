@@ -475,37 +475,54 @@ __global__ void __launch_bounds__(PsCfg<NT>::kThreads, 1) tc_stream_kernel(TcArg
         auto wait_all = [&](uint64_t* bar, uint32_t parity) {
             return __all_sync(kFullMask, ps_wait(bar, parity, a.status, abort));
         };
-        auto pk_s = [&](int it) { return smem_addr(pk0 + (size_t)(it % npk) * pk_stride); };
         bool ok = wait_all(&bars.lut, 0) && wait_all(&bars.pk_full[0], 0);
-        int it = 0, st = 0;
-        uint32_t g = 0;
-        uint32_t cur[20], nxt[20];
-        if (ok) ps_decode16(pk_s(0), row_off, rb, 16 * part, lut_s, cur);
-        while (ok) {
-            const int s = (int)(g % S);
-            if (g >= (uint32_t)S && !wait_all(&bars.empty[s], ((g / S) - 1) & 1)) break;
+        // ring stage s of fill round `round` (its empty barrier is waited for from the
+        // second round on, parity (round - 1) & 1); packed-row buffer pk of the item and
+        // the parity of its full barrier; the decoded words alternate between wa and wb
+        int it = 0, st = 0, s = 0, round = 0, pk = 0;
+        uint32_t pk_ph = 0;
+        const uint32_t pk_base = smem_addr(pk0);
+        uint32_t pk_addr = pk_base;
+        uint32_t wa[20], wb[20];
+        if (ok) ps_decode16(pk_addr, row_off, rb, 16 * part, lut_s, wa);
+        // stores `cur` into stage s, decodes the next stage into `nxt`; false when this
+        // CTA has no further stage (or a wait gave up)
+        auto step = [&](const uint32_t* cur, uint32_t* nxt) {
+            if (round > 0 && !wait_all(&bars.empty[s], (uint32_t)((round - 1) & 1))) {
+                ok = false;
+                return false;
+            }
             const uint32_t col = (uint32_t)(s * Cfg::kStageCols + 20 * part);
             tmem_st16(lane_base + col, cur);
             tmem_st4(lane_base + col + 16, cur + 16);
             bool more = true;
             if (st + 1 < NS) {
                 ++st;
-                ps_decode16(pk_s(it), row_off, rb, Cfg::kRowBytesS * st + 16 * part, lut_s, nxt);
+                ps_decode16(pk_addr, row_off, rb, Cfg::kRowBytesS * st + 16 * part, lut_s, nxt);
             } else {
-                mbar_arrive(&bars.pk_empty[it % npk]);  // this item's packed rows are read
+                mbar_arrive(&bars.pk_empty[pk]);  // this item's packed rows are read
                 ++it;
                 st = 0;
+                if (++pk == npk) {
+                    pk = 0;
+                    pk_ph ^= 1u;
+                }
+                pk_addr = pk_base + (uint32_t)((size_t)pk * pk_stride);
                 more = (int)blockIdx.x + it * stride < n_items;
-                if (more && !wait_all(&bars.pk_full[it % npk], (uint32_t)((it / npk) & 1))) more = false;
-                if (more) ps_decode16(pk_s(it), row_off, rb, 16 * part, lut_s, nxt);
+                if (more && !wait_all(&bars.pk_full[pk], pk_ph)) more = false;
+                if (more) ps_decode16(pk_addr, row_off, rb, 16 * part, lut_s, nxt);
             }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             mbar_arrive(&bars.full[s]);
-            ++g;
-            if (!more) break;
-#pragma unroll
-            for (int i = 0; i < 20; ++i) cur[i] = nxt[i];
+            if (++s == S) {
+                s = 0;
+                ++round;
+            }
+            return more;
+        };
+        while (ok) {
+            if (!step(wa, wb) || !step(wb, wa)) break;
         }
     } else if (warp == kPsMmaWarp) {
         // ---- MMA issue
